@@ -1,0 +1,333 @@
+"""Pins of the fp64 oracle to things other than itself (CPU only).
+
+Each test fixes one function by a closed form, a hand-worked value, brute
+force on a tiny input, or a special case that reduces to a library routine,
+so that a dropped term, a wrong sign or index, or a transposed operand in the
+oracle fails here.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import runs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def _bf16_grid(shape, scale=1.0):
+    """Random float64 values that are exactly bf16 (via torch's own rounding)."""
+    x = torch.from_numpy(rng.standard_normal(shape) * scale).to(torch.bfloat16)
+    return x.to(torch.float64).numpy()
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+def test_bf16_rne_hand_cases():
+    one = 1.0
+    cases = {
+        one: one,
+        one + 2 ** -8: one,                        # tie -> even mantissa (0)
+        one + 3 * 2 ** -8: one + 2 ** -6,          # tie between odd 1+2^-7 and even 1+2^-6
+        one + 2 ** -8 + 2 ** -30: one + 2 ** -7,   # just above the tie
+        -(one + 2 ** -8): -one,
+        3.0 * 2 ** -20: 3.0 * 2 ** -20,
+        257.0: 256.0,                              # 257 needs 9 bits; tie -> 256
+        259.0: 260.0,
+    }
+    for x, want in cases.items():
+        assert oracle.round_bf16(np.array([x]))[0] == want, x
+
+
+def test_bf16_matches_library_rounding():
+    x32 = (rng.standard_normal(200000) * np.exp(rng.uniform(-20, 20, 200000))).astype(np.float32)
+    lib = torch.from_numpy(x32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = oracle.f64_to_bf16_bits(x32.astype(np.float64))
+    assert np.array_equal(lib, ours)
+    back = oracle.bf16_to_f64(ours)
+    assert np.array_equal(back, torch.from_numpy(x32).to(torch.bfloat16).double().numpy())
+
+
+def test_e4m3_all_codes_vs_library():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_value(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(lib)
+    assert set(np.nonzero(nan)[0]) == {0x7F, 0xFF}
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], lib[~nan])
+    # closed forms: largest normal, smallest normal, smallest subnormal
+    assert oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9
+    assert oracle.e4m3_value(0x38) == 1.0
+
+
+def test_e2m1_table():
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    vals = oracle.e2m1_value(np.arange(16))
+    assert list(vals[:8]) == mags
+    assert list(vals[8:]) == [-m for m in mags]
+
+
+def test_nvfp4_decode_layout():
+    # byte 0x21: low nibble code 1 (0.5) is element 0, high nibble code 2 (1.0) element 1
+    packed = np.zeros((1, 8), np.uint8)
+    packed[0, 0] = 0x21
+    packed[0, 7] = 0xF9            # element 14 = code 9 (-0.5), element 15 = code 15 (-6)
+    scale = np.array([[0x38]], np.uint8)   # 1.0
+    v = oracle.nvfp4_decode(packed, scale)
+    assert v.shape == (1, 16)
+    assert v[0, 0] == 0.5 and v[0, 1] == 1.0 and v[0, 14] == -0.5 and v[0, 15] == -6.0
+    assert np.all(v[0, 2:14] == 0)
+    # second group uses its own scale: 0x40 = 2.0
+    packed2 = np.full((1, 16), 0x77, np.uint8)
+    v2 = oracle.nvfp4_decode(packed2, np.array([[0x38, 0x40]], np.uint8))
+    assert np.all(v2[0, :16] == 6.0) and np.all(v2[0, 16:] == 12.0)
+
+
+def test_nvfp4_values_fit_bf16_exactly():
+    # every e2m1 x e4m3 product is a bf16 value (<= 6 significant bits, in range)
+    prod = np.outer(oracle.e2m1_value(np.arange(16)),
+                    oracle.e4m3_value(np.array([c for c in range(256) if c not in (0x7F, 0xFF)])))
+    assert np.array_equal(oracle.round_bf16(prod.ravel()), prod.ravel())
+
+
+# ---------------------------------------------------------------------------
+# pooling
+# ---------------------------------------------------------------------------
+def test_pool_weights_golden():
+    g = json.load(open(os.path.join(GOLDEN, "pool_hand.json")))
+    for c in g["cases"]:
+        a = oracle.pool_weights(np.array(c["gates"]))
+        np.testing.assert_allclose(a, c["weights"], rtol=0, atol=1e-15)
+    blk = g["block"]
+    Kc, Vc = oracle.pool_exact(np.array(blk["K_rows"]), np.array(blk["V_rows"]),
+                               np.array(blk["gates"]), 4)
+    np.testing.assert_allclose(Kc[0], blk["Kc"], atol=1e-14)
+    np.testing.assert_allclose(Vc[0], blk["Vc"], atol=1e-14)
+
+
+def test_pool_weights_invariants():
+    g = rng.standard_normal((1000, 128))
+    a = oracle.pool_weights(g)
+    np.testing.assert_allclose(a.sum(1), 1.0, atol=1e-15)
+    np.testing.assert_allclose(oracle.pool_weights(g + 7.25), a, atol=1e-15)
+    hot = oracle.pool_weights(np.array([100.0, 0.0, 0.0, 0.0]))
+    assert abs(hot[0] - 1.0) < 1e-40 + 1e-15 and hot[1] < 1e-43
+
+
+def test_pool_block_structure_and_tail():
+    T, D, m = 10, 3, 4
+    K = np.repeat(np.arange(T, dtype=np.float64)[:, None], D, axis=1)
+    V = -2.0 * K
+    Kc, Vc = oracle.pool_exact(K, V, np.zeros(T), m)
+    assert Kc.shape == (2, D)                          # tokens 8, 9 form no entry
+    np.testing.assert_allclose(Kc[:, 0], [1.5, 5.5])   # means of 0..3 and 4..7
+    np.testing.assert_allclose(Vc[:, 0], [-3.0, -11.0])
+    # weights follow the block's own gates, and K and V share them
+    gate = np.zeros(T)
+    gate[7] = math.log(5.0)
+    Kc, Vc = oracle.pool_exact(K, V, gate, m)
+    np.testing.assert_allclose(Kc[1, 0], (4 + 5 + 6) / 8 + 7 * 5 / 8)
+    np.testing.assert_allclose(Kc[0, 0], 1.5)
+    np.testing.assert_allclose(Vc[1, 0], -2 * Kc[1, 0])
+
+
+def test_pool_m1_is_identity_and_rounding():
+    K = _bf16_grid((50, 8))
+    V = _bf16_grid((50, 8))
+    Kc, Vc = oracle.pool(K, V, rng.standard_normal(50), 1)
+    assert np.array_equal(Kc, K) and np.array_equal(Vc, V)
+    K = _bf16_grid((64, 8))
+    g = rng.standard_normal(64)
+    ex, _ = oracle.pool_exact(K, K, g, 4)
+    st, _ = oracle.pool(K, K, g, 4)
+    assert np.array_equal(st, oracle.round_bf16(ex))
+    assert np.max(np.abs(st - ex)) <= np.max(np.abs(ex)) * 2 ** -8
+
+
+# ---------------------------------------------------------------------------
+# visibility
+# ---------------------------------------------------------------------------
+def test_visible_count_hand():
+    assert [oracle.visible_count(t, 4) for t in range(9)] == [0, 0, 0, 1, 1, 1, 1, 2, 2]
+    assert oracle.visible_count(126, 128) == 0 and oracle.visible_count(127, 128) == 1
+    assert oracle.visible_count(1048575, 128) == 8192
+    assert oracle.visible_count(10 ** 6, 4, n_valid=7) == 7
+
+
+@pytest.mark.parametrize("m", [1, 4, 128])
+def test_visible_means_block_complete(m):
+    # an entry is visible exactly when its last token is at or before the query
+    for t in range(0, 4 * m + 3):
+        v = oracle.visible_count(t, m)
+        for j in range(0, t // m + 3):
+            assert (j < v) == (j * m + m - 1 <= t)
+
+
+# ---------------------------------------------------------------------------
+# indexer and top-k
+# ---------------------------------------------------------------------------
+def test_index_scores_brute_force():
+    HI, DI, n = 3, 5, 17
+    qI, w, kI = rng.standard_normal((HI, DI)), rng.uniform(0, 1, HI), rng.standard_normal((n, DI))
+    s = oracle.index_scores(qI, w, kI)
+    for j in range(n):
+        want = 0.0
+        for h in range(HI):
+            dot = 0.0
+            for c in range(DI):
+                dot += qI[h][c] * kI[j][c]
+            want += w[h] * (dot if dot > 0 else 0.0)
+        assert abs(s[j] - want) < 1e-12
+
+
+def test_index_scores_one_hot_weight_and_relu():
+    qI, kI = rng.standard_normal((4, 8)), rng.standard_normal((30, 8))
+    for h in range(4):
+        w = np.zeros(4)
+        w[h] = 1.0
+        np.testing.assert_allclose(oracle.index_scores(qI, w, kI), np.maximum(kI @ qI[h], 0), atol=1e-13)
+    assert np.all(oracle.index_scores(qI, np.ones(4), -np.abs(kI) * 0) == 0)
+
+
+def test_topk_matches_full_sort_with_ties():
+    for n, k in [(50, 16), (7, 16), (200, 128), (0, 4), (16, 16)]:
+        s = rng.integers(0, 6, n).astype(np.float64)   # many exact ties
+        idx, kth = oracle.topk_select(s, k)
+        full = sorted(range(n), key=lambda j: (-s[j], j))[:k]
+        assert list(idx[idx >= 0]) == sorted(full)
+        assert np.all(idx[len(full):] == -1)
+        if n >= k:
+            assert kth == s[full[-1]]
+        else:
+            assert kth == -np.inf
+
+
+def test_topk_ties_go_to_lower_index():
+    s = np.zeros(40)
+    s[[5, 30]] = 1.0
+    idx, _ = oracle.topk_select(s, 4)
+    assert list(idx) == [0, 1, 5, 30]
+
+
+# ---------------------------------------------------------------------------
+# attention and merge
+# ---------------------------------------------------------------------------
+def test_attend_vs_library_sdpa():
+    H, D, n = 6, 16, 23
+    q, K, V = rng.standard_normal((H, D)), rng.standard_normal((n, D)), rng.standard_normal((n, D))
+    O, lse = oracle.attend(q, K, V, scale=0.3)
+    tq, tk, tv = (torch.from_numpy(x)[None] for x in (q, K, V))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, scale=0.3)[0].numpy()
+    np.testing.assert_allclose(O, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(torch.from_numpy(0.3 * q @ K.T), 1).numpy(), atol=1e-12)
+
+
+def test_attend_empty():
+    O, lse = oracle.attend(rng.standard_normal((4, 8)), np.zeros((0, 8)), np.zeros((0, 8)))
+    assert np.all(O == 0) and np.all(lse == -np.inf)
+
+
+def _causal_dense(q, K, V):
+    """Textbook causal attention through the library: softmax(QK^T + mask) V."""
+    T = K.shape[0]
+    mask = torch.full((T, T), -float("inf"), dtype=torch.float64).triu(1)
+    outs = []
+    for h in range(q.shape[1]):
+        z = torch.from_numpy(q[:, h] @ K.T) + mask
+        outs.append((torch.softmax(z, 1) @ torch.from_numpy(V)).numpy())
+    return np.stack(outs, 1)
+
+
+def test_hca_m1_no_window_equals_dense_causal():
+    T, H, D = 40, 3, 8
+    K, V, q = _bf16_grid((T, D)), _bf16_grid((T, D)), rng.standard_normal((T, H, D)) * 0.4
+    Kc, Vc = oracle.pool(K, V, rng.standard_normal(T), 1)
+    ref = _causal_dense(q, K, V)
+    for t in range(T):
+        r = runs.hca_branch(q[t], t, Kc, Vc, 1)
+        np.testing.assert_allclose(r["O"], ref[t], atol=1e-12)
+
+
+def test_swa_wide_window_equals_dense_causal():
+    T, H, D = 33, 2, 8
+    K, V, q = _bf16_grid((T, D)), _bf16_grid((T, D)), rng.standard_normal((T, H, D)) * 0.4
+    ref = _causal_dense(q, K, V)
+    for t in range(T):
+        r = runs.swa_branch(q[t], t, K, V, 0, W=T + 5)
+        np.testing.assert_allclose(r["O"], ref[t], atol=1e-12)
+    # a narrow window holds exactly positions t-W+1 .. t
+    assert list(oracle.window_positions(10, 4)) == [7, 8, 9, 10]
+    assert list(oracle.window_positions(2, 4)) == [0, 1, 2]
+    assert list(oracle.window_positions(10, 4, raw_pos0=9)) == [9, 10]
+
+
+def test_csa_with_large_k_equals_hca_m4():
+    T, H, D, HI, DI = 64, 2, 8, 2, 4
+    K, V = _bf16_grid((T, D)), _bf16_grid((T, D))
+    g = rng.standard_normal(T)
+    Kc, Vc = oracle.pool(K, V, g, 4)
+    kI = rng.standard_normal((T // 4, DI))
+    for t in range(T):
+        q = rng.standard_normal((H, D))
+        c = runs.csa_branch(q, t, rng.standard_normal((HI, DI)), rng.uniform(0, 1, HI), kI, Kc, Vc, 4, k=T)
+        h = runs.hca_branch(q, t, Kc, Vc, 4)
+        np.testing.assert_allclose(c["O"], h["O"], atol=1e-12)
+        np.testing.assert_allclose(c["lse"], h["lse"], atol=1e-12)
+        assert c["n_visible"] == h["n_visible"] == (t + 1) // 4
+
+
+def test_merge_equals_softmax_over_concatenation():
+    H, D = 4, 8
+    q = rng.standard_normal((H, D))
+    parts = [(rng.standard_normal((n, D)), rng.standard_normal((n, D))) for n in (5, 9, 3)]
+    res = [oracle.attend(q, Kp, Vp) for Kp, Vp in parts]
+    O, L = oracle.merge([r[0] for r in res], [r[1] for r in res])
+    Ocat, Lcat = oracle.attend(q, np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts]))
+    np.testing.assert_allclose(O, Ocat, atol=1e-12)
+    np.testing.assert_allclose(L, Lcat, atol=1e-12)
+
+
+def test_merge_with_empty_branches():
+    H, D = 3, 4
+    O1, L1 = rng.standard_normal((H, D)), rng.standard_normal(H)
+    O, L = oracle.merge([np.zeros((H, D)), O1], [np.full(H, -np.inf), L1])
+    np.testing.assert_allclose(O, O1, atol=1e-15)
+    np.testing.assert_allclose(L, L1, atol=1e-15)
+    O, L = oracle.merge([np.zeros((H, D)), np.zeros((H, D))], [np.full(H, -np.inf)] * 2)
+    assert np.all(O == 0) and np.all(L == -np.inf)
+
+
+def test_tiny_prefill_early_rows_have_empty_compressed_branches():
+    from datagen.workloads import TinyPrefill
+    cfg = TinyPrefill()
+    inp = {k: (v.view(torch.int16).numpy().view(np.uint16) if v.dtype == torch.bfloat16 else v.numpy())
+           for k, v in cfg.make().items()}
+    out = runs.tiny_prefill(inp, cfg, rows=[0, 2, 3, 127, 2047])
+    r = {x["t"]: x for x in out["rows"]}
+    for t in (0, 2):
+        assert np.all(r[t]["csa"]["lse"] == -np.inf) and np.all(r[t]["csa"]["idx"] == -1)
+        np.testing.assert_allclose(r[t]["csa_layer"][0], r[t]["swa"]["O"], atol=1e-15)
+    assert list(r[3]["csa"]["idx"][:2]) == [0, -1]
+    assert r[127]["hca"]["n_visible"] == 1 and r[127]["swa"]["n_keys"] == 32
+    assert r[2047]["csa"]["n_visible"] == 512 and np.all(r[2047]["csa"]["idx"] >= 0)
+
+
+def test_page_facts_match_workloads():
+    from datagen.workloads import CsaDecode, CsaPrefill, HcaDecode, PairDecode
+    f = json.load(open(os.path.join(GOLDEN, "pages_facts.json")))["facts"]
+    assert CsaPrefill().m == PairDecode().m_csa == f["csa_tokens_per_entry"]["value"]
+    assert HcaDecode().m == PairDecode().m_hca == f["hca_tokens_per_entry"]["value"]
+    assert abs(HcaDecode().N - f["hca_entries_at_1m_tokens_approx"]["value"]) / 8000 < 0.03
+    assert HcaDecode().ctx // HcaDecode().m == HcaDecode().N
+    assert PairDecode().m_hca // PairDecode().m_csa == f["hca_lighter_than_csa"]["value"]
+    for c in (CsaDecode(), CsaPrefill(), PairDecode()):
+        assert c.k == f["csa_topk_typical"]["value"] and c.W == f["window_tokens"]["value"]
