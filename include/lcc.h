@@ -1,0 +1,191 @@
+/*
+ * lcc.h -- C ABI of liblcc.so, the hybrid compressed-attention path
+ * (CSA + HCA + sliding window) for NVIDIA B300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *  [HYBRID] "DeepSeek-V4가 이차적 어텐션 비용 없이 백만 토큰 컨텍스트를 달성하는 방법"
+ *           (How DeepSeek-V4 reaches a million-token context without quadratic
+ *           attention cost), section "두 가지 압축 전략: CSA 및 HCA".
+ *  [VIDEO]  "딥시크 V4 분석: CSA·HCA 어텐션으로 100만 토큰 컨텍스트를 저비용에 구현한 방법",
+ *           sections "쉽게 이해하기" and "주요 인사이트".
+ *  [THREAD] "DeepSeek v4 (Flash)는 정말 운영 비용이 엄청나게 저렴한가요?", section "주요 댓글".
+ *  [V41]    DeepSeek V4.1 Flash post (jjy0501.blogspot.com), passages on the
+ *           lightning indexer / CSA2, FP4 KV storage and SWA Bounded Replay.
+ *
+ * Conventions shared by every call
+ *  - Tensors are row-major and contiguous unless a stride argument says
+ *    otherwise.  Element types: lcc_bf16 = raw bfloat16 bits, float = fp32.
+ *  - Every data pointer is a DEVICE pointer on the current CUDA device,
+ *    16-byte aligned, owned by the caller.  The library never allocates or
+ *    frees device memory and keeps no handles; scratch memory ("workspace")
+ *    is passed in by the caller, sized by the matching *_workspace call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *    validates its arguments on the host, enqueues its kernels on the stream
+ *    and returns without synchronising.
+ *  - Query i of batch b sits at absolute position q_pos0[b] + i.  Compressed
+ *    entry j (ratio m) covers positions j*m .. j*m+m-1 and is visible to the
+ *    query at position t iff j*m + m - 1 <= t and j < n_valid[b].  Raw row r
+ *    of batch b is position raw_pos0[b] + r.
+ *  - Attention outputs are fp32 O [B, Tq, H, D] (already normalised) and the
+ *    natural-log softmax normaliser lse [B, Tq, H]; an empty key set gives
+ *    O = 0 and lse = -inf.
+ *  - Errors: a non-LCC_OK status is returned before anything is enqueued
+ *    when an argument is invalid; lcc_last_error() then describes it
+ *    (thread-local).  Launch failures return LCC_ERR_CUDA.  Conditions found
+ *    on the device (an index out of range) set a device error word that
+ *    lcc_sync_status() reports.  No C++ exception crosses this interface.
+ */
+#ifndef LCC_H_
+#define LCC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lcc_bf16;
+
+typedef enum {
+  LCC_OK = 0,
+  LCC_ERR_ARG = 1,          /* null pointer or invalid value */
+  LCC_ERR_SHAPE = 2,        /* unsupported or inconsistent size */
+  LCC_ERR_ALIGN = 3,        /* pointer or stride not 16-byte aligned */
+  LCC_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
+  LCC_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+  LCC_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up */
+  LCC_ERR_DEVICE = 7,       /* a kernel found invalid data (see lcc_last_error) */
+  LCC_ERR_WORKSPACE = 8     /* workspace missing or too small */
+} lcc_status;
+
+typedef enum { LCC_KEY_BF16 = 0, LCC_KEY_NVFP4 = 1 } lcc_key_format;
+
+/* ---------------------------------------------------------------------- *
+ * Compression: softmax-weighted pooling of m consecutive tokens' K and V
+ * into one compressed entry.  [HYBRID]: CSA merges 4 consecutive tokens,
+ * HCA 128 tokens, into one KV entry by softmax-weighted pooling; [VIDEO]
+ * "쉽게 이해하기": each token's contribution is learned.
+ *
+ * For every batch b and block j < n_blocks, with a_i = softmax over the
+ * block's m gate logits:
+ *   Kc[b, j, :] = bf16_rne( sum_i a_i * K[b, j*m + i, :] )   (same for V)
+ * K, V:   token rows of D bf16; row r of batch b at K + b*kv_bstride + r*D.
+ *         Pass a pointer offset to the block's first token to pool a
+ *         sub-range (e.g. one freshly completed block of a decode buffer).
+ * gate:   one fp32 logit per token; token r of batch b at gate + b*gate_bstride + r.
+ * Kc, Vc: entry j of batch b at Kc + b*c_bstride + j*D.
+ * D in {64, 128}; kv_bstride, c_bstride multiples of 8 elements.
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_csa_compress(const lcc_bf16* K, const lcc_bf16* V, const float* gate,
+                            int B, int n_blocks, int D,
+                            int64_t kv_bstride, int64_t gate_bstride,
+                            lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
+                            void* stream);                      /* m = 4 */
+lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* gate,
+                            int B, int n_blocks, int D,
+                            int64_t kv_bstride, int64_t gate_bstride,
+                            lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
+                            void* stream);                      /* m = 128 */
+
+/* ---------------------------------------------------------------------- *
+ * Lightning indexer + top-k.  [HYBRID]: a light indexer running in FP4
+ * scores the compressed entries against the query and keeps the top-k
+ * (typically about 128) for the expensive attention; [THREAD] "주요 댓글":
+ * it picks the likely-relevant candidates before full attention.
+ *
+ * Score of visible entry j for query (b, i) at position t:
+ *   s = sum_h w[b,i,h] * max(0, qI[b,i,h,:] . kI[b,j,:])
+ * idx[b,i,:] receives the min(k, visible) entries with the largest s, ties
+ * to the lower index, in ascending index order, padded with -1.  score (if
+ * not NULL) receives their scores (fp32, -inf for padding).
+ *
+ * qI:  [B, Tq, HI, DI] bf16; w: [B, Tq, HI] fp32.
+ * kI:  LCC_KEY_BF16:  [B, Ncap, DI] bf16, kI_scale unused (NULL);
+ *      LCC_KEY_NVFP4: [B, Ncap, DI/2] uint8 e2m1 pairs (element 2c in the
+ *      low nibble of byte c) and kI_scale [B, Ncap, DI/16] uint8 e4m3, one
+ *      scale per 16 consecutive elements.  ([V41]: keys kept in FP4.)
+ * q_pos0, n_valid: device arrays [B] (int64, int32).
+ * HI in {4, 8}; DI in {32, 64} (NVFP4: DI = 64); 1 <= k <= 1024; Ncap >= 1.
+ * workspace: at least lcc_index_topk_workspace(B, Tq, Ncap, k) bytes.
+ * With NVFP4 keys the indexer queries are rounded to fp16 for the tensor-
+ * core product (exact for 2^-14 <= |qI| <= 65504).
+ * ---------------------------------------------------------------------- */
+size_t lcc_index_topk_workspace(int B, int Tq, int Ncap, int k);
+lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w,
+                                    int B, int Tq, int HI, int DI,
+                                    const int64_t* q_pos0,
+                                    lcc_key_format fmt, const void* kI, const uint8_t* kI_scale,
+                                    const int32_t* n_valid, int Ncap, int m, int k,
+                                    int32_t* idx, float* score,
+                                    void* workspace, size_t workspace_bytes,
+                                    void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * CSA sparse attention: MQA (all H heads share one K/V row, [HYBRID]) over
+ * the k entries idx[b,i,:] of the compressed cache; entries < 0 are skipped.
+ *   z_h,j = scale * q[b,i,h,:] . Kc[b,idx_j,:];  lse = log sum_j e^z;
+ *   O[b,i,h,:] = sum_j softmax(z)_j Vc[b,idx_j,:]
+ * q: [B, Tq, H, D] bf16; Kc, Vc: [B, Ncap, D] bf16 with rows kv_rstride
+ * elements apart (D for separate tensors, 2*D when K and V rows interleave);
+ * idx: [B, Tq, k] int32, each entry in [-1, Ncap).  H in {8, 16, ..., 128},
+ * D in {64, 128}, 1 <= k <= 4096.
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_csa_sparse_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                               const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                               const int32_t* idx, int k,
+                               float* O, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * HCA dense attention over every visible compressed entry ([HYBRID]: dense
+ * attention over the ~8000 entries a 1M-token context leaves at m=128).
+ * Keys of query (b, i): entries j < min(n_valid[b], (q_pos0[b]+i+1)/m).
+ * Layouts as lcc_csa_sparse_attn.  Decode-sized calls split the key range
+ * across CTAs and need lcc_dense_attn_workspace(...) bytes of workspace.
+ * ---------------------------------------------------------------------- */
+size_t lcc_dense_attn_workspace(int B, int Tq, int H, int D, int Ncap);
+lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                              const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* n_valid, int m,
+                              float* O, float* lse,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Sliding-window attention over raw tokens ([HYBRID]: a window branch runs
+ * in parallel to keep local detail; [VIDEO]: the most recent 128 tokens).
+ * Keys of the query at position t: positions max(0, t-W+1) .. t that the raw
+ * buffer holds, i.e. rows r = p - raw_pos0[b] with 0 <= r < Rcap.
+ * Kr, Vr: [B, Rcap, D] bf16 (rows kv_rstride apart).  1 <= W <= 4096.
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                        const int64_t* q_pos0,
+                        const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t kv_rstride, int Rcap,
+                        const int64_t* raw_pos0, int W,
+                        float* O, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Branch merge by log-sum-exp: with L = log sum_b exp(lse_b),
+ *   out = sum_b exp(lse_b - L) * O_b  (bf16, round to nearest even),
+ *   lse_out = L (optional).
+ * Equal to one softmax over the union of the branches' key lists.
+ * O_parts / lse_parts: HOST arrays of nb device pointers, each [rows, D] /
+ * [rows] fp32, rows = B*Tq*H.  2 <= nb <= 4.  out_f32 (optional, may be
+ * NULL) receives the fp32 result as well.
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_attn_merge(int nb, const float* const* O_parts, const float* const* lse_parts,
+                          int64_t rows, int D,
+                          lcc_bf16* out, float* out_f32, float* lse_out, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Utilities.
+ * ---------------------------------------------------------------------- */
+const char* lcc_last_error(void);          /* thread-local text of the last failure */
+const char* lcc_version(void);
+/* Synchronise `stream`, then report (and clear) the device error word. */
+lcc_status lcc_sync_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCC_H_ */

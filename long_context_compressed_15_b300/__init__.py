@@ -1,0 +1,297 @@
+"""Python binding of liblcc.so, the B300 hybrid compressed-attention library.
+
+Argument marshalling only: every function checks shapes, dtypes and
+devices of torch tensors, passes their device pointers and the current CUDA
+stream to the C function of the same name (``lcc_<name>`` in include/lcc.h)
+and raises :class:`LccError` on a non-OK status.  All computation happens
+in the library's CUDA kernels; there is no fallback path -- importing works
+without a GPU, but every call needs the built ``liblcc.so`` and a CUDA
+device.  PyTorch supplies device memory (outputs and workspace are
+allocated here when the caller does not pass them) and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk",
+    "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
+    "swa_attn", "attn_merge", "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
+]
+
+KEY_BF16, KEY_NVFP4 = 0, 1
+_STATUS = {0: "OK", 1: "ERR_ARG", 2: "ERR_SHAPE", 3: "ERR_ALIGN", 4: "ERR_UNSUPPORTED",
+           5: "ERR_CUDA", 6: "ERR_TIMEOUT", 7: "ERR_DEVICE", 8: "ERR_WORKSPACE"}
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblcc.so")
+
+_lib = None
+_P, _I, _L, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+# name -> argument types (return type is int status unless listed in _RET)
+_SIGS = {
+    "lcc_csa_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
+    "lcc_hca_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
+    "lcc_index_topk_workspace": [_I, _I, _I, _I],
+    "lcc_lightning_index_topk": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
+    "lcc_csa_sparse_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _L, _I, _P, _I, _P, _P, _P],
+    "lcc_dense_attn_workspace": [_I, _I, _I, _I, _I],
+    "lcc_hca_dense_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P, _Z, _P],
+    "lcc_swa_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P],
+    "lcc_attn_merge": [_I, _P, _P, _L, _I, _P, _P, _P, _P],
+    "lcc_last_error": [],
+    "lcc_version": [],
+    "lcc_sync_status": [_P],
+}
+_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z,
+        "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p}
+
+
+class LccError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn}: {_STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load liblcc.so (once).  Raises if the library has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"liblcc.so not found at {p}: build it with "
+                           "`python -m long_context_compressed_15_b300.build`")
+    lib = ctypes.CDLL(p)
+    for name, args in _SIGS.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = _RET.get(name, ctypes.c_int)
+    _lib = lib
+    return lib
+
+
+def last_error() -> str:
+    return load().lcc_last_error().decode()
+
+
+def _call(name, *args):
+    lib = load()
+    st = getattr(lib, name)(*args)
+    if st != 0:
+        raise LccError(name, st, lib.lcc_last_error().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _need(t, dtype, name, dim=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got shape {tuple(t.shape)}")
+
+
+def _rows(t, name):
+    """[B, R, D] with unit element stride and contiguous rows; returns (batch stride, row stride)."""
+    if t.stride(2) != 1:
+        raise ValueError(f"{name}: last dim must be contiguous")
+    return t.stride(0), t.stride(1)
+
+
+def _positions(x, B, device, dtype=torch.int64):
+    if isinstance(x, torch.Tensor):
+        _need(x, dtype, "positions")
+        return x
+    return torch.full((B,), int(x), dtype=dtype, device=device)
+
+
+# ---------------------------------------------------------------------------
+# compression
+# ---------------------------------------------------------------------------
+def _compress(fname, m, K, V, gate, Kc, Vc, n_blocks, stream):
+    for t, n in ((K, "K"), (V, "V"), (Kc, "Kc"), (Vc, "Vc")):
+        _need(t, torch.bfloat16, n, 3)
+    _need(gate, torch.float32, "gate", 2)
+    B, R, D = K.shape
+    kv_bs, kv_rs = _rows(K, "K")
+    if kv_rs != D or V.stride() != K.stride() or gate.stride(1) != 1:
+        raise ValueError("K/V rows must be contiguous with identical strides; gate contiguous per batch")
+    c_bs, c_rs = _rows(Kc, "Kc")
+    if c_rs != D or Vc.stride() != Kc.stride():
+        raise ValueError("Kc/Vc rows must be contiguous with identical strides")
+    n_blocks = R // m if n_blocks is None else int(n_blocks)
+    if n_blocks > Kc.shape[1] or n_blocks * m > R:
+        raise ValueError("n_blocks exceeds the input rows or the output entries")
+    _call(fname, _ptr(K), _ptr(V), _ptr(gate), B, n_blocks, D, kv_bs, gate.stride(0),
+          _ptr(Kc), _ptr(Vc), c_bs, _stream(stream))
+    return Kc, Vc
+
+
+def csa_compress(K, V, gate, Kc, Vc, n_blocks=None, stream=None):
+    """Pool every 4 tokens of K/V [B, R, D] into entries of Kc/Vc [B, N, D]."""
+    return _compress("lcc_csa_compress", 4, K, V, gate, Kc, Vc, n_blocks, stream)
+
+
+def hca_compress(K, V, gate, Kc, Vc, n_blocks=None, stream=None):
+    """Pool every 128 tokens of K/V [B, R, D] into entries of Kc/Vc [B, N, D]."""
+    return _compress("lcc_hca_compress", 128, K, V, gate, Kc, Vc, n_blocks, stream)
+
+
+# ---------------------------------------------------------------------------
+# lightning indexer + top-k
+# ---------------------------------------------------------------------------
+def index_topk_workspace(B, Tq, Ncap, k) -> int:
+    return int(load().lcc_index_topk_workspace(B, Tq, Ncap, k))
+
+
+def lightning_index_topk(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None, idx=None, score=None,
+                         workspace=None, stream=None):
+    """Top-k compressed entries per query by the ReLU-weighted indexer score.
+
+    qI [B, Tq, HI, DI] bf16; w [B, Tq, HI] fp32; kI [B, Ncap, DI] bf16, or
+    NVFP4 packed uint8 [B, Ncap, DI/2] with kI_scale uint8 [B, Ncap, DI/16];
+    q_pos0 / n_valid: int or [B] device tensors.  Returns idx [B, Tq, k] int32
+    (and writes score [B, Tq, k] fp32 if given).
+    """
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    B, Tq, HI, DI = qI.shape
+    if not (qI.is_contiguous() and w.is_contiguous() and kI.is_contiguous()):
+        raise ValueError("qI, w and kI must be contiguous")
+    if kI.dtype == torch.uint8:
+        fmt = KEY_NVFP4
+        _need(kI_scale, torch.uint8, "kI_scale", 3)
+        if not kI_scale.is_contiguous():
+            raise ValueError("kI_scale must be contiguous")
+    else:
+        fmt = KEY_BF16
+        _need(kI, torch.bfloat16, "kI", 3)
+    Ncap = kI.shape[1]
+    dev = qI.device
+    q_pos0 = _positions(q_pos0, B, dev)
+    n_valid = _positions(n_valid, B, dev, torch.int32)
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=dev)
+    _need(idx, torch.int32, "idx", 3)
+    if score is not None:
+        _need(score, torch.float32, "score", 3)
+    need = index_topk_workspace(B, Tq, Ncap, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _call("lcc_lightning_index_topk", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
+          _ptr(kI_scale), _ptr(n_valid), Ncap, int(m), int(k), _ptr(idx), _ptr(score),
+          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return idx
+
+
+# ---------------------------------------------------------------------------
+# attention branches
+# ---------------------------------------------------------------------------
+def _attn_out(q, O, lse):
+    B, Tq, H, D = q.shape
+    if O is None:
+        O = torch.empty((B, Tq, H, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Tq, H), dtype=torch.float32, device=q.device)
+    _need(O, torch.float32, "O", 4)
+    _need(lse, torch.float32, "lse", 3)
+    if not (O.is_contiguous() and lse.is_contiguous() and q.is_contiguous()):
+        raise ValueError("q, O and lse must be contiguous")
+    return O, lse
+
+
+def _kv(Kc, Vc):
+    _need(Kc, torch.bfloat16, "K", 3)
+    _need(Vc, torch.bfloat16, "V", 3)
+    bs, rs = _rows(Kc, "K")
+    if (bs, rs) != _rows(Vc, "V") or bs != Kc.shape[1] * rs:
+        raise ValueError("K and V must share strides, with batch stride = rows * row stride")
+    return rs
+
+
+def csa_sparse_attn(q, Kc, Vc, idx, scale=1.0, O=None, lse=None, stream=None):
+    """MQA over the idx-selected compressed entries; returns (O, lse)."""
+    _need(q, torch.bfloat16, "q", 4)
+    _need(idx, torch.int32, "idx", 3)
+    B, Tq, H, D = q.shape
+    rs = _kv(Kc, Vc)
+    O, lse = _attn_out(q, O, lse)
+    _call("lcc_csa_sparse_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(Kc), _ptr(Vc), rs, Kc.shape[1],
+          _ptr(idx.contiguous()), idx.shape[2], _ptr(O), _ptr(lse), _stream(stream))
+    return O, lse
+
+
+def dense_attn_workspace(B, Tq, H, D, Ncap) -> int:
+    return int(load().lcc_dense_attn_workspace(B, Tq, H, D, Ncap))
+
+
+def hca_dense_attn(q, Kc, Vc, q_pos0, n_valid, m, scale=1.0, O=None, lse=None, workspace=None, stream=None):
+    """MQA over every compressed entry visible at each query; returns (O, lse)."""
+    _need(q, torch.bfloat16, "q", 4)
+    B, Tq, H, D = q.shape
+    rs = _kv(Kc, Vc)
+    O, lse = _attn_out(q, O, lse)
+    q_pos0 = _positions(q_pos0, B, q.device)
+    n_valid = _positions(n_valid, B, q.device, torch.int32)
+    need = dense_attn_workspace(B, Tq, H, D, Kc.shape[1])
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _call("lcc_hca_dense_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(q_pos0), _ptr(Kc), _ptr(Vc), rs,
+          Kc.shape[1], _ptr(n_valid), int(m), _ptr(O), _ptr(lse), _ptr(workspace), nbytes, _stream(stream))
+    return O, lse
+
+
+def swa_attn(q, Kr, Vr, q_pos0, raw_pos0, W, scale=1.0, O=None, lse=None, stream=None):
+    """MQA over the raw tokens of each query's window; returns (O, lse)."""
+    _need(q, torch.bfloat16, "q", 4)
+    B, Tq, H, D = q.shape
+    rs = _kv(Kr, Vr)
+    O, lse = _attn_out(q, O, lse)
+    q_pos0 = _positions(q_pos0, B, q.device)
+    raw_pos0 = _positions(raw_pos0, B, q.device)
+    _call("lcc_swa_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(q_pos0), _ptr(Kr), _ptr(Vr), rs,
+          Kr.shape[1], _ptr(raw_pos0), int(W), _ptr(O), _ptr(lse), _stream(stream))
+    return O, lse
+
+
+def attn_merge(parts, out=None, out_f32=None, lse_out=None, stream=None):
+    """Log-sum-exp merge of [(O, lse), ...] (O [..., D] fp32, lse [...] fp32) -> bf16 out."""
+    Os = [p[0] for p in parts]
+    Ls = [p[1] for p in parts]
+    for o, l in zip(Os, Ls):
+        _need(o, torch.float32, "O part")
+        _need(l, torch.float32, "lse part")
+        if not (o.is_contiguous() and l.is_contiguous()):
+            raise ValueError("parts must be contiguous")
+    D = Os[0].shape[-1]
+    rows = Os[0].numel() // D
+    if out is None:
+        out = torch.empty(Os[0].shape, dtype=torch.bfloat16, device=Os[0].device)
+    nb = len(parts)
+    Oarr = (ctypes.c_void_p * nb)(*[o.data_ptr() for o in Os])
+    Larr = (ctypes.c_void_p * nb)(*[l.data_ptr() for l in Ls])
+    _call("lcc_attn_merge", nb, ctypes.cast(Oarr, ctypes.c_void_p), ctypes.cast(Larr, ctypes.c_void_p), rows, D,
+          _ptr(out), _ptr(out_f32), _ptr(lse_out), _stream(stream))
+    return out
+
+
+def sync_status(stream=None):
+    """Synchronise the stream and raise if a kernel recorded a device-side error."""
+    _call("lcc_sync_status", _stream(stream))

@@ -1,0 +1,116 @@
+// Log-sum-exp combination of attention partials: the branch merge of a
+// layer (window + CSA sparse, or window + HCA dense) and the reduction of
+// key-range splits of one branch.  Both compute, per row,
+//   L = log sum_b exp(lse_b),  O = sum_b exp(lse_b - L) O_b,
+// which equals one softmax over the union of the partials' key sets
+// ("DeepSeek-V4가 이차적 어텐션 비용 없이 ...", section "두 가지 압축 전략: CSA 및 HCA":
+// the window branch runs in parallel with the compressed one).
+#pragma once
+#include "common.cuh"
+
+namespace lcc {
+
+struct MergeArgs {
+  const float* O[4];
+  const float* lse[4];
+  int nb;
+  int64_t rows;
+  int D;
+  bf16* out;       // nullable
+  float* out_f32;  // nullable
+  float* lse_out;  // nullable
+};
+
+// One warp per row; lane owns D/32 consecutive floats.
+template <int D>
+__global__ void __launch_bounds__(256) k_merge(MergeArgs a) {
+  constexpr int PER = D / 32;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= a.rows) return;
+  float l[4];
+  float L = -INFINITY;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    l[b] = b < a.nb ? __ldg(a.lse[b] + row) : -INFINITY;
+    L = fmaxf(L, l[b]);
+  }
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float tot = 0.f;
+  if (L != -INFINITY) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      if (b >= a.nb || l[b] == -INFINITY) continue;
+      const float w = expf(l[b] - L);
+      tot += w;
+      const float* src = a.O[b] + row * D + lane * PER;
+      if constexpr (PER == 4) {
+        float4 v = __ldg(reinterpret_cast<const float4*>(src));
+        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        float2 v = __ldg(reinterpret_cast<const float2*>(src));
+        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
+  }
+  const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] *= inv;
+  if (a.out) {
+    bf16* dst = a.out + row * D + lane * PER;
+    if constexpr (PER == 4) {
+      uint2 o;
+      o.x = pack_bf16(acc[0], acc[1]);
+      o.y = pack_bf16(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(dst) = o;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    }
+  }
+  if (a.out_f32) {
+    float* dst = a.out_f32 + row * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) dst[e] = acc[e];
+  }
+  if (a.lse_out && lane == 0) a.lse_out[row] = (L == -INFINITY) ? -INFINITY : L + logf(tot);
+}
+
+// Reduction of `nsplit` key-range partials stored [nsplit][rows][D] and
+// [nsplit][rows] into O [rows][D] and lse [rows].
+template <int D>
+__global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__ Op, const float* __restrict__ lp,
+                                                       int nsplit, int64_t rows, float* __restrict__ O,
+                                                       float* __restrict__ lse) {
+  constexpr int PER = D / 32;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float L = -INFINITY;
+  for (int s = lane; s < nsplit; s += 32) L = fmaxf(L, __ldg(lp + s * rows + row));
+  L = warp_max(L);
+  float acc[PER];
+#pragma unroll
+  for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+  float tot = 0.f;
+  if (L != -INFINITY) {
+    for (int s = 0; s < nsplit; ++s) {
+      const float ls = __ldg(lp + s * rows + row);
+      if (ls == -INFINITY) continue;
+      const float w = expf(ls - L);
+      tot += w;
+      const float* src = Op + (s * rows + row) * D + lane * PER;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, __ldg(src + e), acc[e]);
+    }
+  }
+  const float inv = tot > 0.f ? 1.0f / tot : 0.f;
+  float* dst = O + row * D + lane * PER;
+#pragma unroll
+  for (int e = 0; e < PER; ++e) dst[e] = acc[e] * inv;
+  if (lane == 0) lse[row] = (L == -INFINITY) ? -INFINITY : L + logf(tot);
+}
+
+}  // namespace lcc

@@ -1,0 +1,95 @@
+"""The C ABI on the host (CPU only): the library loads, exports every function
+include/lcc.h declares, and rejects invalid arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import long_context_compressed_15_b300 as lcc
+from long_context_compressed_15_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return lcc.load()
+
+
+def declared_functions():
+    names = set()
+    for h in HEADERS:
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"\b(lcc_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for f in ("lcc_csa_compress", "lcc_hca_compress", "lcc_lightning_index_topk", "lcc_csa_sparse_attn",
+              "lcc_hca_dense_attn", "lcc_swa_attn", "lcc_attn_merge", "lcc_last_error", "lcc_sync_status"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.lcc_version().decode().startswith("lcc")
+
+
+def test_binding_covers_every_function(lib):
+    for name in declared_functions():
+        assert name in lcc._SIGS, name
+
+
+def status(call):
+    return int(call)
+
+
+def test_null_and_shape_errors_are_reported_on_host(lib):
+    P = ctypes.c_void_p
+    # null K
+    st = lib.lcc_csa_compress(None, P(16), P(16), 1, 1, 128, 0, 0, P(16), P(16), 0, None)
+    assert st == 1 and "null" in lcc.last_error()
+    # unsupported D
+    st = lib.lcc_hca_compress(P(16), P(16), P(16), 1, 1, 96, 0, 0, P(16), P(16), 0, None)
+    assert st == 2 and "D=96" in lcc.last_error()
+    # misaligned K
+    st = lib.lcc_csa_compress(P(18), P(16), P(16), 1, 1, 128, 0, 0, P(16), P(16), 0, None)
+    assert st == 3
+    # empty work is a no-op success
+    assert lib.lcc_csa_compress(None, None, None, 0, 5, 128, 0, 0, None, None, 0, None) == 0
+    # indexer: bad head count, bad k, missing workspace
+    args = [P(16), P(16), 1, 1, 6, 64, P(16), 0, P(16), None, P(16), 1024, 4, 128, P(16), None, None, 0, None]
+    assert lib.lcc_lightning_index_topk(*args) == 2
+    args[4] = 8
+    args[13] = 5000
+    assert lib.lcc_lightning_index_topk(*args) == 2
+    args[13] = 128
+    assert lib.lcc_lightning_index_topk(*args) == 8 and "workspace" in lcc.last_error()
+    # NVFP4 keys need their scales
+    args[7] = 1
+    assert lib.lcc_lightning_index_topk(*args) == 1
+    # attention: head count not a multiple of 8
+    st = lib.lcc_csa_sparse_attn(P(16), 1, 1, 12, 128, 1.0, P(16), P(16), 128, 10, P(16), 4, P(16), P(16), None)
+    assert st == 2
+    st = lib.lcc_swa_attn(P(16), 1, 1, 64, 128, 1.0, P(16), P(16), P(16), 128, 10, P(16), 0, P(16), P(16), None)
+    assert st == 2 and "W=0" in lcc.last_error()
+    # merge: too many parts
+    assert lib.lcc_attn_merge(5, None, None, 10, 128, None, None, None, None) == 1
+
+
+def test_workspace_sizes(lib):
+    assert lcc.index_topk_workspace(32, 1, 16384, 128) >= 32 * 16384 * 4
+    # two-stage top-k needs candidate lists
+    big = lcc.index_topk_workspace(4, 1, 262160, 128)
+    assert big >= 4 * 262160 * 4 + 4 * 33 * 128 * 8
+    # prefill scores are processed in bounded query chunks
+    assert lcc.index_topk_workspace(1, 131072, 32768, 128) <= (1 << 28) * 4 + (1 << 26)
+    assert lcc.dense_attn_workspace(8, 1, 64, 128, 8192) > 0      # decode splits the key range
+    assert lcc.dense_attn_workspace(1, 32768, 64, 128, 8448) == 0  # prefill needs none

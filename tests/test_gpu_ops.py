@@ -1,0 +1,280 @@
+"""Per-call parity of the CUDA path (through the C ABI) against the fp64
+oracle, at sizes the oracle finishes in seconds that still span several
+tiles, ragged tails and the method's degenerate cases."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import long_context_compressed_15_b300 as lcc
+import oracle
+from oracle import runs
+from parity import assert_close, assert_lse_close, bits, check_topk_rows, host
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lcc.load()
+
+
+def f64(t):
+    return runs.f64(host(t))
+
+
+# ---------------------------------------------------------------------------
+# compression
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("m,D,R", [(4, 128, 4 * 37 + 3), (4, 64, 4 * 300 + 1), (128, 128, 128 * 3 + 50),
+                                   (128, 64, 128 * 2)])
+def test_compress_parity(m, D, R):
+    B = 3
+    K = datagen.normal_bf16(11, 1, (B, R, D))
+    V = datagen.normal_bf16(11, 2, (B, R, D))
+    g = datagen.normal_f32(11, 3, (B, R))
+    n = R // m
+    Kc = torch.full((B, n + 2, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.full_like(Kc, float("nan"))
+    fn = lcc.csa_compress if m == 4 else lcc.hca_compress
+    fn(K.to(DEV), V.to(DEV), g.to(DEV), Kc, Vc)
+    torch.cuda.synchronize()
+    for b in range(B):
+        ex_k, ex_v = oracle.pool_exact(f64(K[b]), f64(V[b]), f64(g[b]), m)
+        st_k, st_v = oracle.pool(f64(K[b]), f64(V[b]), f64(g[b]), m)
+        for gpu, ex, st in ((Kc[b, :n], ex_k, st_k), (Vc[b, :n], ex_v, st_v)):
+            gv = f64(gpu)
+            ulp = np.ldexp(1.0, np.frexp(np.abs(ex))[1] - 8)
+            assert np.all(np.abs(gv - ex) <= ulp), "pooled entry off by more than one bf16 ulp"
+            assert np.mean(gv == st) > 0.99
+        # entries past the last complete block are untouched
+        assert torch.isnan(Kc[b, n:].float()).all()
+
+
+def test_compress_one_block_at_offset():
+    # a decode step pools one freshly completed block from the middle of a raw buffer
+    B, R, D = 2, 40, 128
+    K = datagen.normal_bf16(12, 1, (B, R, D))
+    V = datagen.normal_bf16(12, 2, (B, R, D))
+    g = datagen.normal_f32(12, 3, (B, R))
+    Kc = torch.zeros((B, 10, D), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.zeros_like(Kc)
+    Kd, Vd, gd = K.to(DEV), V.to(DEV), g.to(DEV)
+    lcc.csa_compress(Kd[:, 20:], Vd[:, 20:], gd[:, 20:], Kc[:, 7:], Vc[:, 7:], n_blocks=1)
+    torch.cuda.synchronize()
+    for b in range(B):
+        st_k, st_v = oracle.pool(f64(K[b, 20:24]), f64(V[b, 20:24]), f64(g[b, 20:24]), 4)
+        assert np.max(np.abs(f64(Kc[b, 7]) - st_k[0])) <= np.max(np.abs(st_k)) * 2 ** -7
+        assert torch.count_nonzero(Kc[b, :7].float()) == 0 and torch.count_nonzero(Kc[b, 8:].float()) == 0
+
+
+# ---------------------------------------------------------------------------
+# lightning indexer + top-k
+# ---------------------------------------------------------------------------
+def _index_case(seed, B, Tq, HI, DI, Ncap, m, k, q_pos0, n_valid, nvfp4=False):
+    qI = datagen.normal_bf16(seed, 5, (B, Tq, HI, DI))
+    w = datagen.uniform_f32(seed, 6, (B, Tq, HI))
+    if nvfp4:
+        kp, ks = datagen.nvfp4_normal(seed, 7, B * Ncap, DI)
+        kp, ks = kp.reshape(B, Ncap, DI // 2), ks.reshape(B, Ncap, DI // 16)
+        kI_host = oracle.nvfp4_decode(kp.numpy(), ks.numpy())
+        idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), torch.tensor(q_pos0, device=DEV),
+                                       kp.to(DEV), torch.tensor(n_valid, dtype=torch.int32, device=DEV),
+                                       m, k, kI_scale=ks.to(DEV))
+    else:
+        kI = datagen.normal_bf16(seed, 7, (B, Ncap, DI))
+        kI_host = f64(kI)
+        idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), torch.tensor(q_pos0, device=DEV), kI.to(DEV),
+                                       torch.tensor(n_valid, dtype=torch.int32, device=DEV), m, k)
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    g = idx.cpu().numpy()
+    near = 0
+    for b in range(B):
+        rows = []
+        for i in range(Tq):
+            nv = oracle.visible_count(q_pos0[b] + i, m, min(n_valid[b], Ncap))
+            s = oracle.index_scores(f64(qI[b, i]), f64(w[b, i]), kI_host[b, :nv])
+            oi, kth = oracle.topk_select(s, k)
+            rows.append(dict(idx=oi, scores=s, kth=kth))
+        near += check_topk_rows(g[b], rows, k, what=f"batch {b}")
+    return near, g
+
+
+@pytest.mark.parametrize("HI,DI", [(8, 64), (4, 32), (8, 32), (4, 64)])
+def test_index_topk_decode_two_stage(HI, DI):
+    # Ncap > one top-k segment: exercises the per-segment lists and their merge; ragged n_valid
+    B, Ncap = 3, 20000
+    near, g = _index_case(21, B, 1, HI, DI, Ncap, 4, 128, q_pos0=[4 * Ncap - 1] * B, n_valid=[Ncap, 8193, 100])
+    assert np.all(g[2, 0, 100:] == -1) and np.all(g[2, 0, :100] == np.arange(100))
+    assert near <= 1
+
+
+def test_index_topk_prefill_causal_with_ties():
+    # 4 heads: about 1 in 16 entries scores exactly 0 (all four ReLUs vanish); early
+    # queries see fewer than k entries and must be padded
+    near, g = _index_case(22, 1, 700, 4, 32, 175, 4, 16, q_pos0=[0], n_valid=[175])
+    assert np.all(g[0, :3] == -1)
+    assert list(g[0, 3, :2]) == [0, -1]
+    assert near <= 2
+
+
+def test_index_topk_zero_score_ties_bit_exact():
+    # weights of zero make every score 0: the top-k must be the lowest indices
+    B, Ncap, k = 2, 3000, 64
+    qI = datagen.normal_bf16(23, 5, (B, 1, 8, 64)).to(DEV)
+    w = torch.zeros((B, 1, 8), dtype=torch.float32, device=DEV)
+    kI = datagen.normal_bf16(23, 7, (B, Ncap, 64)).to(DEV)
+    idx = lcc.lightning_index_topk(qI, w, 4 * Ncap, kI, Ncap, 4, k)
+    torch.cuda.synchronize()
+    assert torch.equal(idx.cpu(), torch.arange(k, dtype=torch.int32).expand(B, 1, k))
+
+
+def test_index_topk_nvfp4_keys():
+    B, Ncap = 2, 9000
+    near, _ = _index_case(24, B, 2, 8, 64, Ncap, 4, 128, q_pos0=[4 * Ncap - 2] * B, n_valid=[Ncap, 5000],
+                          nvfp4=True)
+    assert near <= 1
+
+
+def test_index_topk_scores_output():
+    B, Ncap, k = 1, 500, 32
+    qI = datagen.normal_bf16(25, 5, (B, 1, 8, 64))
+    w = datagen.uniform_f32(25, 6, (B, 1, 8))
+    kI = datagen.normal_bf16(25, 7, (B, Ncap, 64))
+    sc = torch.empty((B, 1, k), dtype=torch.float32, device=DEV)
+    idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), 4 * Ncap, kI.to(DEV), Ncap, 4, k, score=sc)
+    torch.cuda.synchronize()
+    s = oracle.index_scores(f64(qI[0, 0]), f64(w[0, 0]), f64(kI[0]))
+    ids = idx[0, 0].cpu().numpy()
+    np.testing.assert_allclose(sc[0, 0].cpu().numpy(), s[ids], rtol=1e-5, atol=1e-5)
+
+
+# ---------------------------------------------------------------------------
+# attention branches
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,D,k", [(64, 128, 128), (8, 64, 16), (16, 128, 40), (128, 64, 70)])
+def test_sparse_attn_parity(H, D, k):
+    B, Tq, Ncap = 2, 5, 300
+    q = datagen.normal_bf16(31, 4, (B, Tq, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(31, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(31, 9, (B, Ncap, D))
+    vis = torch.tensor([Ncap, 3, 0, k, 200] * B)[: B * Tq]
+    idx = datagen.random_index_lists(31, 17, vis, k).reshape(B, Tq, k)
+    O, lse = lcc.csa_sparse_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV), idx.to(DEV))
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    for b in range(B):
+        for i in range(Tq):
+            sel = idx[b, i].numpy()
+            sel = sel[sel >= 0]
+            Oo, Lo = oracle.attend(f64(q[b, i]), f64(Kc[b])[sel], f64(Vc[b])[sel])
+            assert_close(O[b, i].cpu().numpy(), Oo, f"O[{b},{i}]")
+            assert_lse_close(lse[b, i].cpu().numpy(), Lo, f"lse[{b},{i}]")
+
+
+def test_sparse_attn_rejects_out_of_range_index():
+    B, Tq, H, D, Ncap, k = 1, 1, 64, 128, 50, 8
+    q = torch.zeros((B, Tq, H, D), dtype=torch.bfloat16, device=DEV)
+    Kc = torch.zeros((B, Ncap, D), dtype=torch.bfloat16, device=DEV)
+    idx = torch.tensor([[[0, 1, 2, 77, -1, -1, -1, -1]]], dtype=torch.int32, device=DEV)
+    lcc.csa_sparse_attn(q, Kc, Kc, idx)
+    with pytest.raises(lcc.LccError) as e:
+        lcc.sync_status()
+    assert e.value.status == 7
+    lcc.sync_status()  # the error word is cleared once reported
+
+
+@pytest.mark.parametrize("m,H,D", [(4, 8, 64), (128, 64, 128)])
+def test_dense_attn_prefill_parity(m, H, D):
+    T = 4 * m + 9
+    q = datagen.normal_bf16(32, 4, (1, T, H, D), scale=D ** -0.5)
+    K = datagen.normal_bf16(32, 1, (1, T, D))
+    V = datagen.normal_bf16(32, 2, (1, T, D))
+    g = datagen.normal_f32(32, 3, (1, T))
+    n = T // m
+    Kc = torch.zeros((1, n, D), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.zeros_like(Kc)
+    (lcc.csa_compress if m == 4 else lcc.hca_compress)(K.to(DEV), V.to(DEV), g.to(DEV), Kc, Vc)
+    O, lse = lcc.hca_dense_attn(q.to(DEV), Kc, Vc, 0, n, m)
+    torch.cuda.synchronize()
+    Kh, Vh = f64(Kc[0]), f64(Vc[0])   # attention parity on the kernel's own pooled entries is
+    Ko, Vo = oracle.pool(f64(K[0]), f64(V[0]), f64(g[0]), m)   # ... checked against the oracle's pooling too
+    assert np.max(np.abs(Kh - Ko)) <= 2 ** -6 * max(1.0, np.max(np.abs(Ko)))
+    for t in range(T):
+        r = runs.hca_branch(f64(q[0, t]), t, Ko, Vo, m)
+        assert_close(O[0, t].cpu().numpy(), r["O"], f"O[{t}]")
+        assert_lse_close(lse[0, t].cpu().numpy(), r["lse"], f"lse[{t}]")
+
+
+def test_dense_attn_decode_split_ragged():
+    B, H, D, Ncap, m = 3, 64, 128, 1000, 128
+    q = datagen.normal_bf16(33, 4, (B, 1, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(33, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(33, 9, (B, Ncap, D))
+    n_valid = [Ncap, 37, 0]
+    pos = m * Ncap + 5
+    O, lse = lcc.hca_dense_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV), pos,
+                                torch.tensor(n_valid, dtype=torch.int32, device=DEV), m)
+    torch.cuda.synchronize()
+    for b in range(B):
+        r = runs.hca_branch(f64(q[b, 0]), pos, f64(Kc[b]), f64(Vc[b]), m, n_valid=n_valid[b])
+        assert_close(O[b, 0].cpu().numpy(), r["O"], f"O[{b}]")
+        assert_lse_close(lse[b, 0].cpu().numpy(), r["lse"], f"lse[{b}]")
+
+
+@pytest.mark.parametrize("W,H,D", [(32, 8, 64), (128, 64, 128), (100, 16, 128)])
+def test_swa_prefill_parity(W, H, D):
+    T = 300
+    q = datagen.normal_bf16(34, 4, (1, T, H, D), scale=D ** -0.5)
+    K = datagen.normal_bf16(34, 1, (1, T, D))
+    V = datagen.normal_bf16(34, 2, (1, T, D))
+    O, lse = lcc.swa_attn(q.to(DEV), K.to(DEV), V.to(DEV), 0, 0, W)
+    torch.cuda.synchronize()
+    for t in range(T):
+        r = runs.swa_branch(f64(q[0, t]), t, f64(K[0]), f64(V[0]), 0, W)
+        assert_close(O[0, t].cpu().numpy(), r["O"], f"O[{t}]")
+        assert_lse_close(lse[0, t].cpu().numpy(), r["lse"], f"lse[{t}]")
+
+
+def test_swa_decode_buffer_offsets():
+    # raw buffers that start after position 0 and hold only part of some windows
+    B, H, D, W, R = 3, 64, 128, 128, 150
+    q = datagen.normal_bf16(35, 4, (B, 2, H, D), scale=D ** -0.5)
+    Kr = datagen.normal_bf16(35, 1, (B, R, D))
+    Vr = datagen.normal_bf16(35, 2, (B, R, D))
+    raw0 = [1000, 1060, 900]
+    qpos = [1000 + 127, 1100, 900 + 149 - 1]
+    O, lse = lcc.swa_attn(q.to(DEV), Kr.to(DEV), Vr.to(DEV), torch.tensor(qpos, device=DEV),
+                          torch.tensor(raw0, device=DEV), W)
+    torch.cuda.synchronize()
+    for b in range(B):
+        for i in range(2):
+            r = runs.swa_branch(f64(q[b, i]), qpos[b] + i, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
+            assert_close(O[b, i].cpu().numpy(), r["O"], f"O[{b},{i}]")
+            assert_lse_close(lse[b, i].cpu().numpy(), r["lse"], f"lse[{b},{i}]")
+
+
+@pytest.mark.parametrize("nb,D", [(2, 128), (3, 64), (4, 128)])
+def test_merge_parity(nb, D):
+    rows = 777
+    parts = []
+    for p in range(nb):
+        O = torch.randn((rows, D), generator=torch.Generator().manual_seed(p), dtype=torch.float32)
+        L = torch.randn((rows,), generator=torch.Generator().manual_seed(100 + p), dtype=torch.float32) * 3
+        L[p::nb] = -float("inf")     # empty branches
+        parts.append((O, L))
+    L_all_empty = list(range(0, rows, 97))
+    for p in range(nb):
+        parts[p][1][L_all_empty] = -float("inf")
+    out_f32 = torch.empty((rows, D), dtype=torch.float32, device=DEV)
+    lse_out = torch.empty((rows,), dtype=torch.float32, device=DEV)
+    out = lcc.attn_merge([(o.to(DEV), l.to(DEV)) for o, l in parts], out_f32=out_f32, lse_out=lse_out)
+    torch.cuda.synchronize()
+    Oo, Lo = oracle.merge([o.double().numpy() for o, _ in parts],
+                          [l.double().numpy() for _, l in parts])
+    assert_close(out_f32.cpu().numpy(), Oo, "merge f32", max_abs=1e-5, mean_abs=1e-6)
+    assert_close(out.float().cpu().numpy(), Oo, "merge bf16")
+    assert_lse_close(lse_out.cpu().numpy(), Lo, "merge lse", tol=1e-5)
+    assert np.all(out_f32.cpu().numpy()[L_all_empty] == 0)
