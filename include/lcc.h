@@ -121,6 +121,16 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w,
                                     void* workspace, size_t workspace_bytes,
                                     void* stream);
 
+/* Indexer scores only: scores[b, i, j] = s for every visible entry j of
+ * query (b, i) (entries past the visible count are left untouched).
+ * scores: [B, Tq, Ncap] fp32.  Other arguments as lcc_lightning_index_topk. */
+lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w,
+                                      int B, int Tq, int HI, int DI,
+                                      const int64_t* q_pos0,
+                                      lcc_key_format fmt, const void* kI, const uint8_t* kI_scale,
+                                      const int32_t* n_valid, int Ncap, int m,
+                                      float* scores, void* stream);
+
 /* ---------------------------------------------------------------------- *
  * CSA sparse attention: MQA (all H heads share one K/V row, [HYBRID]) over
  * the k entries idx[b,i,:] of the compressed cache; entries < 0 are skipped.
@@ -182,6 +192,9 @@ lcc_status lcc_attn_merge(int nb, const float* const* O_parts, const float* cons
  * ---------------------------------------------------------------------- */
 const char* lcc_last_error(void);          /* thread-local text of the last failure */
 const char* lcc_version(void);
+/* Number of kernels this library has enqueued since it was loaded (all
+ * devices and streams; a launch captured into a CUDA graph counts once). */
+uint64_t lcc_launch_count(void);
 /* Synchronise `stream`, then report (and clear) the device error word. */
 lcc_status lcc_sync_status(void* stream);
 

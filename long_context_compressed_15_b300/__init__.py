@@ -17,7 +17,7 @@ import os
 import torch
 
 __all__ = [
-    "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk",
+    "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk", "lightning_index_scores",
     "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
     "swa_attn", "attn_merge", "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
 ]
@@ -36,6 +36,7 @@ _SIGS = {
     "lcc_hca_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
     "lcc_index_topk_workspace": [_I, _I, _I, _I],
     "lcc_lightning_index_topk": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
+    "lcc_lightning_index_scores": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P, _P],
     "lcc_csa_sparse_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _L, _I, _P, _I, _P, _P, _P],
     "lcc_dense_attn_workspace": [_I, _I, _I, _I, _I],
     "lcc_hca_dense_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P, _Z, _P],
@@ -44,9 +45,10 @@ _SIGS = {
     "lcc_last_error": [],
     "lcc_version": [],
     "lcc_sync_status": [_P],
+    "lcc_launch_count": [],
 }
 _RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z,
-        "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p}
+        "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p, "lcc_launch_count": ctypes.c_uint64}
 
 
 class LccError(RuntimeError):
@@ -71,6 +73,11 @@ def load(path: str | None = None):
         f.restype = _RET.get(name, ctypes.c_int)
     _lib = lib
     return lib
+
+
+def launch_count() -> int:
+    """Kernels enqueued by the library so far (graph captures count once)."""
+    return int(load().lcc_launch_count())
 
 
 def last_error() -> str:
@@ -198,6 +205,23 @@ def lightning_index_topk(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None, idx=No
           _ptr(kI_scale), _ptr(n_valid), Ncap, int(m), int(k), _ptr(idx), _ptr(score),
           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     return idx
+
+
+def lightning_index_scores(qI, w, q_pos0, kI, n_valid, m, kI_scale=None, scores=None, stream=None):
+    """Indexer scores of every visible entry: scores [B, Tq, Ncap] fp32 (others untouched)."""
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    B, Tq, HI, DI = qI.shape
+    fmt = KEY_NVFP4 if kI.dtype == torch.uint8 else KEY_BF16
+    Ncap = kI.shape[1]
+    q_pos0 = _positions(q_pos0, B, qI.device)
+    n_valid = _positions(n_valid, B, qI.device, torch.int32)
+    if scores is None:
+        scores = torch.full((B, Tq, Ncap), float("nan"), dtype=torch.float32, device=qI.device)
+    _need(scores, torch.float32, "scores", 3)
+    _call("lcc_lightning_index_scores", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
+          _ptr(kI_scale), _ptr(n_valid), Ncap, int(m), _ptr(scores), _stream(stream))
+    return scores
 
 
 # ---------------------------------------------------------------------------

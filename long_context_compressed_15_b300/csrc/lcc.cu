@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -34,7 +35,10 @@ lcc_status fail(lcc_status s, const char* fmt, ...) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+std::atomic<unsigned long long> g_launches{0};
+
 lcc_status launch_check(const char* what) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(LCC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return LCC_OK;
@@ -140,6 +144,7 @@ extern "C" {
 
 const char* lcc_last_error(void) { return t_last_error.c_str(); }
 const char* lcc_version(void) { return "lcc 0.1 (sm_103a)"; }
+uint64_t lcc_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 lcc_status lcc_sync_status(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
@@ -169,6 +174,50 @@ lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* g
 
 size_t lcc_index_topk_workspace(int B, int Tq, int Ncap, int k) { return index_ws(B, Tq, Ncap, k).total; }
 
+}  // extern "C"
+
+namespace {
+lcc_status check_index_args(const char* name, const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                            const int64_t* q_pos0, lcc_key_format fmt, const void* kI, const uint8_t* kI_scale,
+                            const int32_t* n_valid, int Ncap, int m, const void* out) {
+  if (!qI || !w || !q_pos0 || !kI || !n_valid || !out) return fail(LCC_ERR_ARG, "%s: null pointer", name);
+  if (fmt != LCC_KEY_BF16 && fmt != LCC_KEY_NVFP4) return fail(LCC_ERR_ARG, "%s: unknown key format %d", name, fmt);
+  if (fmt == LCC_KEY_NVFP4 && !kI_scale) return fail(LCC_ERR_ARG, "%s: NVFP4 keys need kI_scale", name);
+  if (HI != 4 && HI != 8) return fail(LCC_ERR_SHAPE, "%s: HI=%d (supported: 4, 8)", name, HI);
+  if (fmt == LCC_KEY_BF16 && DI != 32 && DI != 64) return fail(LCC_ERR_SHAPE, "%s: DI=%d (bf16: 32, 64)", name, DI);
+  if (fmt == LCC_KEY_NVFP4 && (DI != 64 || HI != 8))
+    return fail(LCC_ERR_SHAPE, "%s: HI=%d DI=%d (NVFP4 keys: HI=8, DI=64)", name, HI, DI);
+  if (m < 1 || Ncap < 1) return fail(LCC_ERR_SHAPE, "%s: m=%d Ncap=%d must be >= 1", name, m, Ncap);
+  if (B > 65535) return fail(LCC_ERR_SHAPE, "%s: B=%d too large", name, B);
+  if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(out))
+    return fail(LCC_ERR_ALIGN, "%s: qI, w, kI and the output must be 16-byte aligned", name);
+  return LCC_OK;
+}
+
+lcc_status launch_scores(const IndexArgs& ia, int HI, int DI, lcc_key_format fmt, cudaStream_t s) {
+  if (fmt == LCC_KEY_NVFP4) return launch_index_score<8, 64, true>(ia, s);
+  if (HI == 8 && DI == 64) return launch_index_score<8, 64, false>(ia, s);
+  if (HI == 8 && DI == 32) return launch_index_score<8, 32, false>(ia, s);
+  if (HI == 4 && DI == 64) return launch_index_score<4, 64, false>(ia, s);
+  return launch_index_score<4, 32, false>(ia, s);
+}
+}  // namespace
+
+extern "C" {
+
+lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                                      const int64_t* q_pos0, lcc_key_format fmt, const void* kI,
+                                      const uint8_t* kI_scale, const int32_t* n_valid, int Ncap, int m,
+                                      float* scores, void* stream) {
+  const char* name = "lcc_lightning_index_scores";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d Tq=%d must be >= 0", name, B, Tq);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, scores);
+  if (st != LCC_OK) return st;
+  IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, 0, Tq, scores};
+  return launch_scores(ia, HI, DI, fmt, static_cast<cudaStream_t>(stream));
+}
+
 lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
                                     const int64_t* q_pos0, lcc_key_format fmt, const void* kI,
                                     const uint8_t* kI_scale, const int32_t* n_valid, int Ncap, int m, int k,
@@ -177,18 +226,9 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, i
   const char* name = "lcc_lightning_index_topk";
   if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d Tq=%d must be >= 0", name, B, Tq);
   if (B == 0 || Tq == 0) return LCC_OK;
-  if (!qI || !w || !q_pos0 || !kI || !n_valid || !idx) return fail(LCC_ERR_ARG, "%s: null pointer", name);
-  if (fmt != LCC_KEY_BF16 && fmt != LCC_KEY_NVFP4) return fail(LCC_ERR_ARG, "%s: unknown key format %d", name, fmt);
-  if (fmt == LCC_KEY_NVFP4 && !kI_scale) return fail(LCC_ERR_ARG, "%s: NVFP4 keys need kI_scale", name);
-  if (HI != 4 && HI != 8) return fail(LCC_ERR_SHAPE, "%s: HI=%d (supported: 4, 8)", name, HI);
-  if (fmt == LCC_KEY_BF16 && DI != 32 && DI != 64) return fail(LCC_ERR_SHAPE, "%s: DI=%d (bf16: 32, 64)", name, DI);
-  if (fmt == LCC_KEY_NVFP4 && (DI != 64 || HI != 8))
-    return fail(LCC_ERR_SHAPE, "%s: HI=%d DI=%d (NVFP4 keys: HI=8, DI=64)", name, HI, DI);
+  lcc_status cst = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
+  if (cst != LCC_OK) return cst;
   if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
-  if (m < 1 || Ncap < 1) return fail(LCC_ERR_SHAPE, "%s: m=%d Ncap=%d must be >= 1", name, m, Ncap);
-  if (B > 65535) return fail(LCC_ERR_SHAPE, "%s: B=%d too large", name, B);
-  if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(idx))
-    return fail(LCC_ERR_ALIGN, "%s: qI, w, kI and idx must be 16-byte aligned", name);
   const int nseg = (Ncap + kTopkCap - 1) / kTopkCap;
   if (nseg > 1 && static_cast<int64_t>(nseg) * k > kTopkCap)
     return fail(LCC_ERR_UNSUPPORTED, "%s: Ncap=%d with k=%d exceeds the two-stage top-k capacity", name, Ncap, k);
@@ -213,12 +253,7 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, i
   for (int q0 = 0; q0 < Tq; q0 += qc) {
     const int nq = qc < Tq - q0 ? qc : Tq - q0;
     IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq, scores};
-    lcc_status st;
-    if (fmt == LCC_KEY_NVFP4) st = launch_index_score<8, 64, true>(ia, s);
-    else if (HI == 8 && DI == 64) st = launch_index_score<8, 64, false>(ia, s);
-    else if (HI == 8 && DI == 32) st = launch_index_score<8, 32, false>(ia, s);
-    else if (HI == 4 && DI == 64) st = launch_index_score<4, 64, false>(ia, s);
-    else st = launch_index_score<4, 32, false>(ia, s);
+    lcc_status st = launch_scores(ia, HI, DI, fmt, s);
     if (st != LCC_OK) return st;
 
     TopkArgs ta{};

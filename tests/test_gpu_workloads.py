@@ -153,7 +153,7 @@ def test_csa_prefill_sampled_rows():
         qI_rows=regen_rows(s, wl.T_QI, rows, cfg.HI * cfg.DI).reshape(-1, cfg.HI, cfg.DI),
         w_rows=datagen.uniform_f32(s, wl.T_W, (T, cfg.HI)).numpy()[rows],
     )
-    ref = runs.csa_prefill(host_inp, cfg, rows, cfg.q_rows(rows))
+    ref = runs.csa_prefill(host_inp, cfg, rows, host(cfg.q_rows(rows)))
     assert np.mean(gKc == ref["Kc"]) > 0.99
     near = 0
     for n, r in enumerate(ref["rows"]):
@@ -197,7 +197,7 @@ def test_hca_prefill_sampled_rows():
     gnew = f64(inp["Kc"][0, cfg.N0:])
     del inp, out
     host_inp = {k: host(v) for k, v in cfg.make("cpu", with_q=False).items()}
-    ref = runs.hca_prefill(host_inp, cfg, rows, cfg.q_rows(rows))
+    ref = runs.hca_prefill(host_inp, cfg, rows, host(cfg.q_rows(rows)))
     assert np.mean(gnew == ref["Kc_new"]) > 0.99
     for n, r in enumerate(ref["rows"]):
         assert_close(gout[n], r["layer"][0], f"HCA prefill i={r['i']}")
