@@ -121,10 +121,14 @@ def peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-def csrc_hash():
+KERNEL_SOURCES = {"k_index_score": ["common.cuh", "index.cuh"]}
+
+
+def csrc_hash(kernel: str):
+    """Hash of the source files that define `kernel` (a profile goes stale when they change)."""
     d = os.path.join(ROOT, "long_context_compressed_15_b300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in KERNEL_SOURCES[kernel]:
         h.update(f.encode())
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
@@ -136,7 +140,7 @@ def ncu_traffic(kernel: str, workload: str):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(f"{workload}:{kernel}")
-    if not d or d.get("csrc_sha") != csrc_hash():
+    if not d or d.get("csrc_sha") != csrc_hash(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 

@@ -244,8 +244,8 @@ def test_pair_decode_64_steps():
     for b in range(B):
         kp, ks = datagen.nvfp4_normal(s0, wl.T_KI, cfg.Ncap_csa, cfg.DI, row0=b * cfg.Ncap_csa)
         kI = oracle.nvfp4_decode(kp.numpy(), ks.numpy())[None]
-        kc_rows = lambda bb, rows: (regen_rows(s0, wl.T_KC, b * cfg.Ncap_csa + rows, D),
-                                    regen_rows(s0, wl.T_VC, b * cfg.Ncap_csa + rows, D))
+        kc_rows = lambda bb, rows: (regen_rows(s0, wl.T_KC, b * cfg.N_csa + rows, D),
+                                    regen_rows(s0, wl.T_VC, b * cfg.N_csa + rows, D))
         hb = {k: v[b:b + 1] if k not in ("q", "qI", "w") else v[:, b:b + 1] for k, v in hk.items()}
         ref = runs.pair_decode(hb, cfg, batches=[0], kI=kI, kc_rows=kc_rows)
         for j, (kn, vn) in ref[(cfg.steps - 1, 0)]["new_entries"].items():
