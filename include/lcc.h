@@ -131,6 +131,34 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w,
                                       const int32_t* n_valid, int Ncap, int m,
                                       float* scores, void* stream);
 
+/* Allocation-free variant of lcc_lightning_index_topk.  The pages have no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- code running while a stream is captured into a CUDA graph
+ * (an allocation there is not capturable), plugin-style hosts that hand a
+ * routine only its input and output buffers, and decode loops that must not
+ * touch an allocator between steps.  Same arguments and results as
+ * lcc_lightning_index_topk, minus the workspace: the scratch lives in a
+ * fixed 8 MiB array inside the library (8388608 bytes of device memory that
+ * every GPU loading the library keeps until the process exits).
+ *  - Queries are processed in chunks sized to that array; a request whose
+ *    single query row needs more than 8 MiB (B*Ncap*4 bytes of scores plus
+ *    B*ceil(Ncap/8192)*k*8 bytes of candidate lists when Ncap > 8192) is
+ *    rejected with LCC_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on each device looks up the array's device address
+ *    (and sets kernel attributes); make that first call before any stream
+ *    capture begins.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero.  Calls whose kernels overlap on
+ *    the GPU (different streams, or different host threads) race on it:
+ *    serialise them.
+ *  - It never calls cudaMalloc, cudaFree or any allocating routine. */
+lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const float* w,
+                                            int B, int Tq, int HI, int DI,
+                                            const int64_t* q_pos0,
+                                            lcc_key_format fmt, const void* kI, const uint8_t* kI_scale,
+                                            const int32_t* n_valid, int Ncap, int m, int k,
+                                            int32_t* idx, float* score, void* stream);
+
 /* ---------------------------------------------------------------------- *
  * CSA sparse attention: MQA (all H heads share one K/V row, [HYBRID]) over
  * the k entries idx[b,i,:] of the compressed cache; entries < 0 are skipped.

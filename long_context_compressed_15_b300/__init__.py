@@ -18,6 +18,7 @@ import torch
 
 __all__ = [
     "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk", "lightning_index_scores",
+    "lightning_index_topk_noalloc",
     "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
     "swa_attn", "attn_merge", "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
 ]
@@ -36,6 +37,7 @@ _SIGS = {
     "lcc_hca_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
     "lcc_index_topk_workspace": [_I, _I, _I, _I],
     "lcc_lightning_index_topk": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
+    "lcc_lightning_index_topk_noalloc": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P],
     "lcc_lightning_index_scores": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P, _P],
     "lcc_csa_sparse_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _L, _I, _P, _I, _P, _P, _P],
     "lcc_dense_attn_workspace": [_I, _I, _I, _I, _I],
@@ -204,6 +206,26 @@ def lightning_index_topk(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None, idx=No
     _call("lcc_lightning_index_topk", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
           _ptr(kI_scale), _ptr(n_valid), Ncap, int(m), int(k), _ptr(idx), _ptr(score),
           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return idx
+
+
+def lightning_index_topk_noalloc(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None, idx=None, score=None,
+                                 stream=None):
+    """lightning_index_topk without a workspace, for callers that cannot allocate device memory.
+
+    The library keeps its scratch in a fixed 8 MiB device array shared by all
+    calls (overlapping calls race; make the first call on a device before any
+    graph capture).  idx must be passed in so that nothing is allocated here.
+    """
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    _need(idx, torch.int32, "idx", 3)
+    B, Tq, HI, DI = qI.shape
+    fmt = KEY_NVFP4 if kI.dtype == torch.uint8 else KEY_BF16
+    if not isinstance(q_pos0, torch.Tensor) or not isinstance(n_valid, torch.Tensor):
+        raise ValueError("q_pos0 and n_valid must be device tensors (nothing is allocated here)")
+    _call("lcc_lightning_index_topk_noalloc", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
+          _ptr(kI_scale), _ptr(n_valid), kI.shape[1], int(m), int(k), _ptr(idx), _ptr(score), _stream(stream))
     return idx
 
 

@@ -476,3 +476,117 @@ lcc_status lcc_attn_merge(int nb, const float* const* O_parts, const float* cons
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------- allocation-free top-k
+// Scratch of lcc_lightning_index_topk_noalloc: a fixed device array instead
+// of a caller-provided workspace, for callers that cannot allocate.  Host
+// code reaches it only through the address cudaGetSymbolAddress returns for
+// the current device (the host-side symbol is not a device address).
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+void* g_noalloc_ptr[64] = {};
+std::mutex g_noalloc_mu;
+
+lcc_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(LCC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(LCC_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(LCC_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return LCC_OK;
+}
+}  // namespace
+
+extern "C" lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const float* w, int B, int Tq, int HI,
+                                                       int DI, const int64_t* q_pos0, lcc_key_format fmt,
+                                                       const void* kI, const uint8_t* kI_scale,
+                                                       const int32_t* n_valid, int Ncap, int m, int k, int32_t* idx,
+                                                       float* score, void* stream) {
+  const char* name = "lcc_lightning_index_topk_noalloc";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d Tq=%d must be >= 0", name, B, Tq);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
+  if (st != LCC_OK) return st;
+  if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
+  const int nseg = (Ncap + kTopkCap - 1) / kTopkCap;
+  if (nseg > 1 && static_cast<int64_t>(nseg) * k > kTopkCap)
+    return fail(LCC_ERR_UNSUPPORTED, "%s: Ncap=%d with k=%d exceeds the two-stage top-k capacity", name, Ncap, k);
+  // bytes one query row of every batch needs: scores + (two-stage) candidate lists
+  const size_t per_q_scores = static_cast<size_t>(B) * Ncap * sizeof(float);
+  const size_t per_q_cand = nseg > 1 ? static_cast<size_t>(B) * nseg * k * sizeof(float) : 0;
+  const size_t per_q = round_up(per_q_scores, 256) + 2 * round_up(per_q_cand, 256);
+  if (per_q > kNoAllocScratchBytes)
+    return fail(LCC_ERR_WORKSPACE, "%s: one query row needs %zu scratch bytes, the fixed scratch holds %zu", name,
+                per_q, kNoAllocScratchBytes);
+  int qc = 1;  // largest query chunk whose scores and candidates fit the scratch
+  while (qc < Tq) {
+    const int nx = qc * 2 < Tq ? qc * 2 : Tq;
+    const size_t need = round_up(per_q_scores * nx, 256) + 2 * round_up(per_q_cand * nx, 256);
+    if (need > kNoAllocScratchBytes) break;
+    qc = nx;
+  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != LCC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(k_topk<kTopkNT, kTopkCap, false>, kTopkCap * 4, g_topk_a_done)) != LCC_OK) return st;
+    if ((st = ensure_smem(k_topk<kTopkNT, kTopkCap, true>, kTopkCap * 8, g_topk_b_done)) != LCC_OK) return st;
+  }
+  char* base = static_cast<char*>(scratch);
+  float* scores = reinterpret_cast<float*>(base);
+  const size_t sc_bytes = round_up(per_q_scores * qc, 256);
+  const size_t cand_bytes = round_up(per_q_cand * qc, 256);
+  float* cand_s = reinterpret_cast<float*>(base + sc_bytes);
+  int32_t* cand_i = reinterpret_cast<int32_t*>(base + sc_bytes + cand_bytes);
+  for (int q0 = 0; q0 < Tq; q0 += qc) {
+    const int nq = qc < Tq - q0 ? qc : Tq - q0;
+    IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq, scores};
+    if ((st = launch_scores(ia, HI, DI, fmt, s)) != LCC_OK) return st;
+    TopkArgs ta{};
+    ta.scores = scores;
+    ta.Ncap = Ncap;
+    ta.q_pos0 = q_pos0;
+    ta.n_valid = n_valid;
+    ta.m = m;
+    ta.Tq = Tq;
+    ta.q0 = q0;
+    ta.nq = nq;
+    ta.k = k;
+    ta.seg = kTopkCap;
+    const int rows = B * nq;
+    if (nseg == 1) {
+      ta.out_i = idx;
+      ta.out_s = score;
+      ta.final_out = 1;
+      k_topk<kTopkNT, kTopkCap, false><<<dim3(1, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
+      if ((st = launch_check("k_topk")) != LCC_OK) return st;
+    } else {
+      ta.out_i = cand_i;
+      ta.out_s = cand_s;
+      ta.out_stride = static_cast<int64_t>(nseg) * k;
+      ta.final_out = 0;
+      k_topk<kTopkNT, kTopkCap, false><<<dim3(nseg, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
+      if ((st = launch_check("k_topk")) != LCC_OK) return st;
+      TopkArgs tb = ta;
+      tb.cand_s = cand_s;
+      tb.cand_i = cand_i;
+      tb.ncand = nseg * k;
+      tb.out_i = idx;
+      tb.out_s = score;
+      tb.final_out = 1;
+      k_topk<kTopkNT, kTopkCap, true><<<dim3(1, rows), kTopkNT, kTopkCap * 8, s>>>(tb);
+      if ((st = launch_check("k_topk merge")) != LCC_OK) return st;
+    }
+  }
+  return LCC_OK;
+}
