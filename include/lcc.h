@@ -141,8 +141,9 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w,
  * fixed 8 MiB array inside the library (8388608 bytes of device memory that
  * every GPU loading the library keeps until the process exits).
  *  - Queries are processed in chunks sized to that array; a request whose
- *    single query row needs more than 8 MiB (B*Ncap*4 bytes of scores plus
- *    B*ceil(Ncap/8192)*k*8 bytes of candidate lists when Ncap > 8192) is
+ *    single query row needs more than 8 MiB (per batch row: Ncap*4 bytes of
+ *    scores, ceil(Ncap/16)*4 bytes of group maxima, 16 KiB of candidate
+ *    list and 8 bytes of counters, each array rounded up to 256 bytes) is
  *    rejected with LCC_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on each device looks up the array's device address
  *    (and sets kernel attributes); make that first call before any stream
@@ -201,6 +202,40 @@ lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float sc
                         const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t kv_rstride, int Rcap,
                         const int64_t* raw_pos0, int W,
                         float* O, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Whole layers in one pass ([HYBRID]: the window branch runs in parallel
+ * with the compressed one; [VIDEO] "주요 인사이트": CSA and HCA layers
+ * alternate).  The result is the softmax attention over the union of the
+ * compressed keys and the window keys, which equals the log-sum-exp merge
+ * (lcc_attn_merge) of the two branches:
+ *   lcc_csa_layer_attn  keys = entries idx[b,i,:] of Kc/Vc  ++ window rows
+ *   lcc_hca_layer_attn  keys = visible entries of Kc/Vc     ++ window rows
+ * out: [B, Tq, H, D] bf16 (round to nearest even); lse_out (optional, may be
+ * NULL): [B, Tq, H] fp32 natural-log normaliser of the union.
+ * Compressed and window arguments as in lcc_csa_sparse_attn /
+ * lcc_hca_dense_attn and lcc_swa_attn (Kr/Vr rows r_rstride elements apart,
+ * Rcap rows per batch).  Calls with few rows split the key list across CTAs
+ * and need lcc_layer_attn_workspace(B, Tq, H, D, n_keys) bytes of workspace,
+ * n_keys = k + W (CSA layer) or Ncap + W (HCA layer); 0 means none.
+ * ---------------------------------------------------------------------- */
+size_t lcc_layer_attn_workspace(int B, int Tq, int H, int D, int n_keys);
+lcc_status lcc_csa_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                              const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* idx, int k,
+                              const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride, int Rcap,
+                              const int64_t* raw_pos0, int W,
+                              lcc_bf16* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
+lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                              const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* n_valid, int m,
+                              const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride, int Rcap,
+                              const int64_t* raw_pos0, int W,
+                              lcc_bf16* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------- *
  * Branch merge by log-sum-exp: with L = log sum_b exp(lse_b),

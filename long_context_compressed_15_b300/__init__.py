@@ -20,7 +20,8 @@ __all__ = [
     "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk", "lightning_index_scores",
     "lightning_index_topk_noalloc",
     "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
-    "swa_attn", "attn_merge", "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
+    "swa_attn", "attn_merge", "csa_layer_attn", "hca_layer_attn", "layer_attn_workspace",
+    "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
 ]
 
 KEY_BF16, KEY_NVFP4 = 0, 1
@@ -44,12 +45,17 @@ _SIGS = {
     "lcc_hca_dense_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P, _Z, _P],
     "lcc_swa_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P],
     "lcc_attn_merge": [_I, _P, _P, _L, _I, _P, _P, _P, _P],
+    "lcc_layer_attn_workspace": [_I, _I, _I, _I, _I],
+    "lcc_csa_layer_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _L, _I, _P, _I,
+                           _P, _P, _P, _Z, _P],
+    "lcc_hca_layer_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _L, _I, _P, _I,
+                           _P, _P, _P, _Z, _P],
     "lcc_last_error": [],
     "lcc_version": [],
     "lcc_sync_status": [_P],
     "lcc_launch_count": [],
 }
-_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z,
+_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z,
         "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p, "lcc_launch_count": ctypes.c_uint64}
 
 
@@ -335,6 +341,65 @@ def attn_merge(parts, out=None, out_f32=None, lse_out=None, stream=None):
     Larr = (ctypes.c_void_p * nb)(*[l.data_ptr() for l in Ls])
     _call("lcc_attn_merge", nb, ctypes.cast(Oarr, ctypes.c_void_p), ctypes.cast(Larr, ctypes.c_void_p), rows, D,
           _ptr(out), _ptr(out_f32), _ptr(lse_out), _stream(stream))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# whole layers in one pass (compressed branch ++ window)
+# ---------------------------------------------------------------------------
+def layer_attn_workspace(B, Tq, H, D, n_keys) -> int:
+    return int(load().lcc_layer_attn_workspace(B, Tq, H, D, n_keys))
+
+
+def _layer_out(q, out, lse_out):
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    _need(out, torch.bfloat16, "out", 4)
+    if not (out.is_contiguous() and q.is_contiguous()):
+        raise ValueError("q and out must be contiguous")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, "lse_out", 3)
+    return out
+
+
+def _ws(workspace, need, dev):
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    return workspace, (workspace.numel() * workspace.element_size() if workspace is not None else 0)
+
+
+def csa_layer_attn(q, Kc, Vc, idx, Kr, Vr, q_pos0, raw_pos0, W, scale=1.0, out=None, lse_out=None,
+                   workspace=None, stream=None):
+    """CSA layer: softmax over the idx-selected entries and the window rows -> bf16 [B, Tq, H, D]."""
+    _need(q, torch.bfloat16, "q", 4)
+    _need(idx, torch.int32, "idx", 3)
+    B, Tq, H, D = q.shape
+    rs, rr = _kv(Kc, Vc), _kv(Kr, Vr)
+    out = _layer_out(q, out, lse_out)
+    q_pos0 = _positions(q_pos0, B, q.device)
+    raw_pos0 = _positions(raw_pos0, B, q.device)
+    k = idx.shape[2]
+    workspace, nbytes = _ws(workspace, layer_attn_workspace(B, Tq, H, D, k + int(W)), q.device)
+    _call("lcc_csa_layer_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(q_pos0), _ptr(Kc), _ptr(Vc), rs,
+          Kc.shape[1], _ptr(idx.contiguous()), k, _ptr(Kr), _ptr(Vr), rr, Kr.shape[1], _ptr(raw_pos0), int(W),
+          _ptr(out), _ptr(lse_out), _ptr(workspace), nbytes, _stream(stream))
+    return out
+
+
+def hca_layer_attn(q, Kc, Vc, n_valid, m, Kr, Vr, q_pos0, raw_pos0, W, scale=1.0, out=None, lse_out=None,
+                   workspace=None, stream=None):
+    """HCA layer: softmax over every visible entry and the window rows -> bf16 [B, Tq, H, D]."""
+    _need(q, torch.bfloat16, "q", 4)
+    B, Tq, H, D = q.shape
+    rs, rr = _kv(Kc, Vc), _kv(Kr, Vr)
+    out = _layer_out(q, out, lse_out)
+    q_pos0 = _positions(q_pos0, B, q.device)
+    raw_pos0 = _positions(raw_pos0, B, q.device)
+    n_valid = _positions(n_valid, B, q.device, torch.int32)
+    workspace, nbytes = _ws(workspace, layer_attn_workspace(B, Tq, H, D, Kc.shape[1] + int(W)), q.device)
+    _call("lcc_hca_layer_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(q_pos0), _ptr(Kc), _ptr(Vc), rs,
+          Kc.shape[1], _ptr(n_valid), int(m), _ptr(Kr), _ptr(Vr), rr, Kr.shape[1], _ptr(raw_pos0), int(W),
+          _ptr(out), _ptr(lse_out), _ptr(workspace), nbytes, _stream(stream))
     return out
 
 

@@ -14,6 +14,13 @@
 // own 16 rows each and use the warp-level m16n8k16 MMA; K/V tiles of 64
 // keys are double-buffered with cp.async.  gridDim.z splits the key range
 // (decode); partials are then reduced by k_split_combine.
+//
+// WIN2 appends the window branch as a second key source of the same
+// softmax: the tiles of the compressed source are followed by the tiles of
+// the raw window rows, and one online-softmax state runs over both.  One
+// softmax over the union of the two key lists equals the log-sum-exp merge
+// of the two branches, so a whole CSA layer (sparse + window) or HCA layer
+// (dense + window) comes out of one pass, written as bf16.
 #pragma once
 #include "common.cuh"
 
@@ -41,6 +48,12 @@ struct AttnArgs {
   float* lse;
   int nsplit;
   int64_t rows_total;  // B*Tq*H: stride between split partials
+  // second key source (window rows) for WIN2 kernels
+  const bf16* K2;
+  const bf16* V2;
+  int64_t kv2_bs, kv2_rs;
+  int Ncap2;
+  bf16* out_bf16;      // if set (and nsplit == 1): the result as bf16 instead of fp32 O
 };
 
 template <int D, int ROWS>
@@ -52,6 +65,19 @@ struct AttnSmem {
   static constexpr size_t total = q_bytes + 2 * kv_bytes + key_bytes;
 };
 
+__device__ __forceinline__ void window_bounds(const AttnArgs& a, int b, int qi, int nrows, int& lo, int& hi) {
+  const int64_t t = __ldg(a.q_pos0 + b) + qi;
+  const int64_t rp0 = __ldg(a.raw_pos0 + b);
+  int64_t plo = t - a.W + 1;
+  if (plo < 0) plo = 0;
+  int64_t l = plo - rp0, h = t - rp0 + 1;
+  if (l < 0) l = 0;
+  if (h > nrows) h = nrows;
+  if (h < l) h = l;
+  lo = static_cast<int>(l);
+  hi = static_cast<int>(h);
+}
+
 template <int MODE>
 __device__ __forceinline__ void attn_row_bounds(const AttnArgs& a, int b, int qi, bool valid, int& lo, int& hi) {
   lo = 0;
@@ -61,23 +87,14 @@ __device__ __forceinline__ void attn_row_bounds(const AttnArgs& a, int b, int qi
     hi = a.k;
     return;
   }
-  const int64_t t = __ldg(a.q_pos0 + b) + qi;
   if (MODE == ATT_RANGE) {
-    hi = visible_entries(t, a.m, __ldg(a.n_valid + b), a.Ncap);
+    hi = visible_entries(__ldg(a.q_pos0 + b) + qi, a.m, __ldg(a.n_valid + b), a.Ncap);
   } else {
-    const int64_t rp0 = __ldg(a.raw_pos0 + b);
-    int64_t plo = t - a.W + 1;
-    if (plo < 0) plo = 0;
-    int64_t l = plo - rp0, h = t - rp0 + 1;
-    if (l < 0) l = 0;
-    if (h > a.Ncap) h = a.Ncap;
-    if (h < l) h = l;
-    lo = static_cast<int>(l);
-    hi = static_cast<int>(h);
+    window_bounds(a, b, qi, a.Ncap, lo, hi);
   }
 }
 
-template <int D, int ROWS, int MODE>
+template <int D, int ROWS, int MODE, bool WIN2>
 __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
   constexpr int NT = ROWS * 2;
   constexpr int KT = 64;
@@ -90,7 +107,7 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
   bf16* sK = reinterpret_cast<bf16*>(smem + S::q_bytes);
   bf16* sV = reinterpret_cast<bf16*>(smem + S::q_bytes + S::kv_bytes);
   int* sKey = reinterpret_cast<int*>(smem + S::q_bytes + 2 * S::kv_bytes);
-  __shared__ int s_lo, s_hi;
+  __shared__ int s_lo, s_hi, s_lo2, s_hi2;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
@@ -118,26 +135,35 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
     return qi < a.Tq;
   };
 
-  if (tid == 0) { s_lo = INT_MAX; s_hi = INT_MIN; }
+  if (tid == 0) { s_lo = INT_MAX; s_hi = INT_MIN; s_lo2 = INT_MAX; s_hi2 = INT_MIN; }
   __syncthreads();
   const int rA = warp * 16 + g, rB = rA + 8;
   int qA, hA, qB, hB, loA, hiA, loB, hiB;
+  int wloA = 0, whiA = 0, wloB = 0, whiB = 0;
   const bool vA = row_qh(rA, qA, hA), vB = row_qh(rB, qB, hB);
   attn_row_bounds<MODE>(a, b, qA, vA, loA, hiA);
   attn_row_bounds<MODE>(a, b, qB, vB, loB, hiB);
+  if (WIN2) {
+    if (vA) window_bounds(a, b, qA, a.Ncap2, wloA, whiA);
+    if (vB) window_bounds(a, b, qB, a.Ncap2, wloB, whiB);
+  }
   if (c4 == 0) {
     if (vA && hiA > loA) { atomicMin(&s_lo, loA); atomicMax(&s_hi, hiA); }
     if (vB && hiB > loB) { atomicMin(&s_lo, loB); atomicMax(&s_hi, hiB); }
+    if (WIN2 && vA && whiA > wloA) { atomicMin(&s_lo2, wloA); atomicMax(&s_hi2, whiA); }
+    if (WIN2 && vB && whiB > wloB) { atomicMin(&s_lo2, wloB); atomicMax(&s_hi2, whiB); }
   }
   __syncthreads();
-  int z_lo = 0, z_hi = 0;
-  if (s_hi > s_lo) {
-    const int len = s_hi - s_lo;
-    const int per = ((len + a.nsplit - 1) / a.nsplit + KT - 1) / KT * KT;
-    z_lo = s_lo + z * per;
-    z_hi = min(s_hi, z_lo + per);
-  }
-  const int ntiles = z_hi > z_lo ? (z_hi - z_lo + KT - 1) / KT : 0;
+  // the key tiles of source 1 followed by those of source 2; split z takes a contiguous run
+  const int T1 = s_hi > s_lo ? (s_hi - s_lo + KT - 1) / KT : 0;
+  const int T2 = (WIN2 && s_hi2 > s_lo2) ? (s_hi2 - s_lo2 + KT - 1) / KT : 0;
+  const int per_z = (T1 + T2 + a.nsplit - 1) / a.nsplit;
+  const int t_first = z * per_z;
+  const int ntiles = max(0, min(T1 + T2, t_first + per_z) - t_first);
+  auto tile_start = [&](int tt, int& src, int& j0, int& jend) {
+    if (tt < T1) { src = 0; j0 = s_lo + tt * KT; jend = s_hi; }
+    else { src = 1; j0 = s_lo2 + (tt - T1) * KT; jend = s_hi2; }
+  };
 
   // ---- async loads ----
   const int64_t qrow_base = MODE == ATT_GATHER ? (static_cast<int64_t>(b) * a.Tq + qi_cta) : 0;
@@ -148,14 +174,16 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
     const bf16* src = a.q + ((static_cast<int64_t>(b) * a.Tq + (v ? qi : 0)) * a.H + (v ? h : 0)) * D + cc * 8;
     cp_async16(smem_u32(sQ + r * D + ((cc ^ (r & 7)) * 8)), src, v ? 16 : 0);
   }
-  auto load_kv = [&](int j0, int st) {
+  auto load_kv = [&](int tt, int st) {
+    int src_id, j0, jend;
+    tile_start(tt, src_id, j0, jend);
     for (int u = tid; u < 2 * KT * CPR; u += NT) {
       const int which = u / (KT * CPR), rem = u % (KT * CPR);
       const int kk = rem / CPR, cc = rem % CPR;
       const int j = j0 + kk;
       int e = -1;
-      if (j < z_hi) {
-        if (MODE == ATT_GATHER) {
+      if (j < jend) {
+        if (MODE == ATT_GATHER && src_id == 0) {
           e = __ldg(a.idx + qrow_base * a.k + j);
           if (e >= a.Ncap || e < -1) {
             record_error(DEV_ERR_INDEX, static_cast<unsigned>(j));
@@ -165,14 +193,22 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
           e = j;
         }
       }
-      const bf16* base = which ? a.V : a.K;
-      const bf16* src = base + (e >= 0 ? (b * a.kv_bs + static_cast<int64_t>(e) * a.kv_rs + cc * 8) : 0);
+      const bf16* base;
+      int64_t off;
+      if (src_id == 0) {
+        base = which ? a.V : a.K;
+        off = b * a.kv_bs + static_cast<int64_t>(e) * a.kv_rs;
+      } else {
+        base = which ? a.V2 : a.K2;
+        off = b * a.kv2_bs + static_cast<int64_t>(e) * a.kv2_rs;
+      }
+      const bf16* src = base + (e >= 0 ? off + cc * 8 : 0);
       bf16* dst = (which ? sV : sK) + st * KT * D + kk * D + ((cc ^ (kk & 7)) * 8);
       cp_async16(smem_u32(dst), src, e >= 0 ? 16 : 0);
       if (which == 0 && cc == 0) sKey[st * KT + kk] = e;
     }
   };
-  if (ntiles > 0) load_kv(z_lo, 0);
+  if (ntiles > 0) load_kv(t_first, 0);
   cp_async_commit();
 
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -183,9 +219,12 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
 
   for (int t = 0; t < ntiles; ++t) {
     const int st = t & 1;
-    const int j0 = z_lo + t * KT;
+    int src_id, j0, jend;
+    tile_start(t_first + t, src_id, j0, jend);
+    const int lA = src_id ? wloA : loA, hA_ = src_id ? whiA : hiA;
+    const int lB = src_id ? wloB : loB, hB_ = src_id ? whiB : hiB;
     if (t + 1 < ntiles) {
-      load_kv(j0 + KT, st ^ 1);
+      load_kv(t_first + t + 1, st ^ 1);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
@@ -226,7 +265,7 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
         const int kk = 8 * n + 2 * c4 + (e & 1);
         const int jg = j0 + kk;
         const bool keyok = sKey[st * KT + kk] >= 0;
-        const bool ok = keyok && (e < 2 ? (jg >= loA && jg < hiA) : (jg >= loB && jg < hiB));
+        const bool ok = keyok && (e < 2 ? (jg >= lA && jg < hA_) : (jg >= lB && jg < hB_));
         const float v = ok ? s[n][e] * a.scale_log2 : -INFINITY;
         s[n][e] = v;
         if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
@@ -289,21 +328,36 @@ __global__ void __launch_bounds__(ROWS * 2) k_attn(AttnArgs a) {
   const float LN2 = 0.6931471805599453f;
   auto grow = [&](int qi, int h) -> int64_t { return (static_cast<int64_t>(b) * a.Tq + qi) * a.H + h; };
   const int64_t zoff = static_cast<int64_t>(z) * a.rows_total;
+  const bool to_bf16 = a.out_bf16 != nullptr && a.nsplit == 1;
   if (vA) {
     const int64_t r = zoff + grow(qA, hA);
-    float* o = a.O + r * D;
+    if (to_bf16) {
+      bf16* o = a.out_bf16 + r * D;
 #pragma unroll
-    for (int n = 0; n < NDT; ++n)
-      *reinterpret_cast<float2*>(o + 8 * n + 2 * c4) = make_float2(oacc[n][0] * inv0, oacc[n][1] * inv0);
-    if (c4 == 0) a.lse[r] = l0 > 0.f ? (m0 + log2f(l0)) * LN2 : -INFINITY;
+      for (int n = 0; n < NDT; ++n)
+        *reinterpret_cast<uint32_t*>(o + 8 * n + 2 * c4) = pack_bf16(oacc[n][0] * inv0, oacc[n][1] * inv0);
+    } else {
+      float* o = a.O + r * D;
+#pragma unroll
+      for (int n = 0; n < NDT; ++n)
+        *reinterpret_cast<float2*>(o + 8 * n + 2 * c4) = make_float2(oacc[n][0] * inv0, oacc[n][1] * inv0);
+    }
+    if (c4 == 0 && a.lse) a.lse[r] = l0 > 0.f ? (m0 + log2f(l0)) * LN2 : -INFINITY;
   }
   if (vB) {
     const int64_t r = zoff + grow(qB, hB);
-    float* o = a.O + r * D;
+    if (to_bf16) {
+      bf16* o = a.out_bf16 + r * D;
 #pragma unroll
-    for (int n = 0; n < NDT; ++n)
-      *reinterpret_cast<float2*>(o + 8 * n + 2 * c4) = make_float2(oacc[n][2] * inv1, oacc[n][3] * inv1);
-    if (c4 == 0) a.lse[r] = l1 > 0.f ? (m1 + log2f(l1)) * LN2 : -INFINITY;
+      for (int n = 0; n < NDT; ++n)
+        *reinterpret_cast<uint32_t*>(o + 8 * n + 2 * c4) = pack_bf16(oacc[n][2] * inv1, oacc[n][3] * inv1);
+    } else {
+      float* o = a.O + r * D;
+#pragma unroll
+      for (int n = 0; n < NDT; ++n)
+        *reinterpret_cast<float2*>(o + 8 * n + 2 * c4) = make_float2(oacc[n][2] * inv1, oacc[n][3] * inv1);
+    }
+    if (c4 == 0 && a.lse) a.lse[r] = l1 > 0.f ? (m1 + log2f(l1)) * LN2 : -INFINITY;
   }
 }
 

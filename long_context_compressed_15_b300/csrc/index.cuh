@@ -33,6 +33,9 @@ struct IndexArgs {
   int Ncap, m;
   int q0, nq;            // query chunk [q0, q0+nq)
   float* scores;         // [nq, Ncap] for this chunk (row = (b, i - q0) flattened as b*nq + i-q0)
+  uint32_t* gmax;        // optional [B*nq, g_stride]: key of the largest score of each 16-entry group
+  int g_stride;
+  int* counters;         // optional [2, B*nq]: zeroed here for the top-k kernel that follows
 };
 
 // Each CTA: 4 warps x 64 entries; NQ queries (n-tiles of 8 (query, head) columns).
@@ -52,6 +55,14 @@ __global__ void __launch_bounds__(128) k_index_score(IndexArgs a) {
   const int qlast = min(qbase + NQ, a.q0 + a.nq) - 1;
   const int vis_max = visible_entries(pos0 + qlast, a.m, nval, a.Ncap);
   const int e_cta = blockIdx.x * ENT;
+  if (a.counters && blockIdx.x == 0 && threadIdx.x < NQ) {
+    const int qq = qbase + threadIdx.x;
+    if (qq < a.q0 + a.nq && qq < a.Tq) {
+      const int64_t r = static_cast<int64_t>(b) * a.nq + (qq - a.q0);
+      a.counters[r] = 0;
+      a.counters[static_cast<int64_t>(a.B) * a.nq + r] = 0;
+    }
+  }
   if (e_cta >= vis_max) return;
 
   // ---- B fragments: indexer queries, permuted to match the key loads ----
@@ -153,6 +164,16 @@ __global__ void __launch_bounds__(128) k_index_score(IndexArgs a) {
           if (rowA < vis) dst[rowA] = sA;
           if (rowB < vis) dst[rowB] = sB;
         }
+      }
+      if (a.gmax && HI == 8) {
+        // group maximum over the m-tile's 16 entries (one query per n-tile when HI = 8)
+        const int qq = qbase + nt;
+        const bool qok = qq < a.q0 + a.nq && qq < a.Tq;
+        const int vis = qok ? visible_entries(pos0 + qq, a.m, nval, a.Ncap) : 0;
+        uint32_t key = max(rowA < vis ? f32_to_key(sA) : 0u, rowB < vis ? f32_to_key(sB) : 0u);
+        key = __reduce_max_sync(0xffffffffu, key);
+        if (lane == 0 && qok && e0 < vis)
+          a.gmax[(static_cast<int64_t>(b) * a.nq + (qq - a.q0)) * a.g_stride + (e0 >> 4)] = key;
       }
     }
   }

@@ -15,7 +15,10 @@
 #include "merge.cuh"
 #include "attn.cuh"
 #include "index.cuh"
-#include "topk.cuh"
+#include "index_tc.cuh"
+#include "topk_thr.cuh"
+
+#include <cudaTypedefs.h>
 
 using namespace lcc;
 
@@ -93,7 +96,8 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
 
 // ----------------------------------------------------------------- index/topk
 constexpr int kTopkNT = 256;
-constexpr int kTopkCap = 8192;  // elements per top-k CTA
+constexpr int kCandCap = 2048;   // candidate list per row of the threshold top-k
+constexpr int kTopkSeg = 4096;   // entries per CTA of the threshold top-k
 constexpr size_t kScoreBudget = size_t(1) << 28;  // score elements per query chunk
 
 int index_chunk(int B, int Tq, int Ncap) {
@@ -103,22 +107,108 @@ int index_chunk(int B, int Tq, int Ncap) {
   return static_cast<int>(qc);
 }
 
+int gmax_stride(int Ncap) { return (Ncap + 15) / 16; }
+
+// Scratch of one query chunk of qc queries (rows = B*qc): scores, group
+// maxima, candidate lists and the two per-row counters.
 struct IndexWs {
-  size_t scores, cand_s, cand_i, total;
+  size_t scores, gmax, cand_k, cand_i, counters, total;
 };
-IndexWs index_ws(int B, int Tq, int Ncap, int k) {
+IndexWs index_ws_rows(int64_t rows, int Ncap) {
   IndexWs w{};
-  if (B <= 0 || Tq <= 0 || Ncap <= 0 || k <= 0) return w;
-  const int qc = index_chunk(B, Tq, Ncap);
-  const int64_t rows = static_cast<int64_t>(B) * qc;
-  const int nseg = (Ncap + kTopkCap - 1) / kTopkCap;
   w.scores = round_up(rows * Ncap * sizeof(float), 256);
-  if (nseg > 1) {
-    w.cand_s = round_up(rows * nseg * k * sizeof(float), 256);
-    w.cand_i = round_up(rows * nseg * k * sizeof(int32_t), 256);
-  }
-  w.total = w.scores + w.cand_s + w.cand_i;
+  w.gmax = round_up(rows * gmax_stride(Ncap) * sizeof(uint32_t), 256);
+  w.cand_k = round_up(rows * kCandCap * sizeof(uint32_t), 256);
+  w.cand_i = round_up(rows * kCandCap * sizeof(int32_t), 256);
+  w.counters = round_up(rows * 2 * sizeof(int), 256);
+  w.total = w.scores + w.gmax + w.cand_k + w.cand_i + w.counters;
   return w;
+}
+IndexWs index_ws(int B, int Tq, int Ncap, int k) {
+  if (B <= 0 || Tq <= 0 || Ncap <= 0 || k <= 0) return IndexWs{};
+  return index_ws_rows(static_cast<int64_t>(B) * index_chunk(B, Tq, Ncap), Ncap);
+}
+
+// ---- TMA tensor maps (driver entry point fetched through the runtime) ----
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over `rows` rows of `cols` elements (row stride `ld`
+// elements), box = box_cols x box_rows, with the given swizzle.
+lcc_status make_tmap_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t ld,
+                        uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz, const char* what) {
+  auto enc = tmap_encoder();
+  if (!enc) return fail(LCC_ERR_CUDA, "%s: cuTensorMapEncodeTiled unavailable", what);
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {ld * 2};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LCC_ERR_CUDA, "%s: cuTensorMapEncodeTiled failed (%d)", what, int(r));
+  return LCC_OK;
+}
+
+int g_num_sms = 0;
+int num_sms() {
+  if (g_num_sms == 0) {
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) ==
+        cudaSuccess)
+      g_num_sms = n;
+    else
+      g_num_sms = 148;
+  }
+  return g_num_sms;
+}
+
+unsigned long long g_index_tc_done[2][2][2] = {};
+
+template <int HI, int DI, int NQ>
+lcc_status launch_index_tc_q(const IndexArgs& ia, const CUtensorMap& tm, int bit, cudaStream_t s) {
+  constexpr int STAGES = 4;
+  using C = IndexTcCfg<HI, DI, NQ, STAGES>;
+  auto kern = k_index_tc<HI, DI, NQ, STAGES>;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    lcc_status st = ensure_smem(kern, C::SMEM, g_index_tc_done[HI == 8][DI == 64][bit]);
+    if (st != LCC_OK) return st;
+  }
+  IndexTcArgs a{ia.qI, ia.w, ia.B, ia.Tq, ia.q_pos0, ia.n_valid, ia.Ncap, ia.m, ia.q0, ia.nq, 0,
+                ia.scores, ia.gmax, ia.g_stride, ia.counters};
+  const int ngroups = (ia.nq + NQ - 1) / NQ;
+  const int tiles = (ia.Ncap + C::TILE - 1) / C::TILE;
+  const int64_t base = static_cast<int64_t>(ia.B) * ngroups;
+  const int target = 3 * num_sms();
+  int nsplit = base >= 2 * num_sms() ? 1 : static_cast<int>((target + base - 1) / base);
+  if (nsplit > tiles) nsplit = tiles;
+  if (nsplit < 1) nsplit = 1;
+  a.tiles_per_split = (tiles + nsplit - 1) / nsplit;
+  nsplit = (tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  if (ngroups > 65535) return fail(LCC_ERR_SHAPE, "k_index_tc: %d query groups", ngroups);
+  kern<<<dim3(nsplit, ngroups, ia.B), 192, C::SMEM, s>>>(tm, a);
+  return launch_check("k_index_tc");
+}
+
+template <int HI, int DI>
+lcc_status launch_index_tc(const IndexArgs& ia, cudaStream_t s) {
+  CUtensorMap tm;
+  lcc_status st = make_tmap_2d(&tm, ia.kI, DI, static_cast<uint64_t>(ia.B) * ia.Ncap, DI, DI, 128,
+                               DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "k_index_tc");
+  if (st != LCC_OK) return st;
+  if (ia.nq * HI <= 16) return launch_index_tc_q<HI, DI, 16 / HI>(ia, tm, 0, s);
+  return launch_index_tc_q<HI, DI, 128 / HI>(ia, tm, 1, s);
 }
 
 template <int HI, int DI, bool FP4>
@@ -135,7 +225,6 @@ lcc_status launch_index_score(const IndexArgs& a, cudaStream_t s) {
   return launch_check("k_index_score");
 }
 
-unsigned long long g_topk_a_done = 0, g_topk_b_done = 0;
 
 }  // namespace
 
@@ -196,10 +285,59 @@ lcc_status check_index_args(const char* name, const lcc_bf16* qI, const float* w
 
 lcc_status launch_scores(const IndexArgs& ia, int HI, int DI, lcc_key_format fmt, cudaStream_t s) {
   if (fmt == LCC_KEY_NVFP4) return launch_index_score<8, 64, true>(ia, s);
-  if (HI == 8 && DI == 64) return launch_index_score<8, 64, false>(ia, s);
-  if (HI == 8 && DI == 32) return launch_index_score<8, 32, false>(ia, s);
-  if (HI == 4 && DI == 64) return launch_index_score<4, 64, false>(ia, s);
-  return launch_index_score<4, 32, false>(ia, s);
+  if (HI == 8 && DI == 64) return launch_index_tc<8, 64>(ia, s);
+  if (HI == 8 && DI == 32) return launch_index_tc<8, 32>(ia, s);
+  if (HI == 4 && DI == 64) return launch_index_tc<4, 64>(ia, s);
+  return launch_index_tc<4, 32>(ia, s);
+}
+
+// Indexer + top-k over queries [0, Tq) in chunks of qc queries, with the
+// chunk scratch at `scratch` (index_ws_rows(B*qc, Ncap) bytes).
+lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI, const int64_t* q_pos0,
+                          lcc_key_format fmt, const void* kI, const uint8_t* kI_scale, const int32_t* n_valid,
+                          int Ncap, int m, int k, int32_t* idx, float* score, void* scratch, int qc,
+                          cudaStream_t s) {
+  const IndexWs ws = index_ws_rows(static_cast<int64_t>(B) * qc, Ncap);
+  char* base = static_cast<char*>(scratch);
+  float* scores = reinterpret_cast<float*>(base);
+  uint32_t* gmax = reinterpret_cast<uint32_t*>(base + ws.scores);
+  uint32_t* cand_k = reinterpret_cast<uint32_t*>(base + ws.scores + ws.gmax);
+  int32_t* cand_i = reinterpret_cast<int32_t*>(base + ws.scores + ws.gmax + ws.cand_k);
+  int* counters = reinterpret_cast<int*>(base + ws.scores + ws.gmax + ws.cand_k + ws.cand_i);
+  const int nseg = (Ncap + kTopkSeg - 1) / kTopkSeg;
+  for (int q0 = 0; q0 < Tq; q0 += qc) {
+    const int nq = qc < Tq - q0 ? qc : Tq - q0;
+    IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq,
+                 scores, gmax, gmax_stride(Ncap), counters};
+    lcc_status st = launch_scores(ia, HI, DI, fmt, s);
+    if (st != LCC_OK) return st;
+    TopkThrArgs ta{};
+    ta.scores = scores;
+    ta.gmax = gmax;
+    ta.gs = fmt == LCC_KEY_NVFP4 ? 16 : 32;
+    ta.g_stride = gmax_stride(Ncap);
+    ta.Ncap = Ncap;
+    ta.q_pos0 = q_pos0;
+    ta.n_valid = n_valid;
+    ta.m = m;
+    ta.Tq = Tq;
+    ta.q0 = q0;
+    ta.nq = nq;
+    ta.k = k;
+    ta.seg = kTopkSeg;
+    ta.cand_key = cand_k;
+    ta.cand_idx = cand_i;
+    ta.cap = kCandCap;
+    ta.cnt = counters;
+    ta.done = counters + static_cast<int64_t>(B) * nq;
+    ta.out_i = idx;
+    ta.out_s = score;
+    const int64_t rows = static_cast<int64_t>(B) * nq;
+    if (rows > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
+    k_topk_thr<kTopkNT, kCandCap><<<dim3(static_cast<unsigned>(rows), nseg), kTopkNT, 0, s>>>(ta);
+    if ((st = launch_check("k_topk_thr")) != LCC_OK) return st;
+  }
+  return LCC_OK;
 }
 }  // namespace
 
@@ -214,7 +352,8 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w, int B,
   if (B == 0 || Tq == 0) return LCC_OK;
   lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, scores);
   if (st != LCC_OK) return st;
-  IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, 0, Tq, scores};
+  IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, 0, Tq, scores,
+               nullptr, 0, nullptr};
   return launch_scores(ia, HI, DI, fmt, static_cast<cudaStream_t>(stream));
 }
 
@@ -229,70 +368,12 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, i
   lcc_status cst = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
   if (cst != LCC_OK) return cst;
   if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
-  const int nseg = (Ncap + kTopkCap - 1) / kTopkCap;
-  if (nseg > 1 && static_cast<int64_t>(nseg) * k > kTopkCap)
-    return fail(LCC_ERR_UNSUPPORTED, "%s: Ncap=%d with k=%d exceeds the two-stage top-k capacity", name, Ncap, k);
   const IndexWs ws = index_ws(B, Tq, Ncap, k);
   if (!workspace || workspace_bytes < ws.total)
     return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, ws.total);
   if (!aligned16(workspace)) return fail(LCC_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
-
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  {
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    lcc_status st = ensure_smem(k_topk<kTopkNT, kTopkCap, false>, kTopkCap * 4, g_topk_a_done);
-    if (st != LCC_OK) return st;
-    st = ensure_smem(k_topk<kTopkNT, kTopkCap, true>, kTopkCap * 8, g_topk_b_done);
-    if (st != LCC_OK) return st;
-  }
-  char* wsb = static_cast<char*>(workspace);
-  float* scores = reinterpret_cast<float*>(wsb);
-  float* cand_s = reinterpret_cast<float*>(wsb + ws.scores);
-  int32_t* cand_i = reinterpret_cast<int32_t*>(wsb + ws.scores + ws.cand_s);
-  const int qc = index_chunk(B, Tq, Ncap);
-  for (int q0 = 0; q0 < Tq; q0 += qc) {
-    const int nq = qc < Tq - q0 ? qc : Tq - q0;
-    IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq, scores};
-    lcc_status st = launch_scores(ia, HI, DI, fmt, s);
-    if (st != LCC_OK) return st;
-
-    TopkArgs ta{};
-    ta.scores = scores;
-    ta.Ncap = Ncap;
-    ta.q_pos0 = q_pos0;
-    ta.n_valid = n_valid;
-    ta.m = m;
-    ta.Tq = Tq;
-    ta.q0 = q0;
-    ta.nq = nq;
-    ta.k = k;
-    ta.seg = kTopkCap;
-    const int rows = B * nq;
-    if (nseg == 1) {
-      ta.out_i = idx;
-      ta.out_s = score;
-      ta.final_out = 1;
-      k_topk<kTopkNT, kTopkCap, false><<<dim3(1, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
-      if ((st = launch_check("k_topk")) != LCC_OK) return st;
-    } else {
-      ta.out_i = cand_i;
-      ta.out_s = cand_s;
-      ta.out_stride = static_cast<int64_t>(nseg) * k;
-      ta.final_out = 0;
-      k_topk<kTopkNT, kTopkCap, false><<<dim3(nseg, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
-      if ((st = launch_check("k_topk")) != LCC_OK) return st;
-      TopkArgs tb = ta;
-      tb.cand_s = cand_s;
-      tb.cand_i = cand_i;
-      tb.ncand = nseg * k;
-      tb.out_i = idx;
-      tb.out_s = score;
-      tb.final_out = 1;
-      k_topk<kTopkNT, kTopkCap, true><<<dim3(1, rows), kTopkNT, kTopkCap * 8, s>>>(tb);
-      if ((st = launch_check("k_topk merge")) != LCC_OK) return st;
-    }
-  }
-  return LCC_OK;
+  return run_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx, score, workspace,
+                        index_chunk(B, Tq, Ncap), static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"
@@ -300,24 +381,25 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, i
 // ------------------------------------------------------------------ attention
 namespace {
 
-unsigned long long g_attn_done[2][2][3] = {};
+unsigned long long g_attn_done[2][2][3][2] = {};
 
-template <int D, int ROWS, int MODE>
+template <int D, int ROWS, int MODE, bool WIN2>
 lcc_status launch_attn(const AttnArgs& a, dim3 grid, cudaStream_t s) {
   const size_t smem = AttnSmem<D, ROWS>::total;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
-    lcc_status st = ensure_smem(k_attn<D, ROWS, MODE>, smem, g_attn_done[D == 128][ROWS == 64][MODE]);
+    lcc_status st = ensure_smem(k_attn<D, ROWS, MODE, WIN2>, smem, g_attn_done[D == 128][ROWS == 64][MODE][WIN2]);
     if (st != LCC_OK) return st;
   }
-  k_attn<D, ROWS, MODE><<<grid, ROWS * 2, smem, s>>>(a);
+  k_attn<D, ROWS, MODE, WIN2><<<grid, ROWS * 2, smem, s>>>(a);
   return launch_check("k_attn");
 }
 
-template <int MODE>
+template <int MODE, bool WIN2 = false>
 lcc_status dispatch_attn(const AttnArgs& a, int D, dim3 grid, int rows, cudaStream_t s) {
-  if (D == 128) return rows == 64 ? launch_attn<128, 64, MODE>(a, grid, s) : launch_attn<128, 16, MODE>(a, grid, s);
-  return rows == 64 ? launch_attn<64, 64, MODE>(a, grid, s) : launch_attn<64, 16, MODE>(a, grid, s);
+  if (D == 128)
+    return rows == 64 ? launch_attn<128, 64, MODE, WIN2>(a, grid, s) : launch_attn<128, 16, MODE, WIN2>(a, grid, s);
+  return rows == 64 ? launch_attn<64, 64, MODE, WIN2>(a, grid, s) : launch_attn<64, 16, MODE, WIN2>(a, grid, s);
 }
 
 lcc_status check_attn_common(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, const lcc_bf16* K,
@@ -332,6 +414,56 @@ lcc_status check_attn_common(const char* name, const lcc_bf16* q, int B, int Tq,
   if (!aligned16(q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
     return fail(LCC_ERR_ALIGN, "%s: q, K, V and O must be 16-byte aligned", name);
   return LCC_OK;
+}
+
+// Key-range splits for a call with `rowblocks` CTAs per split and `keys`
+// keys per row: enough CTAs to cover the SMs twice, at least one 64-key
+// tile per split.
+int splits_for(int64_t rowblocks, int64_t keys) {
+  const int64_t target = 2 * num_sms();
+  if (rowblocks >= target) return 1;
+  int64_t ns = (target + rowblocks - 1) / rowblocks;
+  const int64_t tiles = (keys + 63) / 64;
+  if (ns > tiles) ns = tiles;
+  if (ns > 128) ns = 128;
+  return ns < 1 ? 1 : static_cast<int>(ns);
+}
+
+size_t split_ws_bytes(int ns, int64_t rows, int D) {
+  if (ns <= 1) return 0;
+  return round_up(ns * rows * D * sizeof(float), 256) + round_up(ns * rows * sizeof(float), 256);
+}
+
+// One pass over (compressed source ++ window rows) -> bf16 layer output.
+template <int MODE>
+lcc_status layer_attn_impl(const char* name, AttnArgs a, int D, int64_t rowblocks, unsigned gx, int rows_per_cta,
+                           int64_t keys, lcc_bf16* out, float* lse_out, void* workspace, size_t workspace_bytes,
+                           cudaStream_t s) {
+  const int ns = splits_for(rowblocks, keys);
+  const int64_t rowsT = static_cast<int64_t>(a.B) * a.Tq * a.H;
+  const size_t need = split_ws_bytes(ns, rowsT, D);
+  if (ns > 1 && (!workspace || workspace_bytes < need))
+    return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, need);
+  a.nsplit = ns;
+  a.rows_total = rowsT;
+  if (ns == 1) {
+    a.O = nullptr;
+    a.lse = lse_out;
+    a.out_bf16 = reinterpret_cast<bf16*>(out);
+    return dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, 1), rows_per_cta, s);
+  }
+  float* Op = static_cast<float*>(workspace);
+  float* lp = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(ns * rowsT * D * sizeof(float), 256));
+  a.O = Op;
+  a.lse = lp;
+  a.out_bf16 = nullptr;
+  lcc_status st = dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, ns), rows_per_cta, s);
+  if (st != LCC_OK) return st;
+  const unsigned g = static_cast<unsigned>((rowsT + 7) / 8);
+  bf16* ob = reinterpret_cast<bf16*>(out);
+  if (D == 128) k_split_combine<128><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, nullptr, lse_out, ob);
+  else k_split_combine<64><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, nullptr, lse_out, ob);
+  return launch_check("k_split_combine");
 }
 
 int dense_splits(int B, int Tq, int H, int Ncap) {
@@ -418,8 +550,8 @@ lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   st = dispatch_attn<ATT_RANGE>(a, D, dim3(static_cast<unsigned>(rblocks), B, ns), 64, s);
   if (st != LCC_OK) return st;
   const unsigned g = static_cast<unsigned>((rowsT + 7) / 8);
-  if (D == 128) k_split_combine<128><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse);
-  else k_split_combine<64><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse);
+  if (D == 128) k_split_combine<128><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse, nullptr);
+  else k_split_combine<64><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse, nullptr);
   return launch_check("k_split_combine");
 }
 
@@ -446,6 +578,87 @@ lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float sc
   a.O = O; a.lse = lse; a.nsplit = 1; a.rows_total = static_cast<int64_t>(B) * Tq * H;
   return dispatch_attn<ATT_WINDOW>(a, D, dim3(static_cast<unsigned>(rblocks), B, 1), 64,
                                    static_cast<cudaStream_t>(stream));
+}
+
+size_t lcc_layer_attn_workspace(int B, int Tq, int H, int D, int n_keys) {
+  if (B <= 0 || Tq <= 0 || H <= 0 || D <= 0 || n_keys <= 0) return 0;
+  // the CSA layer's CTAs hold one query (H <= 64 heads), the HCA layer's 64 rows
+  const int64_t rb_csa = static_cast<int64_t>(B) * Tq * ((H + 63) / 64);
+  const int64_t rb_hca = static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 63) / 64);
+  const int64_t rb = rb_csa < rb_hca ? rb_csa : rb_hca;
+  return split_ws_bytes(splits_for(rb, n_keys), static_cast<int64_t>(B) * Tq * H, D);
+}
+
+lcc_status lcc_csa_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride,
+                              int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  const char* name = "lcc_csa_layer_attn";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  if (!out) return fail(LCC_ERR_ARG, "%s: null out", name);
+  const float* dummy = reinterpret_cast<const float*>(out);
+  lcc_status st = check_attn_common(name, q, B, Tq, H, D, Kc, Vc, kv_rstride, Ncap, dummy, dummy);
+  if (st != LCC_OK) return st;
+  st = check_attn_common(name, q, B, Tq, H, D, Kr, Vr, r_rstride, Rcap, dummy, dummy);
+  if (st != LCC_OK) return st;
+  if (!idx || !q_pos0 || !raw_pos0) return fail(LCC_ERR_ARG, "%s: null idx / q_pos0 / raw_pos0", name);
+  if (k < 1 || k > 4096) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..4096)", name, k);
+  if (W < 1 || W > 4096) return fail(LCC_ERR_SHAPE, "%s: W=%d (supported: 1..4096)", name, W);
+  AttnArgs a{};
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.B = B; a.Tq = Tq; a.H = H;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.q_pos0 = q_pos0;
+  a.K = reinterpret_cast<const bf16*>(Kc); a.V = reinterpret_cast<const bf16*>(Vc);
+  a.kv_bs = static_cast<int64_t>(Ncap) * kv_rstride; a.kv_rs = kv_rstride; a.Ncap = Ncap;
+  a.idx = idx; a.k = k;
+  a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
+  a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
+  a.raw_pos0 = raw_pos0; a.W = W;
+  const int rows = H <= 16 ? 16 : 64;
+  const int hblocks = (H + rows - 1) / rows;
+  if (static_cast<int64_t>(Tq) * hblocks > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many queries", name);
+  const int64_t rowblocks = static_cast<int64_t>(B) * Tq * hblocks;
+  return layer_attn_impl<ATT_GATHER>(name, a, D, rowblocks, static_cast<unsigned>(Tq * hblocks), rows,
+                                     static_cast<int64_t>(k) + W, out, lse_out, workspace, workspace_bytes,
+                                     static_cast<cudaStream_t>(stream));
+}
+
+lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* n_valid, int m, const lcc_bf16* Kr, const lcc_bf16* Vr,
+                              int64_t r_rstride, int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out,
+                              float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* name = "lcc_hca_layer_attn";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  if (!out) return fail(LCC_ERR_ARG, "%s: null out", name);
+  const float* dummy = reinterpret_cast<const float*>(out);
+  lcc_status st = check_attn_common(name, q, B, Tq, H, D, Kc, Vc, kv_rstride, Ncap, dummy, dummy);
+  if (st != LCC_OK) return st;
+  st = check_attn_common(name, q, B, Tq, H, D, Kr, Vr, r_rstride, Rcap, dummy, dummy);
+  if (st != LCC_OK) return st;
+  if (!q_pos0 || !n_valid || !raw_pos0) return fail(LCC_ERR_ARG, "%s: null q_pos0 / n_valid / raw_pos0", name);
+  if (m < 1) return fail(LCC_ERR_SHAPE, "%s: m=%d", name, m);
+  if (W < 1 || W > 4096) return fail(LCC_ERR_SHAPE, "%s: W=%d (supported: 1..4096)", name, W);
+  const int64_t rblocks = (static_cast<int64_t>(Tq) * H + 63) / 64;
+  if (rblocks > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many queries", name);
+  AttnArgs a{};
+  a.q = reinterpret_cast<const bf16*>(q);
+  a.B = B; a.Tq = Tq; a.H = H;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.q_pos0 = q_pos0;
+  a.K = reinterpret_cast<const bf16*>(Kc); a.V = reinterpret_cast<const bf16*>(Vc);
+  a.kv_bs = static_cast<int64_t>(Ncap) * kv_rstride; a.kv_rs = kv_rstride; a.Ncap = Ncap;
+  a.n_valid = n_valid; a.m = m;
+  a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
+  a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
+  a.raw_pos0 = raw_pos0; a.W = W;
+  return layer_attn_impl<ATT_RANGE>(name, a, D, static_cast<int64_t>(B) * rblocks, static_cast<unsigned>(rblocks),
+                                    64, static_cast<int64_t>(Ncap) + W, out, lse_out, workspace, workspace_bytes,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 lcc_status lcc_attn_merge(int nb, const float* const* O_parts, const float* const* lse_parts, int64_t rows, int D,
@@ -517,76 +730,19 @@ extern "C" lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const
   lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
   if (st != LCC_OK) return st;
   if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
-  const int nseg = (Ncap + kTopkCap - 1) / kTopkCap;
-  if (nseg > 1 && static_cast<int64_t>(nseg) * k > kTopkCap)
-    return fail(LCC_ERR_UNSUPPORTED, "%s: Ncap=%d with k=%d exceeds the two-stage top-k capacity", name, Ncap, k);
-  // bytes one query row of every batch needs: scores + (two-stage) candidate lists
-  const size_t per_q_scores = static_cast<size_t>(B) * Ncap * sizeof(float);
-  const size_t per_q_cand = nseg > 1 ? static_cast<size_t>(B) * nseg * k * sizeof(float) : 0;
-  const size_t per_q = round_up(per_q_scores, 256) + 2 * round_up(per_q_cand, 256);
+  // bytes one query row of every batch needs: scores, group maxima, candidates, counters
+  const size_t per_q = index_ws_rows(B, Ncap).total;
   if (per_q > kNoAllocScratchBytes)
     return fail(LCC_ERR_WORKSPACE, "%s: one query row needs %zu scratch bytes, the fixed scratch holds %zu", name,
                 per_q, kNoAllocScratchBytes);
-  int qc = 1;  // largest query chunk whose scores and candidates fit the scratch
+  int qc = 1;  // largest query chunk whose scratch fits the array
   while (qc < Tq) {
     const int nx = qc * 2 < Tq ? qc * 2 : Tq;
-    const size_t need = round_up(per_q_scores * nx, 256) + 2 * round_up(per_q_cand * nx, 256);
-    if (need > kNoAllocScratchBytes) break;
+    if (index_ws_rows(static_cast<int64_t>(B) * nx, Ncap).total > kNoAllocScratchBytes) break;
     qc = nx;
   }
   void* scratch = nullptr;
   if ((st = noalloc_scratch(&scratch)) != LCC_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  {
-    std::lock_guard<std::mutex> lk(g_attr_mu);
-    if ((st = ensure_smem(k_topk<kTopkNT, kTopkCap, false>, kTopkCap * 4, g_topk_a_done)) != LCC_OK) return st;
-    if ((st = ensure_smem(k_topk<kTopkNT, kTopkCap, true>, kTopkCap * 8, g_topk_b_done)) != LCC_OK) return st;
-  }
-  char* base = static_cast<char*>(scratch);
-  float* scores = reinterpret_cast<float*>(base);
-  const size_t sc_bytes = round_up(per_q_scores * qc, 256);
-  const size_t cand_bytes = round_up(per_q_cand * qc, 256);
-  float* cand_s = reinterpret_cast<float*>(base + sc_bytes);
-  int32_t* cand_i = reinterpret_cast<int32_t*>(base + sc_bytes + cand_bytes);
-  for (int q0 = 0; q0 < Tq; q0 += qc) {
-    const int nq = qc < Tq - q0 ? qc : Tq - q0;
-    IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq, scores};
-    if ((st = launch_scores(ia, HI, DI, fmt, s)) != LCC_OK) return st;
-    TopkArgs ta{};
-    ta.scores = scores;
-    ta.Ncap = Ncap;
-    ta.q_pos0 = q_pos0;
-    ta.n_valid = n_valid;
-    ta.m = m;
-    ta.Tq = Tq;
-    ta.q0 = q0;
-    ta.nq = nq;
-    ta.k = k;
-    ta.seg = kTopkCap;
-    const int rows = B * nq;
-    if (nseg == 1) {
-      ta.out_i = idx;
-      ta.out_s = score;
-      ta.final_out = 1;
-      k_topk<kTopkNT, kTopkCap, false><<<dim3(1, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
-      if ((st = launch_check("k_topk")) != LCC_OK) return st;
-    } else {
-      ta.out_i = cand_i;
-      ta.out_s = cand_s;
-      ta.out_stride = static_cast<int64_t>(nseg) * k;
-      ta.final_out = 0;
-      k_topk<kTopkNT, kTopkCap, false><<<dim3(nseg, rows), kTopkNT, kTopkCap * 4, s>>>(ta);
-      if ((st = launch_check("k_topk")) != LCC_OK) return st;
-      TopkArgs tb = ta;
-      tb.cand_s = cand_s;
-      tb.cand_i = cand_i;
-      tb.ncand = nseg * k;
-      tb.out_i = idx;
-      tb.out_s = score;
-      tb.final_out = 1;
-      k_topk<kTopkNT, kTopkCap, true><<<dim3(1, rows), kTopkNT, kTopkCap * 8, s>>>(tb);
-      if ((st = launch_check("k_topk merge")) != LCC_OK) return st;
-    }
-  }
-  return LCC_OK;
+  return run_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx, score, scratch, qc,
+                        static_cast<cudaStream_t>(stream));
 }

@@ -79,11 +79,12 @@ __global__ void __launch_bounds__(256) k_merge(MergeArgs a) {
 }
 
 // Reduction of `nsplit` key-range partials stored [nsplit][rows][D] and
-// [nsplit][rows] into O [rows][D] and lse [rows].
+// [nsplit][rows] into O [rows][D] fp32 and/or out [rows][D] bf16, and lse
+// [rows] (each output optional).
 template <int D>
 __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__ Op, const float* __restrict__ lp,
                                                        int nsplit, int64_t rows, float* __restrict__ O,
-                                                       float* __restrict__ lse) {
+                                                       float* __restrict__ lse, bf16* __restrict__ out) {
   constexpr int PER = D / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -107,10 +108,25 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
     }
   }
   const float inv = tot > 0.f ? 1.0f / tot : 0.f;
-  float* dst = O + row * D + lane * PER;
 #pragma unroll
-  for (int e = 0; e < PER; ++e) dst[e] = acc[e] * inv;
-  if (lane == 0) lse[row] = (L == -INFINITY) ? -INFINITY : L + logf(tot);
+  for (int e = 0; e < PER; ++e) acc[e] *= inv;
+  if (O) {
+    float* dst = O + row * D + lane * PER;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) dst[e] = acc[e];
+  }
+  if (out) {
+    bf16* dst = out + row * D + lane * PER;
+    if constexpr (PER == 4) {
+      uint2 o;
+      o.x = pack_bf16(acc[0], acc[1]);
+      o.y = pack_bf16(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(dst) = o;
+    } else {
+      *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+    }
+  }
+  if (lse && lane == 0) lse[row] = (L == -INFINITY) ? -INFINITY : L + logf(tot);
 }
 
 }  // namespace lcc

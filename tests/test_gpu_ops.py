@@ -278,3 +278,58 @@ def test_merge_parity(nb, D):
     assert_close(out.float().cpu().numpy(), Oo, "merge bf16")
     assert_lse_close(lse_out.cpu().numpy(), Lo, "merge lse", tol=1e-5)
     assert np.all(out_f32.cpu().numpy()[L_all_empty] == 0)
+
+
+# ---------------------------------------------------------------------------
+# whole layers in one pass: compressed keys ++ window keys, one softmax
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("B,Tq,H,D,k,W", [(3, 1, 64, 128, 128, 128), (2, 40, 8, 64, 16, 32), (1, 7, 16, 128, 70, 100)])
+def test_csa_layer_attn_parity(B, Tq, H, D, k, W):
+    Ncap, R = 400, 160
+    q = datagen.normal_bf16(36, 4, (B, Tq, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(36, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(36, 9, (B, Ncap, D))
+    Kr = datagen.normal_bf16(36, 1, (B, R, D))
+    Vr = datagen.normal_bf16(36, 2, (B, R, D))
+    vis = torch.tensor(([Ncap, 3, 0, k, 200] * (B * Tq))[: B * Tq])
+    idx = datagen.random_index_lists(36, 17, vis, k).reshape(B, Tq, k)
+    raw0 = [500 + 30 * b for b in range(B)]
+    qpos = [raw0[b] + R - Tq - 5 * b for b in range(B)]
+    lse = torch.empty((B, Tq, H), dtype=torch.float32, device=DEV)
+    out = lcc.csa_layer_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV), idx.to(DEV), Kr.to(DEV), Vr.to(DEV),
+                             torch.tensor(qpos, device=DEV), torch.tensor(raw0, device=DEV), W, lse_out=lse)
+    lcc.sync_status()
+    for b in range(B):
+        for i in range(Tq):
+            sel = idx[b, i].numpy()
+            sel = sel[sel >= 0]
+            cO, cL = oracle.attend(f64(q[b, i]), f64(Kc[b])[sel], f64(Vc[b])[sel])
+            sw = runs.swa_branch(f64(q[b, i]), qpos[b] + i, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
+            O, L = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
+            assert_close(out[b, i].float().cpu().numpy(), O, f"CSA layer [{b},{i}]")
+            assert_lse_close(lse[b, i].cpu().numpy(), L, f"CSA layer lse [{b},{i}]")
+
+
+@pytest.mark.parametrize("B,Tq,H,D,m,W", [(3, 1, 64, 128, 128, 128), (1, 300, 8, 64, 4, 32), (2, 9, 64, 128, 4, 128)])
+def test_hca_layer_attn_parity(B, Tq, H, D, m, W):
+    Ncap, R = 700, 300
+    q = datagen.normal_bf16(37, 4, (B, Tq, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(37, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(37, 9, (B, Ncap, D))
+    Kr = datagen.normal_bf16(37, 1, (B, R, D))
+    Vr = datagen.normal_bf16(37, 2, (B, R, D))
+    n_valid = [Ncap, 37, 0][:B] if Tq == 1 else [Ncap] * B
+    # decode: queries far into the context; prefill: the raw buffer starts at 0 and queries at 0
+    qpos = [m * Ncap + 5] * B if Tq == 1 else [0] * B
+    raw0 = [qpos[b] + Tq - R + 3 for b in range(B)] if Tq == 1 else [0] * B
+    out = lcc.hca_layer_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV),
+                             torch.tensor(n_valid, dtype=torch.int32, device=DEV), m, Kr.to(DEV), Vr.to(DEV),
+                             torch.tensor(qpos, device=DEV), torch.tensor(raw0, device=DEV), W)
+    lcc.sync_status()
+    for b in range(B):
+        for i in range(Tq):
+            t = qpos[b] + i
+            h = runs.hca_branch(f64(q[b, i]), t, f64(Kc[b]), f64(Vc[b]), m, n_valid=n_valid[b])
+            sw = runs.swa_branch(f64(q[b, i]), t, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
+            O, _ = oracle.merge([h["O"], sw["O"]], [h["lse"], sw["lse"]])
+            assert_close(out[b, i].float().cpu().numpy(), O, f"HCA layer [{b},{i}]")

@@ -88,12 +88,17 @@ def test_tiny_prefill_all_rows():
 def test_csa_decode_full():
     cfg = wl.CsaDecode()
     g = cfg.make(DEV)
-    plan = CsaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.k, cfg.W)
+    plan = CsaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.k, cfg.W, fused=False)
     out = plan(g["q"], g["qI"], g["w"], cfg.q_pos, g["kI"], cfg.N, g["Kc"], g["Vc"], g["Kr"], g["Vr"],
                cfg.raw_pos0)
+    fplan = CsaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.k, cfg.W)
+    fout = fplan(g["q"], g["qI"], g["w"], cfg.q_pos, g["kI"], cfg.N, g["Kc"], g["Vc"], g["Kr"], g["Vr"],
+                 cfg.raw_pos0)
     lcc.sync_status()
     gi = plan.idx.cpu().numpy()[:, 0]
+    assert np.array_equal(gi, fplan.idx.cpu().numpy()[:, 0])
     gout = out.float().cpu().numpy()[:, 0]
+    gfout = fout.float().cpu().numpy()[:, 0]
     s = cfg.seed
     kI = f64(datagen.normal_bf16(s, wl.T_KI, (cfg.B, cfg.N, cfg.DI)))
     qI = f64(datagen.normal_bf16(s, wl.T_QI, (cfg.B, 1, cfg.HI, cfg.DI)))
@@ -117,6 +122,7 @@ def test_csa_decode_full():
         sw = runs.swa_branch(q[b, 0], cfg.q_pos, Kr[b], Vr[b], cfg.raw_pos0, cfg.W)
         O, _ = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
         assert_close(gout[b], O, f"CSA decode batch {b}")
+        assert_close(gfout[b], O, f"fused CSA decode batch {b}")
         assert_close(plan.O_c[b, 0].cpu().numpy(), cO, f"sparse branch {b}")
         assert_lse_close(plan.L_c[b, 0].cpu().numpy(), cL, f"sparse lse {b}")
     assert near <= 1
@@ -170,14 +176,18 @@ def test_hca_decode_full():
     cfg = wl.HcaDecode()
     inp = cfg.make()
     g = up(inp)
-    plan = HcaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.W)
+    plan = HcaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.W, fused=False)
     out = plan(g["q"], cfg.q_pos, g["Kc"], g["Vc"], cfg.N, g["Kr"], g["Vr"], cfg.raw_pos0)
+    fplan = HcaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.W)
+    fout = fplan(g["q"], cfg.q_pos, g["Kc"], g["Vc"], cfg.N, g["Kr"], g["Vr"], cfg.raw_pos0)
     lcc.sync_status()
     ref = runs.hca_decode({k: host(v) for k, v in inp.items()}, cfg)
     gout = out.float().cpu().numpy()[:, 0]
+    gfout = fout.float().cpu().numpy()[:, 0]
     for r in ref:
         b = r["b"]
         assert_close(gout[b], r["layer"][0], f"HCA decode batch {b}")
+        assert_close(gfout[b], r["layer"][0], f"fused HCA decode batch {b}")
         assert_close(plan.O_h[b, 0].cpu().numpy(), r["hca"]["O"], f"dense branch {b}")
         assert_lse_close(plan.L_h[b, 0].cpu().numpy(), r["hca"]["lse"], f"dense lse {b}")
 
