@@ -121,7 +121,7 @@ def peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
 
 
-KERNEL_SOURCES = {"k_index_score": ["common.cuh", "index.cuh"]}
+KERNEL_SOURCES = {"k_index_tc": ["common.cuh", "tc.cuh", "index_tc.cuh"]}
 
 
 def csrc_hash(kernel: str):
@@ -168,11 +168,28 @@ def time_graph(graph_runs, stream):
 
 
 # ---------------------------------------------------------------------------
-# workload: CSA decode (batch 32, 16384 entries)
+# workloads.  Each defines one step (graph-capturable), the units it
+# processes, the dominant kernel and its algorithmic bytes or FLOPs.
 # ---------------------------------------------------------------------------
+def _visible_pairs(T, m, q0=0, n_cap=None):
+    """Sum over queries t in [q0, q0+T) of the visible compressed entries."""
+    t = np.arange(q0, q0 + T, dtype=np.int64)
+    v = (t + 1) // m
+    if n_cap is not None:
+        v = np.minimum(v, n_cap)
+    return int(v.sum())
+
+
+def _window_pairs(T, W, q0=0, raw_pos0=0):
+    t = np.arange(q0, q0 + T, dtype=np.int64)
+    lo = np.maximum(np.maximum(t - W + 1, 0), raw_pos0)
+    return int((t - lo + 1).sum())
+
+
 class CsaDecodeBench:
     unit = "queries/s"
     name = "csa_decode"
+    rotate = True
 
     def __init__(self):
         from datagen.workloads import CsaDecode
@@ -207,38 +224,32 @@ class CsaDecodeBench:
         self.nval = torch.full((c.B,), c.N, dtype=torch.int32, device=dev)
         self.scores = torch.empty((c.B, 1, c.N), dtype=torch.float32, device=dev)
 
-    def step(self, r):
-        s = self.sets[r]
-        return self.plan(s["q"], s["qI"], s["w"], self.pos, s["kI"], self.nval, s["Kc"], s["Vc"],
-                         s["Kr"], s["Vr"], self.raw0)
+    graph_steps = 64
+
+    def run_steps(self, i0, n):
+        for i in range(i0, i0 + n):
+            s = self.sets[i % NSETS]
+            self.plan(s["q"], s["qI"], s["w"], self.pos, s["kI"], self.nval, s["Kc"], s["Vc"],
+                      s["Kr"], s["Vr"], self.raw0)
 
     # dominant kernel: indexer scoring (streams 2 MiB of keys per query)
-    dominant = "k_index_score"
+    dominant = "k_index_tc"
+    bound = "hbm"
 
-    def dominant_launch(self, r):
+    def dominant_steps(self, i0, n):
         import long_context_compressed_15_b300 as lcc
-        s = self.sets[r]
-        lcc.lightning_index_scores(s["qI"], s["w"], self.pos, s["kI"], self.nval, 4, scores=self.scores)
+        for i in range(i0, i0 + n):
+            s = self.sets[i % NSETS]
+            lcc.lightning_index_scores(s["qI"], s["w"], self.pos, s["kI"], self.nval, 4, scores=self.scores)
 
-    def dominant_bytes(self):
+    def dominant_work(self):
         c = self.cfg
         return c.B * (c.N * c.DI * 2 + c.HI * c.DI * 2 + c.HI * 4 + c.N * 4)
 
-    # end to end through the public API: queries in from pinned host memory, output back
-    def e2e_setup(self):
+    # end to end: the step's queries come from pinned host memory, the layer output goes back
+    def e2e_io(self):
         s = self.sets[0]
-        self.h_in = {k: s[k].cpu().pin_memory() for k in ("q", "qI", "w")}
-        self.h_out = torch.empty(self.plan.out.shape, dtype=torch.bfloat16).pin_memory()
-        return sum(v.numel() * v.element_size() for v in self.h_in.values()), \
-            self.h_out.numel() * self.h_out.element_size()
-
-    def e2e_step(self, graph0):
-        s = self.sets[0]
-        for k, v in self.h_in.items():
-            s[k].copy_(v, non_blocking=True)
-        graph0.replay()
-        self.h_out.copy_(self.plan.out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
+        return [s["q"], s["qI"], s["w"]], self.plan.out
 
     # fp64 oracle on a bounded sample of the workload
     def oracle_sample(self, budget_s, max_queries=None):
@@ -274,6 +285,7 @@ class CsaDecodeBench:
         return done, t_oracle, f"{done} decode queries of the batch (inputs regenerated on the host, untimed)"
 
 
+
 def _host_rows(seed, tid, b, n, d, scale=1.0):
     """Rows [b*n, (b+1)*n) of a [*, d] bf16 tensor, as float64."""
     import datagen
@@ -292,94 +304,392 @@ def _host_entry_rows(seed, tid, rows, d):
     return runs.f64(t.view(torch.int16).numpy().view(np.uint16))
 
 
-WORKLOADS = {"csa_decode": CsaDecodeBench}
+class HcaDecodeBench:
+    """HCA layer decode at 1M context: batch 8, 8192 m=128 entries + 128-token window."""
+    unit = "queries/s"
+    name = "hca_decode"
+    dominant = "k_attn<RANGE+window>+k_split_combine"
+    bound = "hbm"
+    graph_steps = 64
+
+    def __init__(self):
+        from datagen.workloads import HcaDecode
+        self.cfg = HcaDecode()
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "hca_decode: HCA layer decode, batch 8, 1048576-token context, 8192 m=128 entries, "
+                            "window 128, 64 heads x 128", "batch": c.B, "entries": c.N,
+                "l2": f"{NSETS} rotating input sets"}
+
+    def units_per_step(self):
+        return self.cfg.B
+
+    def setup(self, dev):
+        from long_context_compressed_15_b300.layers import HcaLayerPlan
+        c = self.cfg
+        self.sets = [c.make(dev, rot=r) for r in range(NSETS)]
+        self.plan = HcaLayerPlan(c.B, 1, c.H, c.D, c.N, c.W, device=dev)
+        self.pos = torch.full((c.B,), c.q_pos, dtype=torch.int64, device=dev)
+        self.raw0 = torch.full((c.B,), c.raw_pos0, dtype=torch.int64, device=dev)
+        self.nval = torch.full((c.B,), c.N, dtype=torch.int32, device=dev)
+
+    def run_steps(self, i0, n):
+        for i in range(i0, i0 + n):
+            s = self.sets[i % NSETS]
+            self.plan(s["q"], self.pos, s["Kc"], s["Vc"], self.nval, s["Kr"], s["Vr"], self.raw0)
+
+    def dominant_steps(self, i0, n):
+        self.run_steps(i0, n)
+
+    def dominant_work(self):
+        c = self.cfg
+        return c.B * ((c.N + c.W) * 2 * c.D * 2 + 2 * c.H * c.D * 2)
+
+    def e2e_io(self):
+        return [self.sets[0]["q"]], self.plan.out
+
+
+class PairDecodeBench:
+    """Interleaved CSA/HCA layer pair decode at 1M context, batch 4, NVFP4 indexer keys, 64 steps."""
+    unit = "queries/s"
+    name = "pair_decode"
+    dominant = "k_index_score<NVFP4>"
+    bound = "hbm"
+    graph_steps = 64
+
+    def __init__(self):
+        from datagen.workloads import PairDecode
+        self.cfg = PairDecode()
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "pair_decode: CSA+HCA layer pair decode, batch 4, 1048576-token context, "
+                            "262144 CSA entries with NVFP4 indexer keys 8x64, 8192 HCA entries, top-128, "
+                            "window 128, one new token per step (a CSA block pooled every 4 steps)",
+                "batch": c.B, "steps_per_run": c.steps, "unit_note": "one query per sequence per step, "
+                "counted once for the layer pair"}
+
+    def units_per_step(self):
+        return self.cfg.B
+
+    def setup(self, dev):
+        from long_context_compressed_15_b300.layers import CsaLayerPlan, HcaLayerPlan
+        c = self.cfg
+        self.g = c.make(dev)
+        self.csa = CsaLayerPlan(c.B, 1, c.H, c.D, c.Ncap_csa, c.k, c.W, device=dev)
+        self.hca = HcaLayerPlan(c.B, 1, c.H, c.D, c.N_hca, c.W, device=dev)
+        self.nval = torch.full((c.B,), c.N_csa, dtype=torch.int32, device=dev)
+        self.nval_h = torch.full((c.B,), c.N_hca, dtype=torch.int32, device=dev)
+        self.pos = [torch.full((c.B,), c.ctx + s, dtype=torch.int64, device=dev) for s in range(c.steps)]
+        self.raw0 = torch.full((c.B,), c.raw_pos0, dtype=torch.int64, device=dev)
+        self.scores = torch.empty((c.B, 1, c.Ncap_csa), dtype=torch.float32, device=dev)
+
+    def _step(self, s):
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
+        pos = c.ctx + s
+        if s == 0:
+            self.nval.fill_(c.N_csa)
+        if (pos + 1) % c.m_csa == 0:
+            j = (pos + 1) // c.m_csa - 1
+            r1 = c.W + s + 1
+            lcc.csa_compress(g["Kr"][:, r1 - 4:r1], g["Vr"][:, r1 - 4:r1], g["gate"][:, r1 - 4:r1],
+                             g["Kc"][:, j:j + 1], g["Vc"][:, j:j + 1], n_blocks=1)
+            self.nval.add_(1)
+        q = g["q"][s][:, None]
+        self.csa(q, g["qI"][s][:, None], g["w"][s][:, None], self.pos[s], g["kI_packed"], self.nval, g["Kc"],
+                 g["Vc"], g["Kr"], g["Vr"], self.raw0, kI_scale=g["kI_scale"])
+        self.hca(q, self.pos[s], g["Kc_h"], g["Vc_h"], self.nval_h, g["Kr_h"], g["Vr_h"], self.raw0)
+
+    def run_steps(self, i0, n):
+        for i in range(i0, i0 + n):
+            self._step(i % self.cfg.steps)
+
+    def dominant_steps(self, i0, n):
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
+        for i in range(i0, i0 + n):
+            s = i % c.steps
+            lcc.lightning_index_scores(g["qI"][s][:, None], g["w"][s][:, None], self.pos[s], g["kI_packed"],
+                                       c.N_csa, c.m_csa, kI_scale=g["kI_scale"], scores=self.scores)
+
+    def dominant_work(self):
+        c = self.cfg
+        return c.B * (c.N_csa * (c.DI // 2 + c.DI // 16) + c.HI * c.DI * 2 + c.HI * 4 + c.N_csa * 4)
+
+    def e2e_io(self):
+        g = self.g
+        return [g["q"][0], g["qI"][0], g["w"][0]], self.hca.out
+
+
+class CsaPrefillBench:
+    """CSA layer prefill of one 131072-token sequence (pool, indexer + top-k, sparse + window attention)."""
+    unit = "tokens/s"
+    name = "csa_prefill"
+    dominant = "k_index_tc+k_topk_thr"
+    bound = "tensor"
+    graph_steps = 1
+
+    def __init__(self):
+        from datagen.workloads import CsaPrefill
+        self.cfg = CsaPrefill()
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "csa_prefill: CSA layer prefill, 131072 tokens, causal, m=4 (32768 entries), "
+                            "indexer 8x64 top-128, window 128, 64 heads x 128", "tokens": c.T}
+
+    def units_per_step(self):
+        return self.cfg.T
+
+    def setup(self, dev):
+        from long_context_compressed_15_b300.layers import CsaLayerPlan
+        c = self.cfg
+        self.g = c.make(dev)
+        self.Kc = torch.empty((1, c.N, c.D), dtype=torch.bfloat16, device=dev)
+        self.Vc = torch.empty_like(self.Kc)
+        self.plan = CsaLayerPlan(1, c.T, c.H, c.D, c.N, c.k, c.W, device=dev)
+
+    def run_steps(self, i0, n):
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
+        for _ in range(n):
+            lcc.csa_compress(g["K"], g["V"], g["gate"], self.Kc, self.Vc)
+            self.plan(g["q"], g["qI"], g["w"], 0, g["kI"], c.N, self.Kc, self.Vc, g["K"], g["V"], 0)
+
+    def dominant_steps(self, i0, n):
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
+        for _ in range(n):
+            lcc.lightning_index_topk(g["qI"], g["w"], 0, g["kI"], c.N, c.m, c.k, idx=self.plan.idx,
+                                     workspace=self.plan.ws)
+
+    def dominant_work(self):
+        c = self.cfg
+        return 2.0 * c.HI * c.DI * _visible_pairs(c.T, c.m)
+
+    def e2e_io(self):
+        g = self.g
+        return [g["K"], g["V"], g["gate"], g["q"], g["qI"], g["w"], g["kI"]], self.plan.out
+
+    def extra(self):
+        c = self.cfg
+        t = np.arange(c.T, dtype=np.int64)
+        sel = np.minimum((t + 1) // c.m, c.k).sum()
+        return {"indexer_tflop": round(self.dominant_work() / 1e12, 3),
+                "attention_tflop": round(4.0 * c.H * c.D * (sel + _window_pairs(c.T, c.W)) / 1e12, 3)}
+
+
+class HcaPrefillBench:
+    """HCA layer prefill of a 32768-token chunk on a 1M-token context (pool 256 blocks, dense + window)."""
+    unit = "tokens/s"
+    name = "hca_prefill"
+    dominant = "k_attn_tc<RANGE+window>"
+    bound = "tensor"
+    graph_steps = 1
+
+    def __init__(self):
+        from datagen.workloads import HcaPrefill
+        self.cfg = HcaPrefill()
+
+    def config(self):
+        c = self.cfg
+        return {"workload": "hca_prefill: HCA layer prefill of a 32768-token chunk at position 1048576, "
+                            "256 new m=128 blocks pooled, 8448 entries, window 128, 64 heads x 128",
+                "tokens": c.Tc}
+
+    def units_per_step(self):
+        return self.cfg.Tc
+
+    def setup(self, dev):
+        from long_context_compressed_15_b300.layers import HcaLayerPlan
+        c = self.cfg
+        self.g = c.make(dev)
+        self.plan = HcaLayerPlan(1, c.Tc, c.H, c.D, c.Ncap, c.W, device=dev)
+        self.r0 = c.W - 1
+
+    def run_steps(self, i0, n):
+        import long_context_compressed_15_b300 as lcc
+        c, g, r0 = self.cfg, self.g, self.r0
+        for _ in range(n):
+            lcc.hca_compress(g["Kr"][:, r0:], g["Vr"][:, r0:], g["gate"][:, r0:], g["Kc"][:, c.N0:],
+                             g["Vc"][:, c.N0:], n_blocks=c.Tc // c.m)
+            self.plan(g["q"], c.q_pos0, g["Kc"], g["Vc"], c.Ncap, g["Kr"], g["Vr"], c.raw_pos0)
+
+    def dominant_steps(self, i0, n):
+        c, g = self.cfg, self.g
+        for _ in range(n):
+            self.plan(g["q"], c.q_pos0, g["Kc"], g["Vc"], c.Ncap, g["Kr"], g["Vr"], c.raw_pos0)
+
+    def dominant_work(self):
+        c = self.cfg
+        keys = _visible_pairs(c.Tc, c.m, q0=c.ctx, n_cap=c.Ncap) + _window_pairs(c.Tc, c.W, q0=c.ctx,
+                                                                                  raw_pos0=c.raw_pos0)
+        return 4.0 * c.H * c.D * keys
+
+    def e2e_io(self):
+        g = self.g
+        return [g["Kr"], g["Vr"], g["gate"], g["q"]], self.plan.out
+
+
+WORKLOADS = {"csa_decode": CsaDecodeBench, "hca_decode": HcaDecodeBench, "pair_decode": PairDecodeBench,
+             "csa_prefill": CsaPrefillBench, "hca_prefill": HcaPrefillBench}
 
 
 # ---------------------------------------------------------------------------
+def capture(fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+class Schedule:
+    """Graphs of G steps plus graphs of the remainder, replayed to run exactly n steps."""
+
+    def __init__(self, wb):
+        self.wb = wb
+        self.G = wb.graph_steps
+        self.big = capture(lambda: wb.run_steps(0, self.G))
+        self.rem = {}
+
+    def runs(self, n):
+        r = n % self.G
+        if r and r not in self.rem:
+            self.rem[r] = capture(lambda: self.wb.run_steps(0, r))
+        return [self.big] * (n // self.G) + ([self.rem[r]] if r else [])
+
+
+def roofline_of(wb, stream, reps_hint, pk):
+    """Dominant kernel alone, in a graph on the bench stream, timed with CUDA events."""
+    G = wb.graph_steps
+    dg = capture(lambda: wb.dominant_steps(0, G))
+    time_graph([dg], stream)
+    reps = max(2, reps_hint)
+    td = time_graph([dg] * reps, stream) / (reps * G)
+    work = wb.dominant_work()
+    if wb.bound == "hbm":
+        achieved, peak, unit = work / td / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        achieved, peak, unit = work / td / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    return {"bound": wb.bound, "kernel": wb.dominant, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wb.dominant, wb.name),
+            "peak_source": pk["source"], "launch_us": round(td * 1e6, 3)}
+
+
+def e2e_of(wb, ws, n_steps):
+    """The same metric through the public API: per step, the step's inputs are copied in from pinned
+    host memory, the step runs (one-step graph) and the layer output is read back, synchronised."""
+    ins, out = wb.e2e_io()
+    h_in = [t.cpu().pin_memory() for t in ins]
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    g1 = capture(lambda: wb.run_steps(0, 1))
+
+    def one():
+        for d, h in zip(ins, h_in):
+            d.copy_(h, non_blocking=True)
+        g1.replay()
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        one()
+    te = max_over_ranks(time.perf_counter() - t0, ws)
+    return {"value": round(wb.units_per_step() * n_steps * ws / te, 1), "unit": wb.unit, "steps": n_steps,
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in),
+            "d2h_bytes_per_step": h_out.numel() * h_out.element_size(),
+            "note": "per step: pinned H2D of the step's inputs, one-step graph replay, D2H of the bf16 "
+                    "output, synchronise"}
+
+
+def measure_secondary(name, dev, stream, pk):
+    """A short measurement of another workload (throughput + its dominant kernel's roofline)."""
+    import long_context_compressed_15_b300 as lcc
+    wb = WORKLOADS[name]()
+    wb.setup(dev)
+    G = wb.graph_steps
+    wb.run_steps(0, min(G, NSETS))
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    n0 = lcc.launch_count()
+    sch = Schedule(wb)
+    launches = lcc.launch_count() - n0
+    time_graph(sch.runs(G), stream)
+    t1 = time_graph(sch.runs(G), stream)
+    reps = max(3, int(math.ceil(0.3 / max(t1, 1e-6))))
+    t = time_graph(sch.runs(G * reps), stream)
+    lcc.sync_status()
+    steps = G * reps
+    d = {"value": round(wb.units_per_step() * steps / t, 1), "unit": wb.unit, "steps": steps,
+         "ms_per_step": round(t / steps * 1e3, 5), "gpu_launches_per_step": round(launches / G, 2),
+         "config": wb.config(), "roofline": roofline_of(wb, stream, reps, pk)}
+    if hasattr(wb, "extra"):
+        d.update(wb.extra())
+    del wb, sch
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return d
+
+
 def run_ours(args, ws, rank, local):
     import long_context_compressed_15_b300 as lcc
     from long_context_compressed_15_b300 import build
     build.build()
     lcc.load()
     dev = f"cuda:{local}"
+    pk = peaks()
     wb = WORKLOADS[args.workload]()
     wb.setup(dev)
     stream = torch.cuda.current_stream()
-    G = 64  # steps per graph (a multiple of the number of input sets)
-    for r in range(NSETS):  # eager warm-up of every set (also sets kernel attributes)
-        wb.step(r)
+    G = wb.graph_steps
+    wb.run_steps(0, min(G, NSETS))  # eager warm-up (also sets kernel attributes)
     torch.cuda.synchronize()
     lcc.sync_status()
-    # graphs: one per input set (single steps) and one of G steps
-    singles = []
     n0 = lcc.launch_count()
-    for r in range(NSETS):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            wb.step(r)
-        singles.append(g)
-    launches_per_step = (lcc.launch_count() - n0) / NSETS
-    big = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(big):
-        for i in range(G):
-            wb.step(i % NSETS)
-    stream = torch.cuda.current_stream()
+    sch = Schedule(wb)
+    launches_per_step = (lcc.launch_count() - n0) / G
+    sch.runs(args.steps)
+    sch.runs(args.warmup)
 
-    def schedule(n):
-        return [big] * (n // G) + [singles[i % NSETS] for i in range(n % G)]
-
-    time_graph(schedule(args.warmup), stream)
+    time_graph(sch.runs(args.warmup), stream)
     barrier(ws)
     clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
     clocks.start()
-    t = time_graph(schedule(args.steps), stream)
+    t = time_graph(sch.runs(args.steps), stream)
     ck = clocks.stop()
     barrier(ws)
     lcc.sync_status()
     t = max_over_ranks(t, ws)
-    units = wb.units_per_step() * args.steps * ws
-    value = units / t
+    value = wb.units_per_step() * args.steps * ws / t
 
-    # dominant kernel alone, same rotation, CUDA events on its stream
-    dg = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(dg):
-        for i in range(G):
-            wb.dominant_launch(i % NSETS)
-    time_graph([dg] * 2, stream)
-    reps = max(4, min(64, args.steps // G))
-    td = time_graph([dg] * reps, stream) / (reps * G)
-    pk = peaks()
-    achieved = wb.dominant_bytes() / td / 1e9
-    roofline = {"bound": "hbm", "kernel": wb.dominant, "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                "traffic": ncu_traffic(wb.dominant, wb.name), "peak_source": pk["source"],
-                "launch_us": round(td * 1e6, 3),
-                "step_hbm_gbs": round(wb.step_bytes() * args.steps / t / 1e9, 1)}
-
-    # end to end through the public API
-    h2d, d2h = wb.e2e_setup()
-    n_e2e = max(3, min(200, args.steps))
-    for _ in range(3):
-        wb.e2e_step(singles[0])
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(n_e2e):
-        wb.e2e_step(singles[0])
-    te = time.perf_counter() - t0
-    te = max_over_ranks(te, ws)
-    e2e = {"value": round(wb.units_per_step() * n_e2e * ws / te, 1), "unit": wb.unit, "steps": n_e2e,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "note": "per step: pinned H2D of the step's queries, graph replay, D2H of the bf16 output, sync"}
+    roofline = roofline_of(wb, stream, max(4, min(64, args.steps // G)), pk)
+    if hasattr(wb, "step_bytes"):
+        roofline["step_hbm_gbs"] = round(wb.step_bytes() * args.steps / t / 1e9, 1)
+    e2e = e2e_of(wb, ws, max(3, min(200, args.steps)))
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": wb.unit, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": wb.config(), "clocks": ck, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)), "roofline": roofline}
-    if rank == 0 and not args.no_cpu_baseline:
+    if hasattr(wb, "extra"):
+        line["config"].update(wb.extra())
+    if rank == 0 and not args.no_cpu_baseline and hasattr(wb, "oracle_sample"):
         n, tc, what = wb.oracle_sample(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(n / tc, 3), "unit": wb.unit, "cores": blas_threads(),
                                 "kind": "oracle", "sample": what}
+    if not args.no_secondary:
+        del wb, sch
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["workloads"] = {}
+        for name in WORKLOADS:
+            if name != args.workload:
+                line["workloads"][name] = measure_secondary(name, dev, stream, pk)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -388,6 +698,10 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     wb = WORKLOADS[args.workload]()
+    if not hasattr(wb, "oracle_sample"):
+        print(json.dumps({"impl": "reference", "unavailable": f"no timed oracle sample for {args.workload}; "
+                          "the reference arm times the fp64 oracle on csa_decode"}), flush=True)
+        return
     per_step = 1
     wb.oracle_sample(float("inf"), max_queries=min(args.warmup, 3) * per_step)
     t0 = time.perf_counter()
@@ -414,6 +728,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="csa_decode")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the short measurements of the other workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -142,9 +142,10 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w,
  * every GPU loading the library keeps until the process exits).
  *  - Queries are processed in chunks sized to that array; a request whose
  *    single query row needs more than 8 MiB (per batch row: Ncap*4 bytes of
- *    scores, ceil(Ncap/16)*4 bytes of group maxima, 16 KiB of candidate
- *    list and 8 bytes of counters, each array rounded up to 256 bytes) is
- *    rejected with LCC_ERR_WORKSPACE before anything is enqueued.
+ *    scores, ceil(Ncap/16)*4 bytes of group maxima, 8 bytes of counters and,
+ *    when Ncap > 16384, ceil(Ncap/16384)*(4 + 8192) bytes of candidate
+ *    lists; each array rounded up to 256 bytes) is rejected with
+ *    LCC_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on each device looks up the array's device address
  *    (and sets kernel attributes); make that first call before any stream
  *    capture begins.
@@ -236,6 +237,27 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
                               const int64_t* raw_pos0, int W,
                               lcc_bf16* out, float* lse_out,
                               void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * A whole CSA layer in one call: lcc_lightning_index_topk (writes idx) then
+ * lcc_csa_layer_attn on the selected entries and the window.  The library
+ * knows the order of its kernels here, so the attention is launched as a
+ * programmatic dependent of the top-k: it may start while the top-k runs,
+ * reads the queries and window rows early and waits for the index lists.
+ * Arguments as the two calls; idx [B, Tq, k] int32 is written; workspace:
+ * at least lcc_csa_layer_workspace(B, Tq, H, D, Ncap, k, W) bytes.
+ * ---------------------------------------------------------------------- */
+size_t lcc_csa_layer_workspace(int B, int Tq, int H, int D, int Ncap, int k, int W);
+lcc_status lcc_csa_layer(const lcc_bf16* q, const lcc_bf16* qI, const float* w,
+                         int B, int Tq, int H, int D, int HI, int DI, float scale,
+                         const int64_t* q_pos0,
+                         lcc_key_format fmt, const void* kI, const uint8_t* kI_scale,
+                         const int32_t* n_valid,
+                         const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap, int m, int k,
+                         const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride, int Rcap,
+                         const int64_t* raw_pos0, int W,
+                         int32_t* idx, lcc_bf16* out, float* lse_out,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------- *
  * Branch merge by log-sum-exp: with L = log sum_b exp(lse_b),

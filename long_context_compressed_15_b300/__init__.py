@@ -20,7 +20,8 @@ __all__ = [
     "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk", "lightning_index_scores",
     "lightning_index_topk_noalloc",
     "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
-    "swa_attn", "attn_merge", "csa_layer_attn", "hca_layer_attn", "layer_attn_workspace",
+    "swa_attn", "attn_merge", "csa_layer_attn", "hca_layer_attn", "layer_attn_workspace", "csa_layer",
+    "csa_layer_workspace",
     "sync_status", "last_error", "KEY_BF16", "KEY_NVFP4",
 ]
 
@@ -46,6 +47,9 @@ _SIGS = {
     "lcc_swa_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _P],
     "lcc_attn_merge": [_I, _P, _P, _L, _I, _P, _P, _P, _P],
     "lcc_layer_attn_workspace": [_I, _I, _I, _I, _I],
+    "lcc_csa_layer_workspace": [_I, _I, _I, _I, _I, _I, _I],
+    "lcc_csa_layer": [_P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _P, _I, _P, _P, _P, _P, _P, _L, _I, _I, _I,
+                      _P, _P, _L, _I, _P, _I, _P, _P, _P, _P, _Z, _P],
     "lcc_csa_layer_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _L, _I, _P, _I,
                            _P, _P, _P, _Z, _P],
     "lcc_hca_layer_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _P, _L, _I, _P, _I, _P, _P, _L, _I, _P, _I,
@@ -55,7 +59,7 @@ _SIGS = {
     "lcc_sync_status": [_P],
     "lcc_launch_count": [],
 }
-_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z,
+_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z, "lcc_csa_layer_workspace": _Z,
         "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p, "lcc_launch_count": ctypes.c_uint64}
 
 
@@ -383,6 +387,46 @@ def csa_layer_attn(q, Kc, Vc, idx, Kr, Vr, q_pos0, raw_pos0, W, scale=1.0, out=N
     _call("lcc_csa_layer_attn", _ptr(q), B, Tq, H, D, float(scale), _ptr(q_pos0), _ptr(Kc), _ptr(Vc), rs,
           Kc.shape[1], _ptr(idx.contiguous()), k, _ptr(Kr), _ptr(Vr), rr, Kr.shape[1], _ptr(raw_pos0), int(W),
           _ptr(out), _ptr(lse_out), _ptr(workspace), nbytes, _stream(stream))
+    return out
+
+
+def csa_layer_workspace(B, Tq, H, D, Ncap, k, W) -> int:
+    return int(load().lcc_csa_layer_workspace(B, Tq, H, D, Ncap, k, W))
+
+
+def csa_layer(q, qI, w, q_pos0, kI, n_valid, m, k, Kc, Vc, Kr, Vr, raw_pos0, W, kI_scale=None, scale=1.0,
+              idx=None, out=None, lse_out=None, workspace=None, stream=None):
+    """A whole CSA layer (indexer + top-k + attention over the selected entries and the window) -> bf16."""
+    _need(q, torch.bfloat16, "q", 4)
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    B, Tq, H, D = q.shape
+    _, _, HI, DI = qI.shape
+    if not (qI.is_contiguous() and w.is_contiguous() and kI.is_contiguous()):
+        raise ValueError("qI, w and kI must be contiguous")
+    if kI.dtype == torch.uint8:
+        fmt = KEY_NVFP4
+        _need(kI_scale, torch.uint8, "kI_scale", 3)
+    else:
+        fmt = KEY_BF16
+        _need(kI, torch.bfloat16, "kI", 3)
+    rs, rr = _kv(Kc, Vc), _kv(Kr, Vr)
+    out = _layer_out(q, out, lse_out)
+    dev = q.device
+    q_pos0 = _positions(q_pos0, B, dev)
+    raw_pos0 = _positions(raw_pos0, B, dev)
+    n_valid = _positions(n_valid, B, dev, torch.int32)
+    Ncap = kI.shape[1]
+    if Kc.shape[1] != Ncap:
+        raise ValueError("kI and Kc must hold the same number of entries")
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=dev)
+    _need(idx, torch.int32, "idx", 3)
+    workspace, nbytes = _ws(workspace, csa_layer_workspace(B, Tq, H, D, Ncap, k, int(W)), dev)
+    _call("lcc_csa_layer", _ptr(q), _ptr(qI), _ptr(w), B, Tq, H, D, HI, DI, float(scale), _ptr(q_pos0), fmt,
+          _ptr(kI), _ptr(kI_scale), _ptr(n_valid), _ptr(Kc), _ptr(Vc), rs, Ncap, int(m), int(k), _ptr(Kr), _ptr(Vr),
+          rr, Kr.shape[1], _ptr(raw_pos0), int(W), _ptr(idx), _ptr(out), _ptr(lse_out), _ptr(workspace), nbytes,
+          _stream(stream))
     return out
 
 

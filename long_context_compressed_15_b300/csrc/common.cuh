@@ -111,6 +111,14 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel on its stream is still
+// running; pdl_wait() blocks until that kernel has completed and its memory
+// writes are visible (it returns at once for a normally launched kernel).
+// pdl_trigger() lets the next kernel on the stream start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Visible compressed entries for the query at absolute position t.
 __device__ __forceinline__ int visible_entries(int64_t t, int m, int n_valid, int Ncap) {
   int64_t v = (t + 1) / m;

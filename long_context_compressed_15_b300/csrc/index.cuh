@@ -55,6 +55,7 @@ __global__ void __launch_bounds__(128) k_index_score(IndexArgs a) {
   const int qlast = min(qbase + NQ, a.q0 + a.nq) - 1;
   const int vis_max = visible_entries(pos0 + qlast, a.m, nval, a.Ncap);
   const int e_cta = blockIdx.x * ENT;
+  pdl_trigger();  // the top-k that follows may start launching (it waits for this grid)
   if (a.counters && blockIdx.x == 0 && threadIdx.x < NQ) {
     const int qq = qbase + threadIdx.x;
     if (qq < a.q0 + a.nq && qq < a.Tq) {

@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *s_tmem;
+  pdl_trigger();  // the top-k that follows may start launching (it waits for this grid)
 
   if (warp == 0) {
     // ---------------------------------------------------------- producer
@@ -186,7 +187,11 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int t = 0; t < ntiles; ++t) {
       const int acc = t & 1;
-      if (*s_abort || !tc::mbar_wait(tfull + acc, (t >> 1) & 1, 6)) { *s_abort = 1; break; }
+      // the TMEM loads below are warp-collective: leave the loop as a whole warp
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 6))) {
+        *s_abort = 1;
+        break;
+      }
       tc::tc_fence_after();
       const int entry = (t_lo + t) * C::TILE + quarter * 32 + lane;
       constexpr int QPC = 8 / HI < 1 ? 1 : 8 / HI;  // queries per 8-column load

@@ -8,12 +8,14 @@
 #include <atomic>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "lcc.h"
 #include "common.cuh"
 #include "pool.cuh"
 #include "merge.cuh"
 #include "attn.cuh"
+#include "attn_tc.cuh"
 #include "index.cuh"
 #include "index_tc.cuh"
 #include "topk_thr.cuh"
@@ -45,6 +47,25 @@ lcc_status launch_check(const char* what) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(LCC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
   return LCC_OK;
+}
+
+// Launch `kern` on stream s; with pdl the launch may overlap the tail of the
+// previous kernel on the stream (the kernel must pdl_wait() before reading
+// anything that kernel writes).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // Raise a kernel's dynamic shared-memory limit once per device.
@@ -95,9 +116,11 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
 }
 
 // ----------------------------------------------------------------- index/topk
-constexpr int kTopkNT = 256;
-constexpr int kCandCap = 2048;   // candidate list per row of the threshold top-k
-constexpr int kTopkSeg = 4096;   // entries per CTA of the threshold top-k
+constexpr int kTopkNT = 1024;
+constexpr int kTopkPer = 16;     // scores per thread: one CTA covers rows of up to 16384 entries
+constexpr int kCandCap = 2048;   // candidates one CTA selects from
+constexpr int kSegCap = 1024;    // candidates kept per segment of a row longer than one CTA
+constexpr int kTopkSeg = kTopkNT * kTopkPer;   // entries per CTA of the threshold top-k
 constexpr size_t kScoreBudget = size_t(1) << 28;  // score elements per query chunk
 
 int index_chunk(int B, int Tq, int Ncap) {
@@ -108,20 +131,26 @@ int index_chunk(int B, int Tq, int Ncap) {
 }
 
 int gmax_stride(int Ncap) { return (Ncap + 15) / 16; }
+int topk_segments(int Ncap) { return (Ncap + kTopkSeg - 1) / kTopkSeg; }
 
-// Scratch of one query chunk of qc queries (rows = B*qc): scores, group
-// maxima, candidate lists and the two per-row counters.
+// Scratch of one query chunk (rows = B * queries in the chunk): scores,
+// group maxima, per-row counters and, for rows longer than one top-k
+// segment, the per-segment candidate lists.
 struct IndexWs {
-  size_t scores, gmax, cand_k, cand_i, counters, total;
+  size_t scores, gmax, counters, seg_cnt, cand_k, cand_i, total;
 };
 IndexWs index_ws_rows(int64_t rows, int Ncap) {
   IndexWs w{};
+  const int nseg = topk_segments(Ncap);
   w.scores = round_up(rows * Ncap * sizeof(float), 256);
   w.gmax = round_up(rows * gmax_stride(Ncap) * sizeof(uint32_t), 256);
-  w.cand_k = round_up(rows * kCandCap * sizeof(uint32_t), 256);
-  w.cand_i = round_up(rows * kCandCap * sizeof(int32_t), 256);
   w.counters = round_up(rows * 2 * sizeof(int), 256);
-  w.total = w.scores + w.gmax + w.cand_k + w.cand_i + w.counters;
+  if (nseg > 1) {
+    w.seg_cnt = round_up(rows * nseg * sizeof(int), 256);
+    w.cand_k = round_up(rows * nseg * kSegCap * sizeof(uint32_t), 256);
+    w.cand_i = round_up(rows * nseg * kSegCap * sizeof(int32_t), 256);
+  }
+  w.total = w.scores + w.gmax + w.counters + w.seg_cnt + w.cand_k + w.cand_i;
   return w;
 }
 IndexWs index_ws(int B, int Tq, int Ncap, int k) {
@@ -300,11 +329,17 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
   const IndexWs ws = index_ws_rows(static_cast<int64_t>(B) * qc, Ncap);
   char* base = static_cast<char*>(scratch);
   float* scores = reinterpret_cast<float*>(base);
-  uint32_t* gmax = reinterpret_cast<uint32_t*>(base + ws.scores);
-  uint32_t* cand_k = reinterpret_cast<uint32_t*>(base + ws.scores + ws.gmax);
-  int32_t* cand_i = reinterpret_cast<int32_t*>(base + ws.scores + ws.gmax + ws.cand_k);
-  int* counters = reinterpret_cast<int*>(base + ws.scores + ws.gmax + ws.cand_k + ws.cand_i);
-  const int nseg = (Ncap + kTopkSeg - 1) / kTopkSeg;
+  base += ws.scores;
+  uint32_t* gmax = reinterpret_cast<uint32_t*>(base);
+  base += ws.gmax;
+  int* counters = reinterpret_cast<int*>(base);
+  base += ws.counters;
+  int* seg_cnt = reinterpret_cast<int*>(base);
+  base += ws.seg_cnt;
+  uint32_t* cand_k = reinterpret_cast<uint32_t*>(base);
+  base += ws.cand_k;
+  int32_t* cand_i = reinterpret_cast<int32_t*>(base);
+  const int nseg = topk_segments(Ncap);
   for (int q0 = 0; q0 < Tq; q0 += qc) {
     const int nq = qc < Tq - q0 ? qc : Tq - q0;
     IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, q0, nq,
@@ -324,17 +359,18 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
     ta.q0 = q0;
     ta.nq = nq;
     ta.k = k;
-    ta.seg = kTopkSeg;
     ta.cand_key = cand_k;
     ta.cand_idx = cand_i;
-    ta.cap = kCandCap;
-    ta.cnt = counters;
-    ta.done = counters + static_cast<int64_t>(B) * nq;
+    ta.seg_cnt = seg_cnt;
+    ta.seg_cap = kSegCap;
+    ta.nseg = nseg;
+    ta.done = counters;
     ta.out_i = idx;
     ta.out_s = score;
     const int64_t rows = static_cast<int64_t>(B) * nq;
     if (rows > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
-    k_topk_thr<kTopkNT, kCandCap><<<dim3(static_cast<unsigned>(rows), nseg), kTopkNT, 0, s>>>(ta);
+    launch_k(k_topk_thr<kTopkNT, kTopkPer, kCandCap>, dim3(static_cast<unsigned>(rows), nseg), dim3(kTopkNT), 0, s,
+             true, ta);
     if ((st = launch_check("k_topk_thr")) != LCC_OK) return st;
   }
   return LCC_OK;
@@ -384,22 +420,31 @@ namespace {
 unsigned long long g_attn_done[2][2][3][2] = {};
 
 template <int D, int ROWS, int MODE, bool WIN2>
-lcc_status launch_attn(const AttnArgs& a, dim3 grid, cudaStream_t s) {
+lcc_status launch_attn(const AttnArgs& a, dim3 grid, cudaStream_t s, bool pdl) {
   const size_t smem = AttnSmem<D, ROWS>::total;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     lcc_status st = ensure_smem(k_attn<D, ROWS, MODE, WIN2>, smem, g_attn_done[D == 128][ROWS == 64][MODE][WIN2]);
     if (st != LCC_OK) return st;
   }
-  k_attn<D, ROWS, MODE, WIN2><<<grid, ROWS * 2, smem, s>>>(a);
+  launch_k(k_attn<D, ROWS, MODE, WIN2>, grid, dim3(ROWS * 2), smem, s, pdl, a);
   return launch_check("k_attn");
 }
 
 template <int MODE, bool WIN2 = false>
-lcc_status dispatch_attn(const AttnArgs& a, int D, dim3 grid, int rows, cudaStream_t s) {
+lcc_status dispatch_attn(const AttnArgs& a, int D, dim3 grid, int rows, cudaStream_t s, bool pdl = false) {
   if (D == 128)
-    return rows == 64 ? launch_attn<128, 64, MODE, WIN2>(a, grid, s) : launch_attn<128, 16, MODE, WIN2>(a, grid, s);
-  return rows == 64 ? launch_attn<64, 64, MODE, WIN2>(a, grid, s) : launch_attn<64, 16, MODE, WIN2>(a, grid, s);
+    return rows == 64 ? launch_attn<128, 64, MODE, WIN2>(a, grid, s, pdl)
+                      : launch_attn<128, 16, MODE, WIN2>(a, grid, s, pdl);
+  return rows == 64 ? launch_attn<64, 64, MODE, WIN2>(a, grid, s, pdl) : launch_attn<64, 16, MODE, WIN2>(a, grid, s, pdl);
+}
+
+template <int D>
+lcc_status launch_combine(const float* Op, const float* lp, int ns, int64_t rows, float* O, float* lse, bf16* out,
+                          cudaStream_t s) {
+  const unsigned g = static_cast<unsigned>((rows + 7) / 8);
+  launch_k(k_split_combine<D>, dim3(g), dim3(256), 0, s, true, Op, lp, ns, rows, O, lse, out);
+  return launch_check("k_split_combine");
 }
 
 lcc_status check_attn_common(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, const lcc_bf16* K,
@@ -434,11 +479,85 @@ size_t split_ws_bytes(int ns, int64_t rows, int D) {
   return round_up(ns * rows * D * sizeof(float), 256) + round_up(ns * rows * sizeof(float), 256);
 }
 
+// ---- tensor-core attention for long query blocks (prefill) ----
+unsigned long long g_attn_tc_done = 0;
+
+// Worth the tensor-core kernel: D = 128 and enough 128-row blocks to fill the GPU.
+bool use_attn_tc(int B, int Tq, int H, int D) {
+  return D == 128 && static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 127) / 128) >= num_sms();
+}
+
+// src1 (K1/V1, rows kv_rs1 apart, Ncap1 per batch) and optional window src2.
+lcc_status launch_attn_tc(AttnTcArgs a, const bf16* q, const bf16* K1, const bf16* V1, int64_t kv_rs1,
+                          const bf16* K2, const bf16* V2, int64_t kv_rs2, cudaStream_t s, bool pdl) {
+  constexpr int D = 128;
+  using Cf = AttnTcCfg<D>;
+  CUtensorMap tq, tk1, tv1, tk2, tv2;
+  const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * a.H;
+  lcc_status st = make_tmap_2d(&tq, q, D, qrows, D, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_tc q");
+  if (st != LCC_OK) return st;
+  const uint64_t r1 = static_cast<uint64_t>(a.B) * (a.Ncap1 > 0 ? a.Ncap1 : 1);
+  if ((st = make_tmap_2d(&tk1, K1, D, r1, kv_rs1, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_tc K")) != LCC_OK)
+    return st;
+  if ((st = make_tmap_2d(&tv1, V1, D, r1, kv_rs1, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_tc V")) != LCC_OK)
+    return st;
+  if (a.win2) {
+    const uint64_t r2 = static_cast<uint64_t>(a.B) * (a.Ncap2 > 0 ? a.Ncap2 : 1);
+    if ((st = make_tmap_2d(&tk2, K2, D, r2, kv_rs2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_tc Kw")) != LCC_OK)
+      return st;
+    if ((st = make_tmap_2d(&tv2, V2, D, r2, kv_rs2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_tc Vw")) != LCC_OK)
+      return st;
+  } else {
+    tk2 = tk1;
+    tv2 = tv1;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(k_attn_tc<D>, Cf::SMEM, g_attn_tc_done)) != LCC_OK) return st;
+  }
+  const int64_t gx = (static_cast<int64_t>(a.Tq) * a.H + 127) / 128;
+  if (gx > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "k_attn_tc: too many rows");
+  launch_k(k_attn_tc<D>, dim3(static_cast<unsigned>(gx), a.B), dim3(192), Cf::SMEM, s, pdl, tq, tk1, tv1, tk2, tv2,
+           a);
+  return launch_check("k_attn_tc");
+}
+
+unsigned long long g_wsplit_done[2][2] = {};
+constexpr int kWsplitWarps = 16;
+constexpr int kWsplitTile = 16;   // keys per warp tile
+
+// Short key lists with few (query, 16-head) groups: warps of one CTA split
+// the key tiles and combine in shared memory (no workspace, one launch).
+template <int MODE>
+bool use_wsplit(int64_t groups16, int64_t keys) {
+  return groups16 <= 4 * num_sms() && (keys + kWsplitTile - 1) / kWsplitTile <= 4 * kWsplitWarps;
+}
+
+template <int D, int MODE>
+lcc_status launch_wsplit(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pdl) {
+  const size_t smem = WsplitSmem<D, kWsplitWarps, kWsplitTile>::total;
+  auto kern = k_attn_wsplit<D, MODE, true, kWsplitWarps, kWsplitTile>;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    lcc_status st = ensure_smem(kern, smem, g_wsplit_done[D == 128][MODE]);
+    if (st != LCC_OK) return st;
+  }
+  launch_k(kern, dim3(gx, a.B), dim3(kWsplitWarps * 32), smem, s, pdl, a);
+  return launch_check("k_attn_wsplit");
+}
+
 // One pass over (compressed source ++ window rows) -> bf16 layer output.
 template <int MODE>
 lcc_status layer_attn_impl(const char* name, AttnArgs a, int D, int64_t rowblocks, unsigned gx, int rows_per_cta,
                            int64_t keys, lcc_bf16* out, float* lse_out, void* workspace, size_t workspace_bytes,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl = false) {
+  const int64_t groups16 = static_cast<int64_t>(a.B) * a.Tq * ((a.H + 15) / 16);
+  if (use_wsplit<MODE>(groups16, keys) && groups16 / a.B <= 0x7FFFFFFF) {
+    a.out_bf16 = reinterpret_cast<bf16*>(out);
+    a.lse = lse_out;
+    const unsigned gw = static_cast<unsigned>(static_cast<int64_t>(a.Tq) * ((a.H + 15) / 16));
+    return D == 128 ? launch_wsplit<128, MODE>(a, gw, s, pdl) : launch_wsplit<64, MODE>(a, gw, s, pdl);
+  }
   const int ns = splits_for(rowblocks, keys);
   const int64_t rowsT = static_cast<int64_t>(a.B) * a.Tq * a.H;
   const size_t need = split_ws_bytes(ns, rowsT, D);
@@ -450,20 +569,18 @@ lcc_status layer_attn_impl(const char* name, AttnArgs a, int D, int64_t rowblock
     a.O = nullptr;
     a.lse = lse_out;
     a.out_bf16 = reinterpret_cast<bf16*>(out);
-    return dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, 1), rows_per_cta, s);
+    return dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, 1), rows_per_cta, s, pdl);
   }
   float* Op = static_cast<float*>(workspace);
   float* lp = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(ns * rowsT * D * sizeof(float), 256));
   a.O = Op;
   a.lse = lp;
   a.out_bf16 = nullptr;
-  lcc_status st = dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, ns), rows_per_cta, s);
+  lcc_status st = dispatch_attn<MODE, true>(a, D, dim3(gx, a.B, ns), rows_per_cta, s, pdl);
   if (st != LCC_OK) return st;
-  const unsigned g = static_cast<unsigned>((rowsT + 7) / 8);
   bf16* ob = reinterpret_cast<bf16*>(out);
-  if (D == 128) k_split_combine<128><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, nullptr, lse_out, ob);
-  else k_split_combine<64><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, nullptr, lse_out, ob);
-  return launch_check("k_split_combine");
+  return D == 128 ? launch_combine<128>(Op, lp, ns, rowsT, nullptr, lse_out, ob, s)
+                  : launch_combine<64>(Op, lp, ns, rowsT, nullptr, lse_out, ob, s);
 }
 
 int dense_splits(int B, int Tq, int H, int Ncap) {
@@ -540,6 +657,13 @@ lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   a.n_valid = n_valid; a.m = m;
   a.nsplit = ns; a.rows_total = rowsT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (ns == 1 && use_attn_tc(B, Tq, H, D)) {
+    AttnTcArgs t{};
+    t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
+    t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
+    t.O = O; t.lse = lse;
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, s, false);
+  }
   if (ns == 1) {
     a.O = O; a.lse = lse;
     return dispatch_attn<ATT_RANGE>(a, D, dim3(static_cast<unsigned>(rblocks), B, 1), 64, s);
@@ -549,10 +673,8 @@ lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   a.O = Op; a.lse = lp;
   st = dispatch_attn<ATT_RANGE>(a, D, dim3(static_cast<unsigned>(rblocks), B, ns), 64, s);
   if (st != LCC_OK) return st;
-  const unsigned g = static_cast<unsigned>((rowsT + 7) / 8);
-  if (D == 128) k_split_combine<128><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse, nullptr);
-  else k_split_combine<64><<<g, 256, 0, s>>>(Op, lp, ns, rowsT, O, lse, nullptr);
-  return launch_check("k_split_combine");
+  return D == 128 ? launch_combine<128>(Op, lp, ns, rowsT, O, lse, nullptr, s)
+                  : launch_combine<64>(Op, lp, ns, rowsT, O, lse, nullptr, s);
 }
 
 lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
@@ -576,6 +698,14 @@ lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float sc
   a.kv_bs = static_cast<int64_t>(Rcap) * kv_rstride; a.kv_rs = kv_rstride; a.Ncap = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
   a.O = O; a.lse = lse; a.nsplit = 1; a.rows_total = static_cast<int64_t>(B) * Tq * H;
+  if (use_attn_tc(B, Tq, H, D)) {
+    AttnTcArgs t{};
+    t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
+    t.mode1 = ATT_WINDOW; t.Ncap1 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
+    t.O = O; t.lse = lse;
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream),
+                          false);
+  }
   return dispatch_attn<ATT_WINDOW>(a, D, dim3(static_cast<unsigned>(rblocks), B, 1), 64,
                                    static_cast<cudaStream_t>(stream));
 }
@@ -589,12 +719,14 @@ size_t lcc_layer_attn_workspace(int B, int Tq, int H, int D, int n_keys) {
   return split_ws_bytes(splits_for(rb, n_keys), static_cast<int64_t>(B) * Tq * H, D);
 }
 
-lcc_status lcc_csa_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
-                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
-                              const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride,
-                              int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out, float* lse_out,
-                              void* workspace, size_t workspace_bytes, void* stream) {
-  const char* name = "lcc_csa_layer_attn";
+}  // extern "C"
+
+namespace {
+lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                               const int64_t* q_pos0, const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride,
+                               int Ncap, const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr,
+                               int64_t r_rstride, int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out,
+                               float* lse_out, void* workspace, size_t workspace_bytes, void* stream, bool pdl) {
   if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
   if (B == 0 || Tq == 0) return LCC_OK;
   if (!out) return fail(LCC_ERR_ARG, "%s: null out", name);
@@ -623,7 +755,48 @@ lcc_status lcc_csa_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   const int64_t rowblocks = static_cast<int64_t>(B) * Tq * hblocks;
   return layer_attn_impl<ATT_GATHER>(name, a, D, rowblocks, static_cast<unsigned>(Tq * hblocks), rows,
                                      static_cast<int64_t>(k) + W, out, lse_out, workspace, workspace_bytes,
-                                     static_cast<cudaStream_t>(stream));
+                                     static_cast<cudaStream_t>(stream), pdl);
+}
+}  // namespace
+
+extern "C" {
+
+lcc_status lcc_csa_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
+                              const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap,
+                              const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride,
+                              int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out, float* lse_out,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  return csa_layer_attn_impl("lcc_csa_layer_attn", q, B, Tq, H, D, scale, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k,
+                             Kr, Vr, r_rstride, Rcap, raw_pos0, W, out, lse_out, workspace, workspace_bytes, stream,
+                             false);
+}
+
+size_t lcc_csa_layer_workspace(int B, int Tq, int H, int D, int Ncap, int k, int W) {
+  if (B <= 0 || Tq <= 0 || H <= 0 || D <= 0 || Ncap <= 0 || k <= 0 || W <= 0) return 0;
+  return round_up(index_ws(B, Tq, Ncap, k).total, 256) + lcc_layer_attn_workspace(B, Tq, H, D, k + W);
+}
+
+lcc_status lcc_csa_layer(const lcc_bf16* q, const lcc_bf16* qI, const float* w, int B, int Tq, int H, int D, int HI,
+                         int DI, float scale, const int64_t* q_pos0, lcc_key_format fmt, const void* kI,
+                         const uint8_t* kI_scale, const int32_t* n_valid, const lcc_bf16* Kc, const lcc_bf16* Vc,
+                         int64_t kv_rstride, int Ncap, int m, int k, const lcc_bf16* Kr, const lcc_bf16* Vr,
+                         int64_t r_rstride, int Rcap, const int64_t* raw_pos0, int W, int32_t* idx, lcc_bf16* out,
+                         float* lse_out, void* workspace, size_t workspace_bytes, void* stream) {
+  const char* name = "lcc_csa_layer";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  const size_t need = lcc_csa_layer_workspace(B, Tq, H, D, Ncap, k, W);
+  if (!workspace || workspace_bytes < need)
+    return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, need);
+  const size_t ws_index = round_up(index_ws(B, Tq, Ncap, k).total, 256);
+  lcc_status st = lcc_lightning_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx,
+                                           nullptr, workspace, ws_index, stream);
+  if (st != LCC_OK) return st;
+  // the attention follows the top-k kernel on the stream: it may launch early and
+  // prefetch the queries and window rows, then wait for the index lists
+  return csa_layer_attn_impl(name, q, B, Tq, H, D, scale, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k, Kr, Vr,
+                             r_rstride, Rcap, raw_pos0, W, out, lse_out, static_cast<char*>(workspace) + ws_index,
+                             workspace_bytes - ws_index, stream, true);
 }
 
 lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float scale, const int64_t* q_pos0,
@@ -656,6 +829,15 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
   a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
+  if (use_attn_tc(B, Tq, H, D)) {
+    AttnTcArgs t{};
+    t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
+    t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
+    t.win2 = true; t.Ncap2 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
+    t.out_bf16 = reinterpret_cast<bf16*>(out); t.lse = lse_out;
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, a.K2, a.V2, r_rstride, static_cast<cudaStream_t>(stream),
+                          false);
+  }
   return layer_attn_impl<ATT_RANGE>(name, a, D, static_cast<int64_t>(B) * rblocks, static_cast<unsigned>(rblocks),
                                     64, static_cast<int64_t>(Ncap) + W, out, lse_out, workspace, workspace_bytes,
                                     static_cast<cudaStream_t>(stream));

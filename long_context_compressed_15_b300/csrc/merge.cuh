@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
   constexpr int PER = D / 32;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  pdl_wait();  // the partials come from the split attention kernel
   if (row >= rows) return;
   float L = -INFINITY;
   for (int s = lane; s < nsplit; s += 32) L = fmaxf(L, __ldg(lp + s * rows + row));

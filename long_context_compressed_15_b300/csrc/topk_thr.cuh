@@ -11,17 +11,22 @@
 // their maxima, so theta = the k-th largest group maximum is a lower bound
 // of the row's k-th largest score: every top-k entry has a key >= theta.
 // Groups are merged into at most 2k super-groups first (a super-group's
-// maximum is the max of its groups'), which keeps the sort small while the
-// number of entries at or above theta stays a small multiple of k.
+// maximum is the max of its groups'), which keeps the search small while
+// the number of entries at or above theta stays a small multiple of k.
 //
-// Grid (rows, segments): every CTA derives theta for its row, scans its
-// segment of the scores and appends the entries with key >= theta to the
-// row's candidate list.  The last CTA of a row to finish (atomic ticket)
-// sorts the candidates by (score desc, index asc), keeps k, re-sorts them by
-// index and writes the row.  If a row has more candidates than the list
-// holds (massive exact ties at theta), that CTA instead finds the exact k-th
-// key by bisection over the whole row and compacts it in index order.
-// Counters are zeroed by the indexer kernel before this kernel runs.
+// One CTA covers a segment of SEG = NT*PER entries (thread t owns PER
+// consecutive entries, requested first).  It finds theta by counting over
+// the super-group maxima (v is the k-th largest iff fewer than k values
+// exceed v and at least k reach it), compacts the entries >= theta in index
+// order (one block scan), finds the exact k-th largest key T among those
+// candidates by the same count, and writes, in index order, every candidate
+// above T and the lowest-index candidates equal to T.  A row longer than one
+// segment is split over several CTAs that store their candidates in
+// per-segment regions; the last CTA of the row to finish (atomic ticket)
+// gathers the regions in segment order and selects.  When candidates
+// overflow (massive exact ties at theta) the selecting CTA finds T by
+// bisection over the whole row instead.  The per-row ticket counters are
+// zeroed by the indexer kernel that runs just before this one.
 #pragma once
 #include "common.cuh"
 
@@ -36,62 +41,126 @@ struct TopkThrArgs {
   const int32_t* n_valid;
   int m, Tq, q0, nq;
   int k;
-  int seg;                 // entries per segment (one CTA)
-  uint32_t* cand_key;      // row r at + r*cap
+  // rows longer than one segment: segment s of row r keeps its candidates at
+  // cand_* + (r*nseg + s)*seg_cap and their number at seg_cnt[r*nseg + s]
+  uint32_t* cand_key;
   int32_t* cand_idx;
-  int cap;
-  int* cnt;                // [rows] candidates appended
-  int* done;               // [rows] CTAs finished
+  int* seg_cnt;
+  int seg_cap, nseg;
+  int* done;               // [rows] CTAs of the row finished
   int32_t* out_i;          // final list of row (b, i) at (b*Tq + i)*k
   float* out_s;            // optional
 };
 
+// Exclusive prefix sum over the CTA; *total receives the sum.
 template <int NT>
-__device__ __forceinline__ int block_sum(int v, int* s_red) {
-  v = __reduce_add_sync(0xffffffffu, v);
+__device__ __forceinline__ int block_scan_excl(int v, int* s_warp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  __syncthreads();
-  if (lane == 0) s_red[warp] = v;
-  __syncthreads();
-  int t = 0;
+  int x = v;
 #pragma unroll
-  for (int w = 0; w < NT / 32; ++w) t += s_red[w];
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  int pre = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    const int t = s_warp[w];
+    pre += w < warp ? t : 0;
+    tot += t;
+  }
+  *total = tot;
+  return pre + x - v;
+}
+
+template <int NT>
+__device__ __forceinline__ int block_sum(int v, int* s_warp) {
+  int tot;
+  (void)block_scan_excl<NT>(v, s_warp, &tot);
+  return tot;
+}
+
+// Threads that share the counting for one element: the largest power of two
+// <= NT / n, between 1 and 32 (a group stays inside one warp).
+template <int NT>
+__device__ __forceinline__ int threads_per_elem(int n) {
+  int t = 1;
+  while (t < 32 && 2 * t * n <= NT) t <<= 1;
   return t;
 }
 
-// In-place bitonic sort of P (power of two) 64-bit values in shared memory.
-template <int NT, bool DESC>
-__device__ __forceinline__ void bitonic_sort(unsigned long long* v, int P) {
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int t = threadIdx.x; t < P / 2; t += NT) {
-        const int i = 2 * t - (t & (stride - 1));
-        const int j = i + stride;
-        const bool up = (i & size) == 0;
-        const unsigned long long a = v[i], b = v[j];
-        const bool out_of_order = DESC ? (a < b) : (a > b);
-        if (out_of_order == up) { v[i] = b; v[j] = a; }
-      }
-      __syncthreads();
+// k-th largest of vals[0..n) (1 <= k <= n) by counting: the value v with
+// #{x > v} < k <= #{x >= v}.  vals must be zero-padded up to a multiple of
+// 128 entries (0 is never counted: every real value here is >= 1).  Every
+// thread of the CTA calls this; the result is stored in *out.
+template <int NT>
+__device__ __forceinline__ void block_kth_largest(const uint32_t* vals, int n, int k, uint32_t* out) {
+  const int tpe = threads_per_elem<NT>(n);
+  const int np4 = (n + 127) / 128 * 32;  // 4-wide words to scan
+  const int groups = NT / tpe, part = threadIdx.x % tpe;
+  const uint4* v4 = reinterpret_cast<const uint4*>(vals);
+  for (int it = 0; it < (n + groups - 1) / groups; ++it) {
+    const int e = it * groups + static_cast<int>(threadIdx.x) / tpe;
+    const uint32_t v = e < n ? vals[e] : 0xFFFFFFFFu;
+    int gt = 0, ge = 0;
+#pragma unroll 4
+    for (int w = part; w < np4; w += tpe) {
+      const uint4 x = v4[w];
+      gt += (x.x > v) + (x.y > v) + (x.z > v) + (x.w > v);
+      ge += (x.x >= v) + (x.y >= v) + (x.z >= v) + (x.w >= v);
     }
+    for (int o = 1; o < tpe; o <<= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o);
+      ge += __shfl_xor_sync(0xffffffffu, ge, o);
+    }
+    if (e < n && part == 0 && gt < k && ge >= k) *out = v;  // every writer stores the same value
   }
 }
 
-template <int NT, int SORTCAP>
-__global__ void __launch_bounds__(NT) k_topk_thr(TopkThrArgs a) {
-  __shared__ unsigned long long s_v[SORTCAP];
-  __shared__ int s_red[NT / 32];
-  __shared__ uint32_t s_theta;
+template <int NT, int PER, int CAP>
+__global__ void __launch_bounds__(NT, 1) k_topk_thr(TopkThrArgs a) {
+  constexpr int SEG = NT * PER;
+  static_assert(PER % 4 == 0, "4-wide loads");
+  __shared__ __align__(16) uint32_t s_ck[CAP + 128];   // candidates, index order (+ zero padding)
+  __shared__ __align__(16) int32_t s_ci[CAP];
+  __shared__ __align__(16) uint32_t s_g[CAP + 128];    // super-group maxima (+ zero padding)
+  __shared__ int s_warp[NT / 32];
+  __shared__ uint32_t s_theta, s_T;
   __shared__ int s_last;
 
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int row = blockIdx.x, segi = blockIdx.y;
   const int b = row / a.nq, i = a.q0 + row % a.nq;
-  const int vis = visible_entries(__ldg(a.q_pos0 + b) + i, a.m, __ldg(a.n_valid + b), a.Ncap);
   const int k = a.k;
+  const float* srow = a.scores + static_cast<int64_t>(row) * a.Ncap;
+  const int64_t qpos = __ldg(a.q_pos0 + b) + i;   // inputs of the call: ready before the indexer ran
+  const int nval = __ldg(a.n_valid + b);
+  pdl_trigger();
+  pdl_wait();  // scores, group maxima and counters come from the indexer kernel
+  // This thread's PER consecutive scores of the segment, requested before
+  // anything that depends on the visible count (masked once it is known).
+  const int lo = segi * SEG;
+  const int e0 = lo + tid * PER;
+  const int cap_hi = min(a.Ncap, lo + SEG);
+  float sv[PER];
+  if ((a.Ncap & 3) == 0) {
+#pragma unroll
+    for (int u = 0; u < PER; u += 4) {
+      const float4 v = e0 + u < cap_hi ? __ldcg(reinterpret_cast<const float4*>(srow + e0 + u))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      sv[u] = v.x; sv[u + 1] = v.y; sv[u + 2] = v.z; sv[u + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int u = 0; u < PER; ++u) sv[u] = e0 + u < cap_hi ? __ldcg(srow + e0 + u) : 0.f;
+  }
+  const int vis = visible_entries(qpos, a.m, nval, a.Ncap);
   int32_t* oi = a.out_i + (static_cast<int64_t>(b) * a.Tq + i) * k;
   float* os = a.out_s ? a.out_s + (static_cast<int64_t>(b) * a.Tq + i) * k : nullptr;
-  const float* srow = a.scores + static_cast<int64_t>(row) * a.Ncap;
+  const bool multi = vis > SEG;
 
   if (vis <= k) {  // every visible entry is selected
     if (segi == 0)
@@ -101,142 +170,153 @@ __global__ void __launch_bounds__(NT) k_topk_thr(TopkThrArgs a) {
       }
     return;
   }
+  if (!multi && segi > 0) return;
 
-  const int lo = segi * a.seg, hi = min(vis, lo + a.seg);
+  const int hi = min(vis, lo + SEG);
+  int C = 0;  // candidates in s_ck / s_ci (index order); -1 = overflow
   if (lo < hi) {
     // ---- theta: k-th largest super-group maximum ----
     const int G = (vis + a.gs - 1) / a.gs;
-    const int f = (G + 2 * k - 1) / (2 * k);          // groups per super-group
-    const int Gs = (G + f - 1) / f;                   // super-groups (<= 2k)
-    if (tid == 0) s_theta = 0u;
+    const int f = (G + 2 * k - 1) / (2 * k);   // groups per super-group
+    const int Gs = (G + f - 1) / f;            // super-groups (<= 2k <= CAP)
+    if (tid == 0) s_theta = 0u;                // fewer than k groups: every entry is a candidate
     if (Gs >= k) {
-      int P = 1;
-      while (P < Gs) P <<= 1;
       const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
-      for (int s = tid; s < P; s += NT) {
+      const int Gp = (Gs + 127) / 128 * 128;
+      for (int s = tid; s < Gp; s += NT) {
         uint32_t mx = 0u;
         if (s < Gs) {
           const int g1 = min(G, (s + 1) * f);
           for (int g = s * f; g < g1; ++g) mx = max(mx, __ldcg(gm + g));
         }
-        s_v[s] = mx;
+        s_g[s] = mx;
       }
       __syncthreads();
-      bitonic_sort<NT, true>(s_v, P);
-      if (tid == 0) s_theta = static_cast<uint32_t>(s_v[k - 1]);
+      block_kth_largest<NT>(s_g, Gs, k, &s_theta);
     }
     __syncthreads();
     const uint32_t theta = s_theta;
-    // ---- append candidates of this segment ----
-    uint32_t* ck = a.cand_key + static_cast<int64_t>(row) * a.cap;
-    int32_t* ci = a.cand_idx + static_cast<int64_t>(row) * a.cap;
-    for (int e0 = lo; e0 < hi; e0 += NT) {
-      const int e = e0 + tid;
-      uint32_t key = 0u;
-      if (e < hi) key = f32_to_key(__ldcg(srow + e));
-      const bool take = e < hi && key >= theta;
-      const unsigned mask = __ballot_sync(0xffffffffu, take);
-      if (mask) {
-        const int leader = __ffs(mask) - 1;
-        int base = 0;
-        if (lane == leader) base = atomicAdd(a.cnt + row, __popc(mask));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        const int slot = base + __popc(mask & ((1u << lane) - 1u));
-        if (take && slot >= 0 && slot < a.cap) { ck[slot] = key; ci[slot] = e; }
+    // ---- ordered compaction of the entries >= theta ----
+    uint32_t keys[PER];
+    int n = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      keys[u] = e0 + u < hi ? f32_to_key(sv[u]) : 0u;
+      n += keys[u] >= theta && keys[u] != 0u;
+    }
+    int tot;
+    int pos = block_scan_excl<NT>(n, s_warp, &tot);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      if (keys[u] >= theta && keys[u] != 0u) {
+        if (pos < CAP) { s_ck[pos] = keys[u]; s_ci[pos] = e0 + u; }
+        ++pos;
       }
     }
+    C = tot <= CAP ? tot : -1;
+    __syncthreads();
   }
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int ticket = atomicAdd(a.done + row, 1);
-    s_last = ticket == static_cast<int>(gridDim.y) - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
 
-  // ---- the last CTA of the row selects ----
-  const int C = atomicAdd(a.cnt + row, 0);
-  if (C >= 0 && C <= a.cap && C <= SORTCAP) {
-    int P = 1;
-    while (P < C) P <<= 1;
-    const uint32_t* ck = a.cand_key + static_cast<int64_t>(row) * a.cap;
-    const int32_t* ci = a.cand_idx + static_cast<int64_t>(row) * a.cap;
-    for (int s = tid; s < P; s += NT) {
-      unsigned long long v = 0ull;
-      if (s < C) v = (static_cast<unsigned long long>(__ldcg(ck + s)) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(__ldcg(ci + s)));
-      s_v[s] = v;
+  if (multi) {
+    // ---- store this segment's candidates; the last CTA of the row gathers them in order ----
+    const int64_t rs = static_cast<int64_t>(row) * a.nseg + segi;
+    uint32_t* ck = a.cand_key + rs * a.seg_cap;
+    int32_t* ci = a.cand_idx + rs * a.seg_cap;
+    const int nstore = (C >= 0 && C <= a.seg_cap) ? C : -1;
+    for (int u = tid; u < nstore; u += NT) { ck[u] = s_ck[u]; ci[u] = s_ci[u]; }
+    if (tid == 0) a.seg_cnt[rs] = nstore;
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const int ticket = atomicAdd(a.done + row, 1);
+      s_last = ticket == static_cast<int>(gridDim.y) - 1;
     }
     __syncthreads();
-    bitonic_sort<NT, true>(s_v, P);  // (key desc, index asc)
-    int K2 = 1;
-    while (K2 < k) K2 <<= 1;
-    // keep the first k, re-key by (index, key) and sort ascending by index
-    unsigned long long tmp[(1024 + NT - 1) / NT];
-    int c = 0;
-    for (int s = tid; s < K2; s += NT, ++c) {
-      unsigned long long v = ~0ull;
-      if (s < k) {
-        const unsigned long long x = s_v[s];
-        const uint32_t idx = 0xFFFFFFFFu - static_cast<uint32_t>(x & 0xFFFFFFFFu);
-        v = (static_cast<unsigned long long>(idx) << 32) | static_cast<uint32_t>(x >> 32);
+    if (!s_last) return;
+    __threadfence();
+    // gather every segment's list, in segment (= index) order
+    C = 0;
+    for (int sg = 0; sg < a.nseg; ++sg) {
+      const int64_t r2 = static_cast<int64_t>(row) * a.nseg + sg;
+      const int n2 = __ldcg(a.seg_cnt + r2);
+      if (n2 < 0 || C + n2 > CAP) { C = -1; break; }
+      for (int u = tid; u < n2; u += NT) {
+        s_ck[C + u] = __ldcg(a.cand_key + r2 * a.seg_cap + u);
+        s_ci[C + u] = __ldcg(a.cand_idx + r2 * a.seg_cap + u);
       }
-      tmp[c] = v;
+      C += n2;
     }
     __syncthreads();
-    c = 0;
-    for (int s = tid; s < K2; s += NT, ++c) s_v[s] = tmp[c];
+    if (tid == 0) a.done[row] = 0;
+  }
+
+  uint32_t T;
+  if (C >= k) {
+    // ---- exact k-th largest key among the candidates ----
+    for (int c = C + tid; c < (C + 127) / 128 * 128; c += NT) s_ck[c] = 0u;
     __syncthreads();
-    bitonic_sort<NT, false>(s_v, K2);
-    for (int p = tid; p < k; p += NT) {
-      const unsigned long long v = s_v[p];
-      oi[p] = static_cast<int32_t>(v >> 32);
-      if (os) os[p] = key_to_f32(static_cast<uint32_t>(v & 0xFFFFFFFFu));
-    }
-  } else {
-    // ---- overflow: exact k-th key by bisection over the whole row ----
-    uint32_t T = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t c = T | (1u << bit);
-      int n = 0;
-      for (int e = tid; e < vis; e += NT) n += f32_to_key(__ldcg(srow + e)) >= c;
-      if (block_sum<NT>(n, s_red) >= k) T = c;
-    }
-    int ngt = 0;
-    for (int e = tid; e < vis; e += NT) ngt += f32_to_key(__ldcg(srow + e)) > T;
-    const int need_eq = k - block_sum<NT>(ngt, s_red);
-    // ordered compaction: all keys > T, and the first need_eq keys == T by index
-    int out_pos = 0, eq_seen = 0;
-    for (int e0 = 0; e0 < vis; e0 += NT) {
-      const int e = e0 + tid;
-      const uint32_t key = e < vis ? f32_to_key(__ldcg(srow + e)) : 0u;
-      const bool gt = e < vis && key > T, eq = e < vis && key == T;
-      const unsigned meq = __ballot_sync(0xffffffffu, eq);
-      // rank of this tie among the CTA's ties of this chunk
-      __syncthreads();
-      if (lane == 0) s_red[tid >> 5] = __popc(meq);
-      __syncthreads();
-      int before = 0, tot = 0;
-      for (int w = 0; w < NT / 32; ++w) { const int c = s_red[w]; if (w < (tid >> 5)) before += c; tot += c; }
-      const int eq_rank = eq_seen + before + __popc(meq & ((1u << lane) - 1u));
-      eq_seen += tot;
-      const bool sel = gt || (eq && eq_rank < need_eq);
-      const unsigned msel = __ballot_sync(0xffffffffu, sel);
-      __syncthreads();
-      if (lane == 0) s_red[tid >> 5] = __popc(msel);
-      __syncthreads();
-      int sb = 0, st = 0;
-      for (int w = 0; w < NT / 32; ++w) { const int c = s_red[w]; if (w < (tid >> 5)) sb += c; st += c; }
-      if (sel) {
-        const int p = out_pos + sb + __popc(msel & ((1u << lane) - 1u));
-        if (p < k) { oi[p] = e; if (os) os[p] = key_to_f32(key); }
+    block_kth_largest<NT>(s_ck, C, k, &s_T);
+    __syncthreads();
+    T = s_T;
+    // counts of keys above T and equal to T, in one reduction (both <= CAP < 2^16)
+    int pk = 0;
+    for (int c = tid; c < C; c += NT) pk += (s_ck[c] > T ? 1 : 0) + (s_ck[c] == T ? 0x10000 : 0);
+    pk = block_sum<NT>(pk, s_warp);
+    const int need_eq = k - (pk & 0xFFFF), n_eq = pk >> 16;
+    // ---- ordered output: keys > T, and the first need_eq keys == T ----
+    int eq_seen = 0, out_pos = 0;
+    for (int c0 = 0; c0 < C; c0 += NT) {
+      const int c = c0 + tid;
+      const uint32_t key = c < C ? s_ck[c] : 0u;
+      bool sel;
+      if (n_eq == need_eq) {  // every key equal to T is kept (the usual case): one scan
+        sel = c < C && key >= T;
+      } else {
+        const bool eq = c < C && key == T;
+        int eq_tot;
+        const int eq_rank = eq_seen + block_scan_excl<NT>(eq ? 1 : 0, s_warp, &eq_tot);
+        eq_seen += eq_tot;
+        sel = c < C && (key > T || (eq && eq_rank < need_eq));
       }
-      out_pos += st;
+      int sel_tot;
+      const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
+      out_pos += sel_tot;
+      if (sel && p < k) {
+        oi[p] = s_ci[c];
+        if (os) os[p] = key_to_f32(key);
+      }
+    }
+    return;
+  }
+
+  // ---- overflow (or an inconsistent count): exact k-th key by bisection over the whole row ----
+  T = 0u;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t c = T | (1u << bit);
+    int n = 0;
+    for (int e = tid; e < vis; e += NT) n += f32_to_key(__ldcg(srow + e)) >= c;
+    if (block_sum<NT>(n, s_warp) >= k) T = c;
+  }
+  int ngt = 0;
+  for (int e = tid; e < vis; e += NT) ngt += f32_to_key(__ldcg(srow + e)) > T;
+  const int need_eq = k - block_sum<NT>(ngt, s_warp);
+  int out_pos = 0, eq_seen = 0;
+  for (int e0 = 0; e0 < vis; e0 += NT) {
+    const int e = e0 + tid;
+    const uint32_t key = e < vis ? f32_to_key(__ldcg(srow + e)) : 0u;
+    const bool eq = e < vis && key == T;
+    int eq_tot;
+    const int eq_rank = eq_seen + block_scan_excl<NT>(eq ? 1 : 0, s_warp, &eq_tot);
+    eq_seen += eq_tot;
+    const bool sel = e < vis && (key > T || (eq && eq_rank < need_eq));
+    int sel_tot;
+    const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
+    out_pos += sel_tot;
+    if (sel && p < k) {
+      oi[p] = e;
+      if (os) os[p] = key_to_f32(key);
     }
   }
-  __syncthreads();
-  if (tid == 0) { a.cnt[row] = 0; a.done[row] = 0; }
 }
 
 }  // namespace lcc

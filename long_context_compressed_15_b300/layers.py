@@ -11,7 +11,7 @@ for the branch-by-branch form, the branch partials) for fixed sizes, so
 repeated calls allocate nothing and a step can be captured in a CUDA graph.
 Every step runs in liblcc's kernels.  ``fused=True`` (default) computes the
 layer as one softmax over the union of the compressed and window keys
-(lcc_csa_layer_attn / lcc_hca_layer_attn); ``fused=False`` runs the two
+(lcc_csa_layer / lcc_hca_layer_attn); ``fused=False`` runs the two
 branches separately and merges them by log-sum-exp (the same result, with
 the branch partials O_c/L_c, O_h/L_h and O_w/L_w kept for inspection).
 """
@@ -19,8 +19,8 @@ from __future__ import annotations
 
 import torch
 
-from . import (attn_merge, csa_layer_attn, csa_sparse_attn, dense_attn_workspace, hca_dense_attn, hca_layer_attn,
-               index_topk_workspace, layer_attn_workspace, lightning_index_topk, swa_attn)
+from . import (attn_merge, csa_layer, csa_layer_workspace, csa_sparse_attn, dense_attn_workspace, hca_dense_attn,
+               hca_layer_attn, index_topk_workspace, layer_attn_workspace, lightning_index_topk, swa_attn)
 
 
 class CsaLayerPlan:
@@ -37,16 +37,16 @@ class CsaLayerPlan:
             self.O_w = torch.empty((B, Tq, H, D), **f32)
             self.L_w = torch.empty((B, Tq, H), **f32)
         self.out = torch.empty((B, Tq, H, D), dtype=torch.bfloat16, device=device)
-        self.ws = torch.empty(max(16, index_topk_workspace(B, Tq, Ncap, k)), dtype=torch.uint8, device=device)
-        n = layer_attn_workspace(B, Tq, H, D, k + W) if fused else 0
-        self.ws_attn = torch.empty(n, dtype=torch.uint8, device=device) if n else None
+        n = csa_layer_workspace(B, Tq, H, D, Ncap, k, W) if fused else index_topk_workspace(B, Tq, Ncap, k)
+        self.ws = torch.empty(max(16, n), dtype=torch.uint8, device=device)
 
     def __call__(self, q, qI, w, q_pos0, kI, n_valid, Kc, Vc, Kr, Vr, raw_pos0, kI_scale=None, stream=None):
+        if self.fused:
+            return csa_layer(q, qI, w, q_pos0, kI, n_valid, self.m, self.k, Kc, Vc, Kr, Vr, raw_pos0, self.W,
+                             kI_scale=kI_scale, scale=self.scale, idx=self.idx, out=self.out, workspace=self.ws,
+                             stream=stream)
         lightning_index_topk(qI, w, q_pos0, kI, n_valid, self.m, self.k, kI_scale=kI_scale, idx=self.idx,
                              workspace=self.ws, stream=stream)
-        if self.fused:
-            return csa_layer_attn(q, Kc, Vc, self.idx, Kr, Vr, q_pos0, raw_pos0, self.W, self.scale, out=self.out,
-                                  workspace=self.ws_attn, stream=stream)
         csa_sparse_attn(q, Kc, Vc, self.idx, self.scale, O=self.O_c, lse=self.L_c, stream=stream)
         swa_attn(q, Kr, Vr, q_pos0, raw_pos0, self.W, self.scale, O=self.O_w, lse=self.L_w, stream=stream)
         return attn_merge([(self.O_c, self.L_c), (self.O_w, self.L_w)], out=self.out, stream=stream)

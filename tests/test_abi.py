@@ -85,14 +85,16 @@ def test_null_and_shape_errors_are_reported_on_host(lib):
 
 
 def test_workspace_sizes(lib):
-    # per query row: scores, one group maximum per 16 entries, a 2048-entry candidate list, two counters
+    # per query row: scores, one group maximum per 16 entries, two counters and, for rows longer than
+    # one 16384-entry top-k segment, a 1024-entry candidate list and a count per segment
     def row_bytes(n):
-        return n * 4 + (n + 15) // 16 * 4 + 2048 * 8 + 8
+        nseg = (n + 16383) // 16384
+        return n * 4 + (n + 15) // 16 * 4 + 8 + (nseg * (1024 * 8 + 4) if nseg > 1 else 0)
     assert lcc.index_topk_workspace(32, 1, 16384, 128) >= 32 * row_bytes(16384)
     assert lcc.index_topk_workspace(4, 1, 262160, 128) >= 4 * row_bytes(262160)
     # prefill scores are processed in bounded query chunks (2^28 scores)
     rows = (1 << 28) // 32768
-    assert lcc.index_topk_workspace(1, 131072, 32768, 128) <= rows * row_bytes(32768) + 5 * 256
+    assert lcc.index_topk_workspace(1, 131072, 32768, 128) <= rows * row_bytes(32768) + 6 * 256
     assert lcc.layer_attn_workspace(32, 1, 64, 128, 256) > 0      # decode layers split the key list
     assert lcc.layer_attn_workspace(1, 4096, 64, 128, 256) == 0   # prefill layers write bf16 directly
     assert lcc.dense_attn_workspace(8, 1, 64, 128, 8192) > 0      # decode splits the key range

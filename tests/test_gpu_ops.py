@@ -120,9 +120,11 @@ def test_index_topk_prefill_causal_with_ties():
     assert near <= 2
 
 
-def test_index_topk_zero_score_ties_bit_exact():
-    # weights of zero make every score 0: the top-k must be the lowest indices
-    B, Ncap, k = 2, 3000, 64
+@pytest.mark.parametrize("Ncap", [3000, 40000])
+def test_index_topk_zero_score_ties_bit_exact(Ncap):
+    # weights of zero make every score 0: the top-k must be the lowest indices (3000 entries: one
+    # top-k CTA whose candidate list overflows; 40000: three segments whose lists overflow)
+    B, k = 2, 64
     qI = datagen.normal_bf16(23, 5, (B, 1, 8, 64)).to(DEV)
     w = torch.zeros((B, 1, 8), dtype=torch.float32, device=DEV)
     kI = datagen.normal_bf16(23, 7, (B, Ncap, 64)).to(DEV)
@@ -283,9 +285,12 @@ def test_merge_parity(nb, D):
 # ---------------------------------------------------------------------------
 # whole layers in one pass: compressed keys ++ window keys, one softmax
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("B,Tq,H,D,k,W", [(3, 1, 64, 128, 128, 128), (2, 40, 8, 64, 16, 32), (1, 7, 16, 128, 70, 100)])
-def test_csa_layer_attn_parity(B, Tq, H, D, k, W):
-    Ncap, R = 400, 160
+# the first three run the warp-split kernel (short key lists); the last is long enough for the
+# split-across-CTAs path with its combine kernel
+@pytest.mark.parametrize("B,Tq,H,D,k,W,Ncap", [(3, 1, 64, 128, 128, 128, 400), (2, 40, 8, 64, 16, 32, 400),
+                                               (1, 7, 16, 128, 70, 100, 400), (2, 1, 64, 128, 1000, 128, 1500)])
+def test_csa_layer_attn_parity(B, Tq, H, D, k, W, Ncap):
+    R = 160
     q = datagen.normal_bf16(36, 4, (B, Tq, H, D), scale=D ** -0.5)
     Kc = datagen.normal_bf16(36, 8, (B, Ncap, D))
     Vc = datagen.normal_bf16(36, 9, (B, Ncap, D))
@@ -310,9 +315,13 @@ def test_csa_layer_attn_parity(B, Tq, H, D, k, W):
             assert_lse_close(lse[b, i].cpu().numpy(), L, f"CSA layer lse [{b},{i}]")
 
 
-@pytest.mark.parametrize("B,Tq,H,D,m,W", [(3, 1, 64, 128, 128, 128), (1, 300, 8, 64, 4, 32), (2, 9, 64, 128, 4, 128)])
-def test_hca_layer_attn_parity(B, Tq, H, D, m, W):
-    Ncap, R = 700, 300
+# warp-split kernel for the short lists; 3000 entries take the split-across-CTAs path; 2000 prefill
+# queries fill enough CTAs for the single-pass kernel that writes bf16 directly
+@pytest.mark.parametrize("B,Tq,H,D,m,W,Ncap", [(3, 1, 64, 128, 128, 128, 700), (1, 300, 8, 64, 4, 32, 700),
+                                               (2, 9, 64, 128, 4, 128, 700), (3, 1, 64, 128, 128, 128, 3000),
+                                               (1, 2000, 64, 128, 4, 128, 600)])
+def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
+    R = 300 if Tq < 300 else Tq
     q = datagen.normal_bf16(37, 4, (B, Tq, H, D), scale=D ** -0.5)
     Kc = datagen.normal_bf16(37, 8, (B, Ncap, D))
     Vc = datagen.normal_bf16(37, 9, (B, Ncap, D))
@@ -326,8 +335,9 @@ def test_hca_layer_attn_parity(B, Tq, H, D, m, W):
                              torch.tensor(n_valid, dtype=torch.int32, device=DEV), m, Kr.to(DEV), Vr.to(DEV),
                              torch.tensor(qpos, device=DEV), torch.tensor(raw0, device=DEV), W)
     lcc.sync_status()
+    rows = range(Tq) if Tq <= 300 else sorted(set(range(0, Tq, 7)) | {Tq - 1})
     for b in range(B):
-        for i in range(Tq):
+        for i in rows:
             t = qpos[b] + i
             h = runs.hca_branch(f64(q[b, i]), t, f64(Kc[b]), f64(Vc[b]), m, n_valid=n_valid[b])
             sw = runs.swa_branch(f64(q[b, i]), t, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
