@@ -240,6 +240,36 @@ lcc_status launch_index_tc(const IndexArgs& ia, cudaStream_t s) {
   return launch_index_tc_q<HI, DI, 128 / HI>(ia, tm, 1, s);
 }
 
+unsigned long long g_index_topk_tc_done[2][2] = {};
+constexpr int kFusedTopkMaxK = 256;
+
+// Prefill: indexer with the streaming top-k in its epilogue (no score buffer).
+template <int HI, int DI>
+lcc_status launch_index_topk_tc(const lcc_bf16* qI, const float* w, int B, int Tq, const int64_t* q_pos0,
+                                const void* kI, const int32_t* n_valid, int Ncap, int m, int k, int32_t* idx,
+                                float* score, cudaStream_t s) {
+  constexpr int NQ = 128 / HI, STAGES = 3;
+  using X = IndexTopkTcCfg<HI, DI, NQ, STAGES>;
+  auto kern = k_index_topk_tc<HI, DI, NQ, STAGES>;
+  CUtensorMap tm;
+  lcc_status st = make_tmap_2d(&tm, kI, DI, static_cast<uint64_t>(B) * Ncap, DI, DI, 128,
+                               DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "k_index_topk_tc");
+  if (st != LCC_OK) return st;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(kern, X::SMEM, g_index_topk_tc_done[HI == 8][DI == 64])) != LCC_OK) return st;
+  }
+  IndexTopkTcArgs a{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, n_valid, Ncap, m, k, idx, score};
+  const int groups = (Tq + NQ - 1) / NQ;
+  launch_k(kern, dim3(1, groups, B), dim3(320), X::SMEM, s, false, tm, a);
+  return launch_check("k_index_topk_tc");
+}
+
+bool use_fused_topk(lcc_key_format fmt, int Tq, int HI, int k) {
+  return fmt == LCC_KEY_BF16 && static_cast<int64_t>(Tq) * HI > 16 && k <= kFusedTopkMaxK &&
+         (Tq + 128 / HI - 1) / (128 / HI) <= 65535;
+}
+
 template <int HI, int DI, bool FP4>
 lcc_status launch_index_score(const IndexArgs& a, cudaStream_t s) {
   constexpr int QPT = 8 / HI;
@@ -326,6 +356,12 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
                           lcc_key_format fmt, const void* kI, const uint8_t* kI_scale, const int32_t* n_valid,
                           int Ncap, int m, int k, int32_t* idx, float* score, void* scratch, int qc,
                           cudaStream_t s) {
+  if (use_fused_topk(fmt, Tq, HI, k)) {
+    if (HI == 8 && DI == 64) return launch_index_topk_tc<8, 64>(qI, w, B, Tq, q_pos0, kI, n_valid, Ncap, m, k, idx, score, s);
+    if (HI == 8 && DI == 32) return launch_index_topk_tc<8, 32>(qI, w, B, Tq, q_pos0, kI, n_valid, Ncap, m, k, idx, score, s);
+    if (HI == 4 && DI == 64) return launch_index_topk_tc<4, 64>(qI, w, B, Tq, q_pos0, kI, n_valid, Ncap, m, k, idx, score, s);
+    return launch_index_topk_tc<4, 32>(qI, w, B, Tq, q_pos0, kI, n_valid, Ncap, m, k, idx, score, s);
+  }
   const IndexWs ws = index_ws_rows(static_cast<int64_t>(B) * qc, Ncap);
   char* base = static_cast<char*>(scratch);
   float* scores = reinterpret_cast<float*>(base);

@@ -343,3 +343,20 @@ def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
             sw = runs.swa_branch(f64(q[b, i]), t, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
             O, _ = oracle.merge([h["O"], sw["O"]], [h["lse"], sw["lse"]])
             assert_close(out[b, i].float().cpu().numpy(), O, f"HCA layer [{b},{i}]")
+
+
+def test_index_topk_prefill_fused_zero_score_ties():
+    # prefill-shaped calls keep a running top-k inside the indexer; with zero weights every score
+    # ties, so each query must keep its lowest visible indices (candidate buffers compact often)
+    B, Tq, HI, DI, Ncap, k, m = 1, 300, 8, 64, 1000, 64, 4
+    qI = datagen.normal_bf16(26, 5, (B, Tq, HI, DI)).to(DEV)
+    w = torch.zeros((B, Tq, HI), dtype=torch.float32, device=DEV)
+    kI = datagen.normal_bf16(26, 7, (B, Ncap, DI)).to(DEV)
+    q0 = 3000
+    idx = lcc.lightning_index_topk(qI, w, q0, kI, Ncap, m, k)
+    torch.cuda.synchronize()
+    g = idx.cpu().numpy()[0]
+    for i in range(Tq):
+        vis = min(Ncap, (q0 + i + 1) // m)
+        want = np.arange(min(vis, k))
+        assert np.array_equal(g[i, :len(want)], want) and np.all(g[i, len(want):] == -1), f"row {i}"
