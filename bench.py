@@ -25,9 +25,7 @@ import hashlib
 import json
 import math
 import os
-import subprocess
 import sys
-import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -78,37 +76,71 @@ def max_over_ranks(x: float, ws: int) -> float:
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Polls SM clock and clock-event reasons through NVML on a host thread.
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
-        self.p = None
+    Samples are taken every `period` seconds between start() and stop(), plus
+    one on demand (sample_now, called right after the timed steps are
+    enqueued, while the device is still running them), so even a timed region
+    of a few milliseconds has samples.  Nothing is set on the device."""
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, device: int, period: float = 0.002):
+        import threading
+        self.period = period
+        self.samples = []
+        self.stop_ev = threading.Event()
+        self.th = None
+        self.h = None
+        self.err = None
+        try:
+            import pynvml
+            self.nv = pynvml
+            pynvml.nvmlInit()
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            try:
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device)
+            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM))
+        except Exception as e:  # no NVML: report the clocks as unavailable
+            self.err = f"nvml unavailable: {type(e).__name__}"
+
+    def sample_now(self):
+        if self.h is None:
+            return
+        nv = self.nv
+        try:
+            sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+            r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+            self.samples.append((float(sm), int(r)))
+        except Exception as e:
+            self.err = f"nvml query failed: {type(e).__name__}"
+
+    def _loop(self):
+        while not self.stop_ev.is_set():
+            self.sample_now()
+            self.stop_ev.wait(self.period)
 
     def start(self):
-        try:
-            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "50"],
-                                      stdout=self.f, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.p = None
+        import threading
+        if self.h is not None:
+            self.th = threading.Thread(target=self._loop, daemon=True)
+            self.th.start()
 
     def stop(self):
-        if self.p is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
-        self.p.terminate()
-        self.p.wait()
-        self.f.flush()
-        rows = [l.split(",") for l in open(self.f.name).read().strip().splitlines() if l.strip()]
-        os.unlink(self.f.name)
-        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4) if r[5 + i].strip() == "Active"})
-        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+        if self.th is not None:
+            self.stop_ev.set()
+            self.th.join()
+        busy = [(s, r) for s, r in self.samples if not r & 0x1]  # drop samples taken while the GPU idled
+        if self.h is None or not busy:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [self.err or "no samples under load"],
+                    "samples": 0}
+        sm = [s for s, _ in busy]
+        reasons = sorted({n for _, r in busy for n, bit in self.REASONS if r & bit})
+        return {"sm_mhz": float(np.median(sm)), "sm_min_mhz": min(sm), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(busy), "idle_samples": len(self.samples) - len(busy),
+                "source": "nvml"}
 
 
 # ---------------------------------------------------------------------------
@@ -154,8 +186,10 @@ def blas_threads():
         return 1
 
 
-def time_graph(graph_runs, stream):
-    """graph_runs: list of callables (graph replays); returns seconds (CUDA events)."""
+def time_graph(graph_runs, stream, on_enqueued=None):
+    """graph_runs: list of callables (graph replays); returns seconds (CUDA events).
+    on_enqueued runs on the host after the last replay is enqueued, while the
+    device is still executing the timed steps."""
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -163,6 +197,8 @@ def time_graph(graph_runs, stream):
     for g in graph_runs:
         g.replay()
     end.record(stream)
+    if on_enqueued is not None:
+        on_enqueued()
     torch.cuda.synchronize()
     return start.elapsed_time(end) / 1e3
 
@@ -657,9 +693,10 @@ def run_ours(args, ws, rank, local):
 
     time_graph(sch.runs(args.warmup), stream)
     barrier(ws)
-    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local)
+    clocks = ClockSampler(torch.cuda.current_device())
+    runs = sch.runs(args.steps)
     clocks.start()
-    t = time_graph(sch.runs(args.steps), stream)
+    t = time_graph(runs, stream, on_enqueued=clocks.sample_now)
     ck = clocks.stop()
     barrier(ws)
     lcc.sync_status()

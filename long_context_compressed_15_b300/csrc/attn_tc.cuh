@@ -40,6 +40,9 @@ struct AttnTcArgs {
   bf16* out_bf16;     // [B*Tq*H, D] bf16, or
   float* O;           // [B*Tq*H, D] fp32 with
   float* lse;         // [B*Tq*H] (optional with out_bf16)
+  int rpt;            // rows per CTA tile: 128, or H (one query's heads) for decode
+  int tps;            // key tiles per split (gridDim.z splits the tile list)
+  int64_t rows_total; // B*Tq*H: distance between the fp32 partials of two splits
 };
 
 template <int D>
@@ -85,14 +88,14 @@ __global__ void __launch_bounds__(192, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
   const int64_t rows_b = static_cast<int64_t>(a.Tq) * a.H;
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 128;
+  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * a.rpt;  // rows past rpt are padding
 
   // ---- per-row key ranges (softmax threads own one row each) ----
   int lo1 = 0, hi1 = 0, lo2 = 0, hi2 = 0;
   bool row_ok = false;
   if (warp < 4) {
     const int64_t r = row0 + threadIdx.x;
-    row_ok = r < rows_b;
+    row_ok = static_cast<int>(threadIdx.x) < a.rpt && r < rows_b;
     if (row_ok) {
       const int qi = static_cast<int>(r / a.H);
       const int64_t t = __ldg(a.q_pos0 + b) + qi;
@@ -146,7 +149,9 @@ __global__ void __launch_bounds__(192, 1)
   const int rlo1 = s_rng[0], rhi1 = s_rng[1], rlo2 = s_rng[2], rhi2 = s_rng[3];
   const int T1 = rhi1 > rlo1 ? (rhi1 - rlo1 + 127) / 128 : 0;
   const int T2 = rhi2 > rlo2 ? (rhi2 - rlo2 + 127) / 128 : 0;
-  const int ntiles = T1 + T2;
+  // this split's run of the tile list (tiles of source 1, then of the window)
+  const int tt0 = static_cast<int>(blockIdx.z) * a.tps;
+  const int ntiles = max(0, min(T1 + T2, tt0 + a.tps) - tt0);
   uint8_t* sQ = smem + C::OFF_Q;
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
@@ -165,10 +170,11 @@ __global__ void __launch_bounds__(192, 1)
         const int s = t % C::STAGES;
         if (*s_abort || !tc::mbar_wait(kv_empty + s, ((t / C::STAGES) & 1) ^ 1, 11)) { *s_abort = 1; break; }
         tc::mbar_arrive_expect_tx(kv_full + s, 2 * C::OP);
-        const bool w = t >= T1;
+        const int tg = tt0 + t;
+        const bool w = tg >= T1;
         const CUtensorMap* mk = w ? &tmK2 : &tmK1;
         const CUtensorMap* mv = w ? &tmV2 : &tmV1;
-        const int y = w ? b * a.Ncap2 + rlo2 + (t - T1) * 128 : b * a.Ncap1 + rlo1 + t * 128;
+        const int y = w ? b * a.Ncap2 + rlo2 + (tg - T1) * 128 : b * a.Ncap1 + rlo1 + tg * 128;
         for (int h = 0; h < D / 64; ++h) {
           tc::tma_load_2d(sK + s * C::OP + h * C::HALF, mk, kv_full + s, h * 64, y);
           tc::tma_load_2d(sV + s * C::OP + h * C::HALF, mv, kv_full + s, h * 64, y);
@@ -243,8 +249,9 @@ __global__ void __launch_bounds__(192, 1)
       tc::tc_fence_before();
       tc::mbar_arrive(s_free + sb);
       // mask and scale into the log2 domain
-      const bool w = t >= T1;
-      const int j0 = w ? rlo2 + (t - T1) * 128 : rlo1 + t * 128;
+      const int tg = tt0 + t;
+      const bool w = tg >= T1;
+      const int j0 = w ? rlo2 + (tg - T1) * 128 : rlo1 + tg * 128;
       const int lo = row_ok ? (w ? lo2 : lo1) : 0, hi = row_ok ? (w ? hi2 : hi1) : 0;
       float mx = -INFINITY;
 #pragma unroll
@@ -310,7 +317,8 @@ __global__ void __launch_bounds__(192, 1)
     // ---- epilogue: O / l ----
     if (ntiles > 0 && ok) ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(o_full, 0, 20));
     tc::tc_fence_after();
-    const int64_t grow = static_cast<int64_t>(b) * rows_b + row0 + r;
+    const int64_t grow = static_cast<int64_t>(b) * rows_b + row0 + r +
+                         static_cast<int64_t>(blockIdx.z) * a.rows_total;  // split partials
     const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
     for (int c = 0; c < D / 32; ++c) {

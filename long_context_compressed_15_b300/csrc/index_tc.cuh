@@ -264,14 +264,17 @@ __device__ __forceinline__ uint32_t warp_kth(const uint32_t (&v)[CAPQ / 32], int
 
 // Keep the top-k of a query's buffer (key desc, index asc); returns the new
 // count (min(n, k)) and sets *theta to the k-th key when n >= k.  One warp.
+// Every register array is indexed by compile-time constants (unrolled
+// loops), so it stays in registers.
 template <int CAPQ>
 __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* ids, int n, int k, uint32_t* theta) {
+  constexpr int V = CAPQ / 32;
   const int lane = threadIdx.x & 31;
   if (n <= k) return n;
-  uint32_t v[CAPQ / 32];
-  int32_t id[CAPQ / 32];
+  uint32_t v[V];
+  int32_t id[V];
 #pragma unroll
-  for (int i = 0; i < CAPQ / 32; ++i) {
+  for (int i = 0; i < V; ++i) {
     const int e = lane + 32 * i;
     v[i] = e < n ? keys[e] : 0u;
     id[i] = e < n ? ids[e] : 0x7FFFFFFF;
@@ -279,26 +282,33 @@ __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* ids, int n,
   const uint32_t T = warp_kth<CAPQ>(v, k);
   int gt = 0, eq = 0;
 #pragma unroll
-  for (int i = 0; i < CAPQ / 32; ++i) { gt += v[i] > T; eq += v[i] == T; }
+  for (int i = 0; i < V; ++i) { gt += v[i] > T; eq += v[i] == T; }
   gt = __reduce_add_sync(0xffffffffu, gt);
   eq = __reduce_add_sync(0xffffffffu, eq);
   const int need_eq = k - gt;
-  __syncwarp();
-  // kept = keys above T, and the need_eq lowest indices among keys equal to T
+  // which of my entries are kept: keys above T, and the need_eq lowest indices
+  // among keys equal to T (counted from the buffer itself; only when some
+  // ties must be dropped, which needs exactly equal scores)
+  uint32_t keepm = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    bool keep = v[i] > T;
+    if (v[i] == T) {
+      if (eq == need_eq) {
+        keep = true;
+      } else {
+        int before = 0;
+        for (int e2 = 0; e2 < n; ++e2) before += (keys[e2] == T) && (ids[e2] < id[i]);
+        keep = before < need_eq;
+      }
+    }
+    keepm |= (keep ? 1u : 0u) << i;
+  }
+  __syncwarp();  // every lane has read the buffer before it is overwritten
   int out = 0;
 #pragma unroll
-  for (int i = 0; i < CAPQ / 32; ++i) {
-    const bool tie = v[i] == T;
-    int before = 0;  // ties with a lower index; only needed when some ties are dropped (rare)
-    if (eq != need_eq) {  // warp-uniform
-      for (int j = 0; j < CAPQ / 32; ++j)
-        for (int l2 = 0; l2 < 32; ++l2) {
-          const uint32_t vj = __shfl_sync(0xffffffffu, v[j], l2);
-          const int32_t ij = __shfl_sync(0xffffffffu, id[j], l2);
-          before += (vj == T && ij < id[i]);
-        }
-    }
-    const bool keep = v[i] > T || (tie && (eq == need_eq || before < need_eq));
+  for (int i = 0; i < V; ++i) {
+    const bool keep = (keepm >> i) & 1u;
     const unsigned m = __ballot_sync(0xffffffffu, keep);
     if (keep) {
       const int p = out + __popc(m & ((1u << lane) - 1u));
@@ -472,16 +482,15 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + half * COLS;
     // this warp's queries: head weights and visible counts are fixed for the
     // CTA, thresholds change only at buffer checks -- all kept in registers
-    float wr[QH * HI];
+    // the threshold test runs on floats: key(s) > key(theta) <=> s > f(theta)
+    // with f(0) = -inf (no threshold yet); keys are formed only for entries taken
+    const float4* sW4 = reinterpret_cast<const float4*>(sW) + half * QH * HI / 4;  // broadcast reads
     int visr[QH];
-    uint32_t thr[QH];
+    float thf[QH];
 #pragma unroll
     for (int j = 0; j < QH; ++j) {
-      const int qi = half * QH + j;
-#pragma unroll
-      for (int h = 0; h < HI; ++h) wr[j * HI + h] = sW[qi * HI + h];
-      visr[j] = sVis[qi];
-      thr[j] = 0u;
+      visr[j] = sVis[half * QH + j];
+      thf[j] = -INFINITY;
     }
     for (int t = 0; t < ntiles; ++t) {
       const int acc = t & 1;
@@ -504,21 +513,27 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
       tc::mbar_arrive(tempty + acc);  // the accumulator is in registers: the next MMA may start
       const int entry = t * C::TILE + quarter * 32 + lane;
       const bool all_vis = (t + 1) * C::TILE <= vis_min;  // every query sees the whole tile
-      uint32_t keys[QH];
+      float sc[QH];
       bool any = false;
 #pragma unroll
       for (int j = 0; j < QH; ++j) {
         float s = 0.f;
 #pragma unroll
-        for (int h = 0; h < HI; ++h) s = fmaf(wr[j * HI + h], fmaxf(v[j * HI + h], 0.f), s);
-        keys[j] = (all_vis || entry < visr[j]) ? f32_to_key(s) : 0u;
-        any |= keys[j] > thr[j];
+        for (int h4 = 0; h4 < HI / 4; ++h4) {
+          const float4 wv = sW4[j * HI / 4 + h4];
+          s = fmaf(wv.x, fmaxf(v[j * HI + 4 * h4 + 0], 0.f), s);
+          s = fmaf(wv.y, fmaxf(v[j * HI + 4 * h4 + 1], 0.f), s);
+          s = fmaf(wv.z, fmaxf(v[j * HI + 4 * h4 + 2], 0.f), s);
+          s = fmaf(wv.w, fmaxf(v[j * HI + 4 * h4 + 3], 0.f), s);
+        }
+        sc[j] = (all_vis || entry < visr[j]) ? s : -INFINITY;
+        any |= sc[j] > thf[j];
       }
-      if (__any_sync(0xffffffffu, any)) {  // rare once the thresholds have settled
+      if (__any_sync(0xffffffffu, any)) {  // some entry of this warp passes a threshold
 #pragma unroll
         for (int j = 0; j < QH; ++j) {
           const int qi = half * QH + j;
-          const bool take = keys[j] > thr[j];
+          const bool take = sc[j] > thf[j];
           const unsigned msk = __ballot_sync(0xffffffffu, take);
           if (msk) {
             const int leader = __ffs(msk) - 1;
@@ -528,7 +543,7 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
             if (take) {
               const int slot = base + __popc(msk & ((1u << lane) - 1u));
               if (slot < X::CAPQ) {  // cannot fail: buffers keep room for SYNC whole tiles
-                sKeys[qi * X::CAPQ + slot] = keys[j];
+                sKeys[qi * X::CAPQ + slot] = f32_to_key(sc[j]);
                 sIds[qi * X::CAPQ + slot] = entry;
               }
             }
@@ -549,7 +564,10 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
         }
         tc::named_sync(1, NEPI);
 #pragma unroll
-        for (int j = 0; j < QH; ++j) thr[j] = sTheta[half * QH + j];
+        for (int j = 0; j < QH; ++j) {
+          const uint32_t th = sTheta[half * QH + j];
+          thf[j] = th == 0u ? -INFINITY : key_to_f32(th);
+        }
       }
     }
     // ---- final: exact top-k of every query, in ascending index order ----

@@ -525,7 +525,7 @@ bool use_attn_tc(int B, int Tq, int H, int D) {
 
 // src1 (K1/V1, rows kv_rs1 apart, Ncap1 per batch) and optional window src2.
 lcc_status launch_attn_tc(AttnTcArgs a, const bf16* q, const bf16* K1, const bf16* V1, int64_t kv_rs1,
-                          const bf16* K2, const bf16* V2, int64_t kv_rs2, cudaStream_t s, bool pdl) {
+                          const bf16* K2, const bf16* V2, int64_t kv_rs2, int nsplit, cudaStream_t s, bool pdl) {
   constexpr int D = 128;
   using Cf = AttnTcCfg<D>;
   CUtensorMap tq, tk1, tv1, tk2, tv2;
@@ -551,11 +551,58 @@ lcc_status launch_attn_tc(AttnTcArgs a, const bf16* q, const bf16* K1, const bf1
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if ((st = ensure_smem(k_attn_tc<D>, Cf::SMEM, g_attn_tc_done)) != LCC_OK) return st;
   }
-  const int64_t gx = (static_cast<int64_t>(a.Tq) * a.H + 127) / 128;
+  if (a.rpt <= 0) a.rpt = 128;
+  if (a.tps <= 0) a.tps = 0x3FFFFFFF;
+  const int64_t gx = (static_cast<int64_t>(a.Tq) * a.H + a.rpt - 1) / a.rpt;
   if (gx > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "k_attn_tc: too many rows");
-  launch_k(k_attn_tc<D>, dim3(static_cast<unsigned>(gx), a.B), dim3(192), Cf::SMEM, s, pdl, tq, tk1, tv1, tk2, tv2,
-           a);
+  launch_k(k_attn_tc<D>, dim3(static_cast<unsigned>(gx), a.B, nsplit), dim3(192), Cf::SMEM, s, pdl, tq, tk1, tv1, tk2,
+           tv2, a);
   return launch_check("k_attn_tc");
+}
+
+// Decode-sized calls on the tensor cores: one query's H <= 128 heads per CTA
+// tile (the rest of the 128-row MMA is padding), the key tiles split across
+// CTAs, fp32 partials combined to the output.  Returns LCC_ERR_UNSUPPORTED
+// when this path does not apply (the caller then uses another kernel).
+size_t tc_decode_ws(int B, int Tq, int H, int D, int64_t keys, int* nsplit_out, int* tps_out) {
+  const int64_t tiles = (keys + 127) / 128;
+  const int64_t ctas = static_cast<int64_t>(B) * Tq;
+  int64_t ns = (num_sms() + ctas - 1) / ctas;
+  if (ns > tiles) ns = tiles;
+  if (ns < 1) ns = 1;
+  const int64_t tps = (tiles + ns - 1) / ns;
+  ns = (tiles + tps - 1) / tps;
+  if (nsplit_out) *nsplit_out = static_cast<int>(ns);
+  if (tps_out) *tps_out = static_cast<int>(tps);
+  const int64_t rows = static_cast<int64_t>(B) * Tq * H;
+  return ns > 1 ? round_up(ns * rows * D * sizeof(float), 256) + round_up(ns * rows * sizeof(float), 256) : 0;
+}
+
+lcc_status tc_decode_attn(AttnTcArgs t, int D, int64_t keys, const bf16* q, const bf16* K1, const bf16* V1,
+                          int64_t rs1, const bf16* K2, const bf16* V2, int64_t rs2, bf16* out, float* O, float* lse,
+                          void* workspace, size_t workspace_bytes, cudaStream_t s, const char* name) {
+  int ns = 1, tps = 1;
+  const size_t need = tc_decode_ws(t.B, t.Tq, t.H, D, keys, &ns, &tps);
+  if (ns > 1 && (!workspace || workspace_bytes < need))
+    return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, need);
+  const int64_t rowsT = static_cast<int64_t>(t.B) * t.Tq * t.H;
+  t.rpt = t.H;
+  t.tps = tps;
+  t.rows_total = rowsT;
+  if (ns == 1) {
+    t.out_bf16 = out;
+    t.O = O;
+    t.lse = lse;
+    return launch_attn_tc(t, q, K1, V1, rs1, K2, V2, rs2, 1, s, false);
+  }
+  float* Op = static_cast<float*>(workspace);
+  float* lp = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(ns * rowsT * D * sizeof(float), 256));
+  t.out_bf16 = nullptr;
+  t.O = Op;
+  t.lse = lp;
+  lcc_status st = launch_attn_tc(t, q, K1, V1, rs1, K2, V2, rs2, ns, s, false);
+  if (st != LCC_OK) return st;
+  return launch_combine<128>(Op, lp, ns, rowsT, O, lse, out, s);
 }
 
 unsigned long long g_wsplit_done[2][2] = {};
@@ -698,7 +745,7 @@ lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
     t.O = O; t.lse = lse;
-    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, s, false);
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, 1, s, false);
   }
   if (ns == 1) {
     a.O = O; a.lse = lse;
@@ -739,7 +786,7 @@ lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float sc
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_WINDOW; t.Ncap1 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
     t.O = O; t.lse = lse;
-    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, static_cast<cudaStream_t>(stream),
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0, 1, static_cast<cudaStream_t>(stream),
                           false);
   }
   return dispatch_attn<ATT_WINDOW>(a, D, dim3(static_cast<unsigned>(rblocks), B, 1), 64,
@@ -752,7 +799,9 @@ size_t lcc_layer_attn_workspace(int B, int Tq, int H, int D, int n_keys) {
   const int64_t rb_csa = static_cast<int64_t>(B) * Tq * ((H + 63) / 64);
   const int64_t rb_hca = static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 63) / 64);
   const int64_t rb = rb_csa < rb_hca ? rb_csa : rb_hca;
-  return split_ws_bytes(splits_for(rb, n_keys), static_cast<int64_t>(B) * Tq * H, D);
+  const size_t legacy = split_ws_bytes(splits_for(rb, n_keys), static_cast<int64_t>(B) * Tq * H, D);
+  const size_t tcd = D == 128 ? tc_decode_ws(B, Tq, H, D, n_keys, nullptr, nullptr) : 0;
+  return legacy > tcd ? legacy : tcd;
 }
 
 }  // extern "C"
@@ -871,8 +920,18 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
     t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
     t.win2 = true; t.Ncap2 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
     t.out_bf16 = reinterpret_cast<bf16*>(out); t.lse = lse_out;
-    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, a.K2, a.V2, r_rstride, static_cast<cudaStream_t>(stream),
+    return launch_attn_tc(t, a.q, a.K, a.V, kv_rstride, a.K2, a.V2, r_rstride, 1, static_cast<cudaStream_t>(stream),
                           false);
+  }
+  const int64_t groups16 = static_cast<int64_t>(B) * Tq * ((H + 15) / 16);
+  if (D == 128 && H <= 128 && !use_wsplit<ATT_RANGE>(groups16, static_cast<int64_t>(Ncap) + W)) {
+    AttnTcArgs t{};
+    t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
+    t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
+    t.win2 = true; t.Ncap2 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
+    return tc_decode_attn(t, D, static_cast<int64_t>(Ncap) + W, a.q, a.K, a.V, kv_rstride, a.K2, a.V2, r_rstride,
+                          reinterpret_cast<bf16*>(out), nullptr, lse_out, workspace, workspace_bytes,
+                          static_cast<cudaStream_t>(stream), name);
   }
   return layer_attn_impl<ATT_RANGE>(name, a, D, static_cast<int64_t>(B) * rblocks, static_cast<unsigned>(rblocks),
                                     64, static_cast<int64_t>(Ncap) + W, out, lse_out, workspace, workspace_bytes,

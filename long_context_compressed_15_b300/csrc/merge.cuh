@@ -90,6 +90,7 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
   const int lane = threadIdx.x & 31;
   pdl_wait();  // the partials come from the split attention kernel
   if (row >= rows) return;
+  // every split's lse at once (lane s holds splits s, s+32, ...), then weights
   float L = -INFINITY;
   for (int s = lane; s < nsplit; s += 32) L = fmaxf(L, __ldg(lp + s * rows + row));
   L = warp_max(L);
@@ -98,14 +99,42 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float tot = 0.f;
   if (L != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float ls = __ldg(lp + s * rows + row);
-      if (ls == -INFINITY) continue;
-      const float w = expf(ls - L);
-      tot += w;
-      const float* src = Op + (s * rows + row) * D + lane * PER;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+      const int sl = s0 + lane;
+      const float ls = sl < nsplit ? __ldg(lp + sl * rows + row) : -INFINITY;
+      const float wl = ls == -INFINITY ? 0.f : expf(ls - L);
+      const int n = min(32, nsplit - s0);
+      // partial rows are independent loads: issue them in groups of four
+      int j = 0;
+      for (; j + 4 <= n; j += 4) {
+        float wj[4];
+        const float* src[4];
 #pragma unroll
-      for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, __ldg(src + e), acc[e]);
+        for (int u = 0; u < 4; ++u) {
+          wj[u] = __shfl_sync(0xffffffffu, wl, j + u);
+          src[u] = Op + ((s0 + j + u) * rows + row) * D + lane * PER;
+        }
+        float x[4][PER];  // an empty split's partial is written as zeros: no branch needed
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int e = 0; e < PER; ++e) x[u][e] = __ldg(src[u] + e);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          tot += wj[u];
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(wj[u], x[u][e], acc[e]);
+        }
+      }
+      for (; j < n; ++j) {
+        const float wj = __shfl_sync(0xffffffffu, wl, j);
+        tot += wj;
+        if (wj != 0.f) {
+          const float* src = Op + ((s0 + j) * rows + row) * D + lane * PER;
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[e] = fmaf(wj, __ldg(src + e), acc[e]);
+        }
+      }
     }
   }
   const float inv = tot > 0.f ? 1.0f / tot : 0.f;
