@@ -86,6 +86,7 @@ class ClockSampler:
                ("sw_power_cap", 0x4), ("hw_power_brake_slowdown", 0x80))
 
     def __init__(self, device: int, period: float = 0.002):
+        import ctypes
         import threading
         self.period = period
         self.samples = []
@@ -93,29 +94,36 @@ class ClockSampler:
         self.th = None
         self.h = None
         self.err = None
-        try:
-            import pynvml
-            self.nv = pynvml
-            pynvml.nvmlInit()
+        try:  # NVML's C API through ctypes (the driver ships libnvidia-ml)
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
             uuid = str(torch.cuda.get_device_properties(device).uuid)
-            try:
-                self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            except Exception:
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(device)
-            self.max_mhz = float(pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM))
+            uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            if nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(device), ctypes.byref(h)) != 0:
+                    raise RuntimeError("no NVML handle for the device")
+            self.nv, self.h, self.ct = nv, h, ctypes
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            nv.nvmlDeviceGetMaxClockInfo(h, ctypes.c_int(1), ctypes.byref(mx))  # 1 = SM clock domain
+            self.max_mhz = float(mx.value)
         except Exception as e:  # no NVML: report the clocks as unavailable
-            self.err = f"nvml unavailable: {type(e).__name__}"
+            self.h = None
+            self.err = f"nvml unavailable: {type(e).__name__}: {e}"
 
     def sample_now(self):
         if self.h is None:
             return
-        nv = self.nv
-        try:
-            sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
-            r = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-            self.samples.append((float(sm), int(r)))
-        except Exception as e:
-            self.err = f"nvml query failed: {type(e).__name__}"
+        ct = self.ct
+        sm, r = ct.c_uint(), ct.c_ulonglong()
+        if self.nv.nvmlDeviceGetClockInfo(self.h, ct.c_int(1), ct.byref(sm)) == 0 and \
+                self.reasons_fn(self.h, ct.byref(r)) == 0:
+            self.samples.append((float(sm.value), int(r.value)))
+        else:
+            self.err = "nvml query failed"
 
     def _loop(self):
         while not self.stop_ev.is_set():
@@ -344,7 +352,7 @@ class HcaDecodeBench:
     """HCA layer decode at 1M context: batch 8, 8192 m=128 entries + 128-token window."""
     unit = "queries/s"
     name = "hca_decode"
-    dominant = "k_attn<RANGE+window>+k_split_combine"
+    dominant = "k_attn_tc<RANGE+window>+k_split_combine"
     bound = "hbm"
     graph_steps = 64
 
@@ -463,7 +471,7 @@ class CsaPrefillBench:
     """CSA layer prefill of one 131072-token sequence (pool, indexer + top-k, sparse + window attention)."""
     unit = "tokens/s"
     name = "csa_prefill"
-    dominant = "k_index_tc+k_topk_thr"
+    dominant = "k_index_topk_tc"
     bound = "tensor"
     graph_steps = 1
 
