@@ -18,7 +18,9 @@
 #include "attn_tc.cuh"
 #include "index.cuh"
 #include "index_tc.cuh"
+#include "index_topk_tc.cuh"
 #include "topk_thr.cuh"
+#include "topk_cluster.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -65,6 +67,27 @@ cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// Launch `kern` as clusters of `cx` CTAs along x (grid.x a multiple of cx).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kc(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      unsigned cx, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cx;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
@@ -132,6 +155,21 @@ int index_chunk(int B, int Tq, int Ncap) {
 
 int gmax_stride(int Ncap) { return (Ncap + 15) / 16; }
 int topk_segments(int Ncap) { return (Ncap + kTopkSeg - 1) / kTopkSeg; }
+
+// Cluster top-k (one cluster of up to 8 CTAs per row): rows of up to
+// 8 * kClSeg entries, k up to kClMaxG / 2 with k * (entries per group) <= kClCap.
+constexpr int kClNT = 256;
+constexpr int kClPer = 8;
+constexpr int kClSeg = kClNT * kClPer;
+constexpr int kClCap = 4096;
+constexpr int kClMaxG = 512;
+using ClSmem = TopkClSmem<kClNT, kClPer, kClCap, kClMaxG>;
+unsigned long long g_topk_cl_done = 0;
+
+int topk_cluster_ctas(int Ncap, int k, int gs) {
+  if (Ncap > 8 * kClSeg || 2 * k > kClMaxG || static_cast<int64_t>(k) * gs > kClCap) return 0;
+  return (Ncap + kClSeg - 1) / kClSeg;
+}
 
 // Scratch of one query chunk (rows = B * queries in the chunk): scores,
 // group maxima, per-row counters and, for rows longer than one top-k
@@ -404,7 +442,19 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
     ta.out_i = idx;
     ta.out_s = score;
     const int64_t rows = static_cast<int64_t>(B) * nq;
-    if (rows > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
+    if (rows > 0x7FFFFFFF / 8) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
+    const int cl = topk_cluster_ctas(Ncap, k, ta.gs);
+    if (cl > 0) {
+      auto kern = k_topk_cluster<kClNT, kClPer, kClCap, kClMaxG>;
+      {
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if ((st = ensure_smem(kern, ClSmem::total, g_topk_cl_done)) != LCC_OK) return st;
+      }
+      launch_kc(kern, dim3(static_cast<unsigned>(rows * cl)), dim3(kClNT), ClSmem::total, s, true,
+                static_cast<unsigned>(cl), ta);
+      if ((st = launch_check("k_topk_cluster")) != LCC_OK) return st;
+      continue;
+    }
     launch_k(k_topk_thr<kTopkNT, kTopkPer, kCandCap>, dim3(static_cast<unsigned>(rows), nseg), dim3(kTopkNT), 0, s,
              true, ta);
     if ((st = launch_check("k_topk_thr")) != LCC_OK) return st;

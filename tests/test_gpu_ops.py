@@ -111,6 +111,18 @@ def test_index_topk_decode_two_stage(HI, DI):
     assert near <= 1
 
 
+@pytest.mark.parametrize("HI,DI", [(8, 64), (4, 32)])
+def test_index_topk_decode_cluster(HI, DI):
+    # rows of up to 16384 entries go to the cluster top-k (one CTA per 2048 entries); the visible
+    # counts cover a full row, rows whose group maxima give no threshold (fewer than k groups: 4000,
+    # 2049 entries, the latter one entry into the second CTA), a row just above k and one below it
+    B, Ncap = 5, 16384
+    near, g = _index_case(26, B, 1, HI, DI, Ncap, 4, 128, q_pos0=[4 * Ncap - 1] * B,
+                          n_valid=[Ncap, 4000, 2049, 129, 50])
+    assert np.all(g[4, 0, 50:] == -1) and np.all(g[4, 0, :50] == np.arange(50))
+    assert near <= 1
+
+
 def test_index_topk_prefill_causal_with_ties():
     # 4 heads: about 1 in 16 entries scores exactly 0 (all four ReLUs vanish); early
     # queries see fewer than k entries and must be padded
