@@ -398,7 +398,8 @@ struct WsplitSmem {
   static constexpr size_t q_bytes = size_t(16) * D * 2;
   static constexpr size_t kv_bytes = size_t(KT) * D * 2;          // one of K or V, one warp
   static constexpr size_t tile_bytes = (2 * kv_bytes + KT * 4 + 127) / 128 * 128;  // K, V, key ids of a warp
-  static constexpr size_t comb_bytes = size_t(NW) * 16 * (D + 2) * 4;
+  static constexpr int CS = D + 8;  // combine row stride (floats): conflict-free float2 stores of the MMA layout
+  static constexpr size_t comb_bytes = size_t(NW) * 16 * (CS + 2) * 4;
   static constexpr size_t work = NW * tile_bytes > comb_bytes ? NW * tile_bytes : comb_bytes;
   static constexpr size_t total = q_bytes + work;
 };
@@ -516,13 +517,14 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit(AttnArgs a) {
 
   // ---- combine the warps' states ----
   __syncthreads();  // all tiles consumed: the work area becomes the combine area
-  float* cO = reinterpret_cast<float*>(work);                    // [NW][16][D]
-  float* cM = cO + NW * 16 * D;                                  // [NW][16]
+  constexpr int CS = S::CS;
+  float* cO = reinterpret_cast<float*>(work);                    // [NW][16][CS]
+  float* cM = cO + NW * 16 * CS;                                 // [NW][16]
   float* cL = cM + NW * 16;                                      // [NW][16]
 #pragma unroll
   for (int n = 0; n < NDT; ++n) {
-    *reinterpret_cast<float2*>(cO + (warp * 16 + g) * D + 8 * n + 2 * c4) = make_float2(oacc[n][0], oacc[n][1]);
-    *reinterpret_cast<float2*>(cO + (warp * 16 + g + 8) * D + 8 * n + 2 * c4) = make_float2(oacc[n][2], oacc[n][3]);
+    *reinterpret_cast<float2*>(cO + (warp * 16 + g) * CS + 8 * n + 2 * c4) = make_float2(oacc[n][0], oacc[n][1]);
+    *reinterpret_cast<float2*>(cO + (warp * 16 + g + 8) * CS + 8 * n + 2 * c4) = make_float2(oacc[n][2], oacc[n][3]);
   }
   if (c4 == 0) {
     cM[warp * 16 + g] = m0; cL[warp * 16 + g] = l0;
@@ -546,16 +548,27 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit(AttnArgs a) {
   if (h0 + r < a.H) {
     const int64_t orow = qrow * a.H + h0 + r;
     bf16* o = a.out_bf16 + orow * D + d0;
+    // each thread reads its DPT consecutive floats of every warp's row as one vector
+    float x[DPT];
 #pragma unroll
-    for (int d = 0; d < DPT; d += 2) {
-      float x0 = 0.f, x1 = 0.f;
+    for (int d = 0; d < DPT; ++d) x[d] = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        x0 = fmaf(wt[w], cO[(w * 16 + r) * D + d0 + d], x0);
-        x1 = fmaf(wt[w], cO[(w * 16 + r) * D + d0 + d + 1], x1);
+    for (int w = 0; w < NW; ++w) {
+      const float* src = cO + (w * 16 + r) * CS + d0;
+      if constexpr (DPT == 4) {
+        const float4 v = *reinterpret_cast<const float4*>(src);
+        x[0] = fmaf(wt[w], v.x, x[0]); x[1] = fmaf(wt[w], v.y, x[1]);
+        x[2] = fmaf(wt[w], v.z, x[2]); x[3] = fmaf(wt[w], v.w, x[3]);
+      } else {
+#pragma unroll
+        for (int d = 0; d < DPT; d += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(src + d);
+          x[d] = fmaf(wt[w], v.x, x[d]); x[d + 1] = fmaf(wt[w], v.y, x[d + 1]);
+        }
       }
-      *reinterpret_cast<uint32_t*>(o + d) = pack_bf16(x0 * inv, x1 * inv);
     }
+#pragma unroll
+    for (int d = 0; d < DPT; d += 2) *reinterpret_cast<uint32_t*>(o + d) = pack_bf16(x[d] * inv, x[d + 1] * inv);
     if (a.lse && tid % TPR == 0) a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
 }

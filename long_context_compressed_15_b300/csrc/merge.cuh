@@ -104,35 +104,29 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
       const float ls = sl < nsplit ? __ldg(lp + sl * rows + row) : -INFINITY;
       const float wl = ls == -INFINITY ? 0.f : expf(ls - L);
       const int n = min(32, nsplit - s0);
-      // partial rows are independent loads: issue them in groups of four
-      int j = 0;
-      for (; j + 4 <= n; j += 4) {
-        float wj[4];
-        const float* src[4];
+      // partial rows are independent loads: up to 16 vector loads in flight per lane
+      for (int j = 0; j < n; j += 16) {
+        float wj[16];
+        float x[16][PER];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          wj[u] = __shfl_sync(0xffffffffu, wl, j + u);
-          src[u] = Op + ((s0 + j + u) * rows + row) * D + lane * PER;
+        for (int u = 0; u < 16; ++u) {
+          wj[u] = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
+          const bool in = j + u < n;  // an empty split's partial is written as zeros
+          const float* src = Op + ((s0 + j + u) * rows + row) * D + lane * PER;
+          if constexpr (PER == 4) {
+            const float4 v = in ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < PER; ++e) x[u][e] = in ? __ldg(src + e) : 0.f;
+          }
+          if (!in) wj[u] = 0.f;
         }
-        float x[4][PER];  // an empty split's partial is written as zeros: no branch needed
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-#pragma unroll
-          for (int e = 0; e < PER; ++e) x[u][e] = __ldg(src[u] + e);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < 16; ++u) {
           tot += wj[u];
 #pragma unroll
           for (int e = 0; e < PER; ++e) acc[e] = fmaf(wj[u], x[u][e], acc[e]);
-        }
-      }
-      for (; j < n; ++j) {
-        const float wj = __shfl_sync(0xffffffffu, wl, j);
-        tot += wj;
-        if (wj != 0.f) {
-          const float* src = Op + ((s0 + j) * rows + row) * D + lane * PER;
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[e] = fmaf(wj, __ldg(src + e), acc[e]);
         }
       }
     }

@@ -8,20 +8,22 @@
 //
 // The same threshold argument as k_topk_thr (theta = k-th largest
 // super-group maximum is a lower bound of the k-th largest score), spread
-// over the CL CTAs of a cluster so that each SM touches 1/CL of the row and
-// of the counting work, and the CTAs exchange through distributed shared
-// memory instead of global memory:
-//   1. every CTA loads its SEG = NT*PER scores and builds all super-group
-//      maxima from the group maxima; CTA r counts the r-th share of them and
-//      the owner of the k-th largest writes theta into every CTA;
-//   2. every CTA compacts its entries >= theta in index order (its list is
-//      complete: SEG entries at most), then gathers all CTAs' keys in rank
-//      (= index) order; CTA r counts the r-th share of the candidates and
-//      the owner of the exact k-th largest key T writes it into CTA 0;
-//   3. CTA 0 writes every candidate above T and the lowest-index candidates
-//      equal to T.
-// Candidates that do not fit CAP (massive exact ties) fall back to a
-// bisection over the row's scores in CTA 0.  Control flow through the
+// over the CL CTAs of a cluster so that each SM loads 1/CL of the row:
+//   1. every CTA loads its SEG = NT*PER scores, builds all super-group
+//      maxima from the group maxima and finds theta itself (the same
+//      deterministic selection in every CTA: no exchange);
+//   2. every CTA compacts its entries >= theta (a run in index order),
+//      reserves room for the run in CTA 0 with one atomic on CTA 0's shared
+//      counter and stores it there through distributed shared memory, with
+//      the run's place and length; one cluster barrier;
+//   3. CTA 0 lays the runs out in CTA (= index) order, selects the exact
+//      k-th largest key T and writes every candidate above T and the
+//      lowest-index candidates equal to T.
+// Selections use a 256-bin histogram over the current key interval, each
+// round narrowing the interval to the bin that holds the k-th value (at
+// most four rounds for 32-bit keys), so no step is quadratic in the number
+// of values.  Candidates that do not fit CAP (massive exact ties) fall back
+// to a bisection over the row's scores in CTA 0.  Control flow through the
 // cluster barriers depends only on per-row values, so every CTA of the
 // cluster meets each barrier.
 #pragma once
@@ -61,72 +63,137 @@ __device__ __forceinline__ uint32_t ld(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t atom_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
 }  // namespace clu
 
-// The elements vals[s0..s1) that are the k-th largest of vals[0..n) (zero
-// padded to a multiple of 128): v with #{x > v} < k <= #{x >= v}.  Each one
-// found is stored at shared variable `dst` of the cluster CTAs [r0, r1).
-// Every thread of the CTA calls this with the same arguments.
+// k-th largest of vals[0..n) (1 <= k <= n), returned to every thread of
+// the CTA (every thread calls this).  Each round histograms the values in
+// the current interval [lo, hi] into 256 bins of width w = ceil((hi-lo+1)/256),
+// finds the bin holding the k-th largest of them and narrows the interval to
+// it; with w = 1 the bin is a single value.
 template <int NT>
-__device__ __forceinline__ void kth_share(const uint32_t* vals, int n, int k, int s0, int s1, const uint32_t* dst,
-                                          uint32_t r0, uint32_t r1) {
-  const int ne = s1 - s0;
-  if (ne <= 0) return;
-  const int tpe = threads_per_elem<NT>(ne);
-  const int np4 = (n + 127) / 128 * 32;
-  const int groups = NT / tpe, part = threadIdx.x % tpe;
-  const uint4* v4 = reinterpret_cast<const uint4*>(vals);
-  for (int it = 0; it < (ne + groups - 1) / groups; ++it) {
-    const int e = s0 + it * groups + static_cast<int>(threadIdx.x) / tpe;
-    const bool real = e < s1;
-    const uint32_t v = real ? vals[e] : 0xFFFFFFFFu;
-    int gt = 0, ge = 0;
-#pragma unroll 4
-    for (int w = part; w < np4; w += tpe) {
-      const uint4 x = v4[w];
-      gt += (x.x > v) + (x.y > v) + (x.z > v) + (x.w > v);
-      ge += (x.x >= v) + (x.y >= v) + (x.z >= v) + (x.w >= v);
-    }
-    for (int o = 1; o < tpe; o <<= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o);
-      ge += __shfl_xor_sync(0xffffffffu, ge, o);
-    }
-    if (real && part == 0 && gt < k && ge >= k)
-      for (uint32_t r = r0; r < r1; ++r) clu::st(clu::map(dst, r), v);
+__device__ __forceinline__ uint32_t block_kth_hist(const uint32_t* vals, int n, int k, uint32_t* s_hist,
+                                                   uint32_t* s_bc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t mn = 0xFFFFFFFFu, mx = 0u;
+  for (int i = tid; i < n; i += NT) {
+    const uint32_t v = vals[i];
+    mn = min(mn, v);
+    mx = max(mx, v);
   }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    mn = min(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
+  for (int b = tid; b < 256; b += NT) s_hist[b] = 0u;
+  if (lane == 0) {
+    atomicMin(s_bc + 2, mn);
+    atomicMax(s_bc + 3, mx);
+  }
+  __syncthreads();
+  uint32_t lo = s_bc[2], hi = s_bc[3];
+  int krem = k;
+  while (true) {
+    const uint64_t range = static_cast<uint64_t>(hi) - lo + 1;
+    const uint32_t w = static_cast<uint32_t>((range + 255) / 256);
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t v = vals[i];
+      if (v >= lo && v <= hi) atomicAdd(s_hist + (v - lo) / w, 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane L owns bins 8L .. 8L+7; suffix sums from the top bin down
+      uint32_t h[8], t = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[j] = s_hist[lane * 8 + j];
+        t += h[j];
+      }
+      uint32_t above = t;  // inclusive suffix over lanes >= lane
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xffffffffu, above, o);
+        if (lane + o < 32) above += y;
+      }
+      uint32_t run = above - t;  // values in bins of higher lanes
+      int bstar = -1;
+      uint32_t ab = 0;
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        if (bstar < 0 && run + h[j] >= static_cast<uint32_t>(krem)) {
+          bstar = lane * 8 + j;
+          ab = run;
+        }
+        run += h[j];
+      }
+      int best = bstar;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) best = max(best, __shfl_xor_sync(0xffffffffu, best, o));
+      if (bstar == best && bstar >= 0) {
+        s_bc[0] = static_cast<uint32_t>(bstar);
+        s_bc[1] = ab;
+      }
+    }
+    __syncthreads();
+    const uint32_t bs = s_bc[0];
+    krem -= static_cast<int>(s_bc[1]);
+    const uint32_t nlo = lo + bs * w;
+    const uint64_t nhi = static_cast<uint64_t>(nlo) + w - 1;
+    hi = nhi < hi ? static_cast<uint32_t>(nhi) : hi;
+    lo = nlo;
+    if (w == 1u) break;
+    for (int b = tid; b < 256; b += NT) s_hist[b] = 0u;
+    __syncthreads();
+  }
+  __syncthreads();  // s_bc and s_hist may be reused after the return
+  if (tid == 0) {
+    s_bc[2] = 0xFFFFFFFFu;
+    s_bc[3] = 0u;
+  }
+  return lo;
 }
 
 template <int NT, int PER, int CAP, int MAXG>
 struct TopkClSmem {
-  static constexpr int SEG = NT * PER;
-  static constexpr size_t lk = 0;                                   // this CTA's candidates (keys)
-  static constexpr size_t li = lk + SEG * 4;                        // ... and their entries
-  static constexpr size_t ck = li + SEG * 4;                        // all candidates' keys (+ zero pad)
-  static constexpr size_t ci = ck + (CAP + 128) * 4;                // all candidates' entries (CTA 0)
-  static constexpr size_t g = ci + CAP * 4;                         // super-group maxima (+ zero pad)
-  static constexpr size_t total = g + (MAXG + 128) * 4;
+  static constexpr size_t ck = 0;                   // candidate keys, in arrival order (CTA 0)
+  static constexpr size_t ci = ck + CAP * 4;        // ... their entries
+  static constexpr size_t ok = ci + CAP * 4;        // candidate keys in index order (CTA 0)
+  static constexpr size_t oi = ok + CAP * 4;        // ... their entries
+  static constexpr size_t g = oi + CAP * 4;         // super-group maxima
+  static constexpr size_t total = g + MAXG * 4;
 };
 
 // MAXG: most super-groups (2k); the host routes rows to this kernel only when
-// 2k <= MAXG, k * (entries per group) <= CAP and the row fits CL*SEG entries.
+// 2k <= MAXG, k * (entries per group) <= CAP and the row fits 8*NT*PER entries.
 template <int NT, int PER, int CAP, int MAXG>
 __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
   using L = TopkClSmem<NT, PER, CAP, MAXG>;
-  constexpr int SEG = L::SEG;
+  constexpr int SEG = NT * PER;
   static_assert(PER % 4 == 0, "4-wide loads");
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint32_t* s_lk = reinterpret_cast<uint32_t*>(smem + L::lk);
-  int32_t* s_li = reinterpret_cast<int32_t*>(smem + L::li);
+  extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(smem + L::ck);
   int32_t* s_ci = reinterpret_cast<int32_t*>(smem + L::ci);
+  uint32_t* s_ok = reinterpret_cast<uint32_t*>(smem + L::ok);
+  int32_t* s_oi = reinterpret_cast<int32_t*>(smem + L::oi);
   uint32_t* s_g = reinterpret_cast<uint32_t*>(smem + L::g);
   __shared__ int s_warp[NT / 32];
-  __shared__ uint32_t s_theta, s_T;
-  __shared__ int s_cnt;
-  __shared__ int s_off[9];
+  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_bc[4];
+  __shared__ uint32_t s_cnt, s_base;
+  __shared__ uint32_t s_rb[8], s_rc[8];  // CTA 0: place and length of each CTA's run
 
   const int tid = threadIdx.x;
   const uint32_t rk = clu::rank(), CL = clu::size();
+  if (tid == 0) {  // before the arrive, so that no remote access can precede these
+    s_cnt = 0u;
+    s_bc[2] = 0xFFFFFFFFu;
+    s_bc[3] = 0u;
+  }
   clu::arrive();  // every CTA of the cluster has started before any remote access (wait below)
   const int row = static_cast<int>(blockIdx.x / CL);
   const int b = row / a.nq, i = a.q0 + row % a.nq;
@@ -167,38 +234,24 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
     for (int u = 0; u < PER; ++u) sv[u] = e0 + u < hi ? __ldcg(srow + e0 + u) : 0.f;
   }
 
-  // super-group maxima (all of them, in every CTA)
+  // theta from the super-group maxima (the same value in every CTA)
   const int G = (vis + a.gs - 1) / a.gs;
   const int f = (G + 2 * k - 1) / (2 * k);
   const int Gs = (G + f - 1) / f;
-  const bool use_theta = Gs >= k;
-  if (use_theta) {
+  uint32_t theta = 0u;  // fewer than k super-groups: every visible entry is a candidate
+  if (Gs >= k) {
     const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
-    const int Gp = (Gs + 127) / 128 * 128;
-    for (int s = tid; s < Gp; s += NT) {
+    for (int s = tid; s < Gs; s += NT) {
       uint32_t mx = 0u;
-      if (s < Gs) {
-        const int g1 = min(G, (s + 1) * f);
-        for (int g = s * f; g < g1; ++g) mx = max(mx, __ldcg(gm + g));
-      }
+      const int g1 = min(G, (s + 1) * f);
+      for (int g = s * f; g < g1; ++g) mx = max(mx, __ldcg(gm + g));
       s_g[s] = mx;
     }
+    __syncthreads();
+    theta = block_kth_hist<NT>(s_g, Gs, k, s_hist, s_bc);
   }
-  if (tid == 0) {
-    s_theta = 0u;  // fewer than k super-groups: every visible entry is a candidate
-    s_T = 0u;
-  }
-  __syncthreads();
-  clu::wait();
-  if (use_theta) {
-    const int spc = (Gs + static_cast<int>(CL) - 1) / static_cast<int>(CL);
-    const int s0 = static_cast<int>(rk) * spc;
-    kth_share<NT>(s_g, Gs, k, s0, min(Gs, s0 + spc), &s_theta, 0u, CL);
-  }
-  clu::sync();  // theta everywhere
-  const uint32_t theta = s_theta;
 
-  // this CTA's candidates, in index order
+  // this CTA's run of candidates, stored into CTA 0
   uint32_t keys[PER];
   int n = 0;
 #pragma unroll
@@ -208,52 +261,56 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
   }
   int tot;
   int pos = block_scan_excl<NT>(n, s_warp, &tot);
+  clu::wait();
+  if (tid == 0) {
+    const uint32_t base = clu::atom_add(clu::map(&s_cnt, 0), static_cast<uint32_t>(tot));
+    s_base = base;
+    clu::st(clu::map(s_rb + rk, 0), base);
+    clu::st(clu::map(s_rc + rk, 0), static_cast<uint32_t>(tot));
+  }
+  __syncthreads();
+  {
+    const int base = static_cast<int>(s_base);
+    const uint32_t rck = clu::map(s_ck, 0), rci = clu::map(s_ci, 0);
 #pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    if (keys[u] >= theta && keys[u] != 0u) {
-      s_lk[pos] = keys[u];
-      s_li[pos] = e0 + u;
-      ++pos;
+    for (int u = 0; u < PER; ++u) {
+      if (keys[u] >= theta && keys[u] != 0u) {
+        const int slot = base + pos;
+        if (slot < CAP) {
+          clu::st(rck + 4u * slot, keys[u]);
+          clu::st(rci + 4u * slot, static_cast<uint32_t>(e0 + u));
+        }
+        ++pos;
+      }
     }
   }
-  if (tid == 0) s_cnt = tot;
-  clu::sync();  // every CTA's list and count
-
-  if (tid < static_cast<int>(CL)) s_off[tid + 1] = static_cast<int>(clu::ld(clu::map(&s_cnt, tid)));
-  if (tid == 0) s_off[0] = 0;
-  __syncthreads();
-  if (tid == 0)
-    for (uint32_t r = 1; r <= CL; ++r) s_off[r] += s_off[r - 1];
-  __syncthreads();
-  const int C = s_off[CL];
-  const bool ok = C >= k && C <= CAP;
-  if (ok) {
-    for (int c = tid; c < C; c += NT) {
-      uint32_t r = 0;
-      while (c >= s_off[r + 1]) ++r;
-      const int j = c - s_off[r];
-      s_ck[c] = clu::ld(clu::map(s_lk + j, r));
-      if (rk == 0) s_ci[c] = static_cast<int32_t>(clu::ld(clu::map(s_li + j, r)));
-    }
-    for (int c = C + tid; c < (C + 127) / 128 * 128; c += NT) s_ck[c] = 0u;
-    __syncthreads();
-    const int cpc = (C + static_cast<int>(CL) - 1) / static_cast<int>(CL);
-    const int c0 = static_cast<int>(rk) * cpc;
-    kth_share<NT>(s_ck, C, k, c0, min(C, c0 + cpc), &s_T, 0u, 1u);
-  }
-  clu::sync();  // T in CTA 0; no remote access after this point
+  clu::sync();  // CTA 0 holds every run; no remote access after this point
   if (rk != 0) return;
 
-  if (ok) {
-    const uint32_t T = s_T;
+  const int C = static_cast<int>(s_cnt);
+  if (C >= k && C <= CAP) {
+    // runs in CTA order = index order
+    for (int c = tid; c < C; c += NT) {
+      int off = 0;
+      for (uint32_t r = 0; r < CL; ++r) {
+        const int rb = static_cast<int>(s_rb[r]), rc = static_cast<int>(s_rc[r]);
+        if (c >= rb && c < rb + rc) {
+          s_ok[off + c - rb] = s_ck[c];
+          s_oi[off + c - rb] = s_ci[c];
+        }
+        off += rc;
+      }
+    }
+    __syncthreads();
+    const uint32_t T = block_kth_hist<NT>(s_ok, C, k, s_hist, s_bc);
     int pk = 0;
-    for (int c = tid; c < C; c += NT) pk += (s_ck[c] > T ? 1 : 0) + (s_ck[c] == T ? 0x10000 : 0);
+    for (int c = tid; c < C; c += NT) pk += (s_ok[c] > T ? 1 : 0) + (s_ok[c] == T ? 0x10000 : 0);
     pk = block_sum<NT>(pk, s_warp);
     const int need_eq = k - (pk & 0xFFFF), n_eq = pk >> 16;
     int eq_seen = 0, out_pos = 0;
     for (int cb = 0; cb < C; cb += NT) {
       const int c = cb + tid;
-      const uint32_t key = c < C ? s_ck[c] : 0u;
+      const uint32_t key = c < C ? s_ok[c] : 0u;
       bool sel;
       if (n_eq == need_eq) {
         sel = c < C && key >= T;
@@ -268,7 +325,7 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
       const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
       out_pos += sel_tot;
       if (sel && p < k) {
-        oi[p] = s_ci[c];
+        oi[p] = s_oi[c];
         if (os) os[p] = key_to_f32(key);
       }
     }
