@@ -9,13 +9,17 @@
 // heads that is two queries -- and walks 128-key tiles of the compressed
 // source then of the window:
 //   warp 4 (TMA)      Q once; K and V tiles (two 64-column swizzled halves
-//                     each) into a two-stage ring;
+//                     each) into two-stage rings; a K stage is released by
+//                     its Q K^T, a V stage by its P V, so the next K tile
+//                     streams in while the softmax still runs;
 //   warp 5 (MMA)      S[t] = Q K[t]^T into one of two TMEM buffers, then
-//                     O += P[t-1] V[t-1] (P from shared memory, V as an
-//                     MN-major operand), O accumulating in TMEM;
-//   warps 0..3        one thread per row (= TMEM lane): read S, mask, online
-//                     softmax in the log2 domain, write P (bf16, swizzled)
-//                     for the tensor core; at the end O / l to global memory.
+//                     O += P[t-1] V[t-1] (P from one of two shared-memory
+//                     buffers, V as an MN-major operand), O in TMEM;
+//   warps 0..3        one thread per row (= TMEM lane): read S, row maximum
+//                     (masking only tiles that cross the row's key range),
+//                     online softmax in the log2 domain with the scale folded
+//                     into one FMA per score, write P (bf16, swizzled) for
+//                     the tensor core; at the end O / l to global memory.
 // The running maximum is only raised (and O, l rescaled) when a tile's
 // maximum exceeds it by more than 8 (a factor 256): P stays <= 2^8, exact
 // in the final normalisation, and O is rarely touched.
@@ -55,8 +59,9 @@ struct AttnTcCfg {
   static constexpr int OFF_K = OFF_Q + OP;
   static constexpr int OFF_V = OFF_K + STAGES * OP;
   static constexpr int OFF_P = OFF_V + STAGES * OP;
-  static constexpr int OFF_BAR = OFF_P + 2 * HALF;      // P: 128 rows x 128 keys
-  static constexpr int NBAR = 1 + 2 * STAGES + 2 + 2 + 2 + 1;
+  static constexpr int PB = 2 * HALF;                   // one P buffer: 128 rows x 128 keys
+  static constexpr int OFF_BAR = OFF_P + 2 * PB;        // two P buffers
+  static constexpr int NBAR = 1 + 4 * STAGES + 2 + 2 + 2 + 2 + 1;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 64 + 1024;
   static constexpr uint32_t IDESC_S = tc::idesc_f16(128, 128, true);            // Q K^T
   static constexpr uint32_t IDESC_O = tc::idesc_f16(128, D, true, false, true); // P V, V MN-major
@@ -74,13 +79,15 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;                 // [STAGES]
-  uint64_t* kv_empty = bars + 1 + C::STAGES;    // [STAGES]
-  uint64_t* s_full = bars + 1 + 2 * C::STAGES;  // [2]
+  uint64_t* k_full = bars + 1;                  // [STAGES]
+  uint64_t* k_empty = k_full + C::STAGES;       // [STAGES]
+  uint64_t* v_full = k_empty + C::STAGES;       // [STAGES]
+  uint64_t* v_empty = v_full + C::STAGES;       // [STAGES]
+  uint64_t* s_full = v_empty + C::STAGES;       // [2]
   uint64_t* s_free = s_full + 2;                // [2]
-  uint64_t* p_full = s_free + 2;                // [1]
-  uint64_t* p_free = p_full + 1;                // [1]
-  uint64_t* o_full = p_free + 1;                // [1]
+  uint64_t* p_full = s_free + 2;                // [2]
+  uint64_t* p_free = p_full + 2;                // [2]
+  uint64_t* o_full = p_free + 2;                // [1]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   int* s_rng = reinterpret_cast<int*>(s_tmem + 2);  // lo1, hi1, lo2, hi2
@@ -128,10 +135,12 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     s_rng[0] = INT_MAX; s_rng[1] = INT_MIN; s_rng[2] = INT_MAX; s_rng[3] = INT_MIN;
     tc::mbar_init(q_full, 1);
-    for (int i = 0; i < C::STAGES; ++i) { tc::mbar_init(kv_full + i, 1); tc::mbar_init(kv_empty + i, 1); }
+    for (int i = 0; i < C::STAGES; ++i) {
+      tc::mbar_init(k_full + i, 1); tc::mbar_init(k_empty + i, 1);
+      tc::mbar_init(v_full + i, 1); tc::mbar_init(v_empty + i, 1);
+    }
     for (int i = 0; i < 2; ++i) { tc::mbar_init(s_full + i, 1); tc::mbar_init(s_free + i, 128); }
-    tc::mbar_init(p_full, 128);
-    tc::mbar_init(p_free, 1);
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(p_full + i, 128); tc::mbar_init(p_free + i, 1); }
     tc::mbar_init(o_full, 1);
     *s_abort = 0;
     tc::fence_barrier_init();
@@ -165,26 +174,40 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_arrive_expect_tx(q_full, C::OP);
       const int qy = static_cast<int>(static_cast<int64_t>(b) * rows_b + row0);
       for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(sQ + h * C::HALF, &tmQ, q_full, h * 64, qy);
-      int issued = 0;
-      for (int t = 0; t < ntiles; ++t) {
-        const int s = t % C::STAGES;
-        if (*s_abort || !tc::mbar_wait(kv_empty + s, ((t / C::STAGES) & 1) ^ 1, 11)) { *s_abort = 1; break; }
-        tc::mbar_arrive_expect_tx(kv_full + s, 2 * C::OP);
-        const int tg = tt0 + t;
+      // K of tile i, then V of tile i - 1: a V stage frees later (after P V)
+      // than a K stage (after Q K^T), so K loads run one tile ahead
+      auto tile_y = [&](int tg, const CUtensorMap*& mk, const CUtensorMap*& mv) {
         const bool w = tg >= T1;
-        const CUtensorMap* mk = w ? &tmK2 : &tmK1;
-        const CUtensorMap* mv = w ? &tmV2 : &tmV1;
-        const int y = w ? b * a.Ncap2 + rlo2 + (tg - T1) * 128 : b * a.Ncap1 + rlo1 + tg * 128;
-        for (int h = 0; h < D / 64; ++h) {
-          tc::tma_load_2d(sK + s * C::OP + h * C::HALF, mk, kv_full + s, h * 64, y);
-          tc::tma_load_2d(sV + s * C::OP + h * C::HALF, mv, kv_full + s, h * 64, y);
+        mk = w ? &tmK2 : &tmK1;
+        mv = w ? &tmV2 : &tmV1;
+        return w ? b * a.Ncap2 + rlo2 + (tg - T1) * 128 : b * a.Ncap1 + rlo1 + tg * 128;
+      };
+      int ik = 0, iv = 0;
+      bool pok = true;
+      for (int i = 0; pok && i <= ntiles; ++i) {
+        const CUtensorMap *mk, *mv;
+        if (i < ntiles) {
+          const int s = i % C::STAGES;
+          if (*s_abort || !tc::mbar_wait(k_empty + s, ((i / C::STAGES) & 1) ^ 1, 11)) { pok = false; break; }
+          tc::mbar_arrive_expect_tx(k_full + s, C::OP);
+          const int y = tile_y(tt0 + i, mk, mv);
+          for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(sK + s * C::OP + h * C::HALF, mk, k_full + s, h * 64, y);
+          ik = i + 1;
         }
-        issued = t + 1;
+        if (i > 0) {
+          const int u = i - 1, s = u % C::STAGES;
+          if (*s_abort || !tc::mbar_wait(v_empty + s, ((u / C::STAGES) & 1) ^ 1, 11)) { pok = false; break; }
+          tc::mbar_arrive_expect_tx(v_full + s, C::OP);
+          const int y = tile_y(tt0 + u, mk, mv);
+          for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(sV + s * C::OP + h * C::HALF, mv, v_full + s, h * 64, y);
+          iv = u + 1;
+        }
       }
+      if (!pok) *s_abort = 1;
       // every copy this CTA started has landed before it may exit
       tc::mbar_wait(q_full, 0, 12);
-      for (int t = max(0, issued - C::STAGES); t < issued; ++t)
-        tc::mbar_wait(kv_full + t % C::STAGES, (t / C::STAGES) & 1, 12);
+      for (int t = max(0, ik - C::STAGES); t < ik; ++t) tc::mbar_wait(k_full + t % C::STAGES, (t / C::STAGES) & 1, 12);
+      for (int t = max(0, iv - C::STAGES); t < iv; ++t) tc::mbar_wait(v_full + t % C::STAGES, (t / C::STAGES) & 1, 12);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -194,7 +217,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int t = 0; ok && t <= ntiles; ++t) {
         if (t < ntiles) {
           const int s = t % C::STAGES, sb = t & 1;
-          if (*s_abort || !tc::mbar_wait(kv_full + s, (t / C::STAGES) & 1, 14) ||
+          if (*s_abort || !tc::mbar_wait(k_full + s, (t / C::STAGES) & 1, 14) ||
               !tc::mbar_wait(s_free + sb, ((t >> 1) & 1) ^ 1, 15)) { ok = false; break; }
           tc::tc_fence_after();
 #pragma unroll
@@ -204,20 +227,23 @@ __global__ void __launch_bounds__(192, 1)
                            tc::smem_desc(ka + s * C::OP + off, 16, 1024, tc::SW_128B), C::IDESC_S, kk > 0);
           }
           tc::mma_commit(s_full + sb);
+          tc::mma_commit(k_empty + s);
         }
         if (t > 0) {
           const int u = t - 1, su = u % C::STAGES;
-          if (*s_abort || !tc::mbar_wait(p_full, u & 1, 16)) { ok = false; break; }
+          const int pb = u & 1;
+          if (*s_abort || !tc::mbar_wait(p_full + pb, (u >> 1) & 1, 16) ||
+              !tc::mbar_wait(v_full + su, (u / C::STAGES) & 1, 16)) { ok = false; break; }
           tc::tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
             const uint32_t poff = (kk >> 2) * C::HALF + (kk & 3) * 32;
-            tc::mma_f16_ss(tmem_o, tc::smem_desc(pa + poff, 16, 1024, tc::SW_128B),
+            tc::mma_f16_ss(tmem_o, tc::smem_desc(pa + pb * C::PB + poff, 16, 1024, tc::SW_128B),
                            tc::smem_desc(va + su * C::OP + kk * 2048, C::HALF, 1024, tc::SW_128B), C::IDESC_O,
                            (u > 0 || kk > 0) ? 1u : 0u);
           }
-          tc::mma_commit(p_free);
-          tc::mma_commit(kv_empty + su);
+          tc::mma_commit(p_free + pb);
+          tc::mma_commit(v_empty + su);
         }
       }
       if (!ok) *s_abort = 1;
@@ -230,6 +256,7 @@ __global__ void __launch_bounds__(192, 1)
     // tcgen05.ld / st are warp-collective: every branch around them is warp-uniform.
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int r = threadIdx.x;
+    const float sc = a.scale_log2;  // > 0 (the host routes other scales elsewhere)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < ntiles; ++t) {
@@ -248,25 +275,31 @@ __global__ void __launch_bounds__(192, 1)
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(s_free + sb);
-      // mask and scale into the log2 domain
+      // row maximum of the raw scores; only a tile that crosses the row's key
+      // range is masked (masked scores become -inf, which the positive scale
+      // keeps at -inf)
       const int tg = tt0 + t;
       const bool w = tg >= T1;
       const int j0 = w ? rlo2 + (tg - T1) * 128 : rlo1 + tg * 128;
       const int lo = row_ok ? (w ? lo2 : lo1) : 0, hi = row_ok ? (w ? hi2 : hi1) : 0;
-      float mx = -INFINITY;
+      if (j0 < lo || j0 + 128 > hi) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const int j = j0 + c;
-        const float x = (j >= lo && j < hi) ? v[c] * a.scale_log2 : -INFINITY;
-        v[c] = x;
-        mx = fmaxf(mx, x);
+        for (int c = 0; c < 128; ++c) {
+          const int j = j0 + c;
+          if (j < lo || j >= hi) v[c] = -INFINITY;
+        }
       }
-      // the previous P V has completed: P may be overwritten and O is stable
-      if (t > 0) {
-        ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(p_free, (t - 1) & 1, 19));
-        if (!ok) break;
-      }
-      tc::tc_fence_after();
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = v[i];
+#pragma unroll
+      for (int c = 8; c < 128; c += 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx8[i] = fmaxf(mx8[i], v[c + i]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + 4]);
+      const float mx = fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])) * sc;
+      const int pb = t & 1;  // P buffer of this tile
       float f = 1.f;
       if (mx > -INFINITY) {
         if (m == -INFINITY) {
@@ -278,6 +311,13 @@ __global__ void __launch_bounds__(192, 1)
         }
       }
       if (__any_sync(0xffffffffu, f != 1.f)) {
+        // O is rescaled in place: the previous P V must have completed
+        if (t > 0) {
+          ok = __all_sync(0xffffffffu,
+                          !*s_abort && tc::mbar_wait(p_free + ((t - 1) & 1), ((t - 1) >> 1) & 1, 19));
+          if (!ok) break;
+        }
+        tc::tc_fence_after();
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           float o[32];
@@ -289,16 +329,24 @@ __global__ void __launch_bounds__(192, 1)
         }
         tc::tmem_wait_st();
       }
-      // P = 2^(z - m) as bf16, K-major swizzled rows (two 64-key halves)
-      const float base = m == -INFINITY ? 0.f : m;
-      float rs = 0.f;
+      // this P buffer was last read by the P V of tile t - 2
+      if (t > 1) {
+        ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(p_free + pb, ((t - 2) >> 1) & 1, 19));
+        if (!ok) break;
+        tc::tc_fence_after();
+      }
+      // P = 2^(sc * s - m) as bf16, K-major swizzled rows (two 64-key halves)
+      const float nbase = m == -INFINITY ? 0.f : -m;
+      float rs8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         float p[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          p[i] = exp2f(v[ch * 8 + i] - base);
-          rs += p[i];
+          p[i] = ex2_approx(fmaf(v[ch * 8 + i], sc, nbase));
+          rs8[i] += p[i];
         }
         uint4 pk;
         pk.x = pack_bf16(p[0], p[1]);
@@ -306,13 +354,16 @@ __global__ void __launch_bounds__(192, 1)
         pk.z = pack_bf16(p[4], p[5]);
         pk.w = pack_bf16(p[6], p[7]);
         const int half = ch >> 3, c8 = ch & 7;
-        uint8_t* dst = sP + half * C::HALF + (r >> 3) * 1024 + (r & 7) * 128 + ((c8 ^ (r & 7)) << 4);
+        uint8_t* dst = sP + pb * C::PB + half * C::HALF + (r >> 3) * 1024 + (r & 7) * 128 + ((c8 ^ (r & 7)) << 4);
         *reinterpret_cast<uint4*>(dst) = pk;
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rs8[i] += rs8[i + 4];
+      const float rs = (rs8[0] + rs8[1]) + (rs8[2] + rs8[3]);
       l += rs;
       tc::fence_proxy_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full);
+      tc::mbar_arrive(p_full + pb);
     }
     // ---- epilogue: O / l ----
     if (ntiles > 0 && ok) ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(o_full, 0, 20));

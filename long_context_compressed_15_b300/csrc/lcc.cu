@@ -569,8 +569,13 @@ size_t split_ws_bytes(int ns, int64_t rows, int D) {
 unsigned long long g_attn_tc_done = 0;
 
 // Worth the tensor-core kernel: D = 128 and enough 128-row blocks to fill the GPU.
-bool use_attn_tc(int B, int Tq, int H, int D) {
-  return D == 128 && static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 127) / 128) >= num_sms();
+// The tensor-core kernels fold the (positive, finite) scale into the
+// exponent after the row maximum; other scales take the legacy path.
+bool tc_scale_ok(float scale) { return scale > 0.f && scale < 3.0e38f; }
+
+bool use_attn_tc(int B, int Tq, int H, int D, float scale) {
+  return D == 128 && tc_scale_ok(scale) &&
+         static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 127) / 128) >= num_sms();
 }
 
 // src1 (K1/V1, rows kv_rs1 apart, Ncap1 per batch) and optional window src2.
@@ -790,7 +795,7 @@ lcc_status lcc_hca_dense_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   a.n_valid = n_valid; a.m = m;
   a.nsplit = ns; a.rows_total = rowsT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (ns == 1 && use_attn_tc(B, Tq, H, D)) {
+  if (ns == 1 && use_attn_tc(B, Tq, H, D, scale)) {
     AttnTcArgs t{};
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
@@ -831,7 +836,7 @@ lcc_status lcc_swa_attn(const lcc_bf16* q, int B, int Tq, int H, int D, float sc
   a.kv_bs = static_cast<int64_t>(Rcap) * kv_rstride; a.kv_rs = kv_rstride; a.Ncap = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
   a.O = O; a.lse = lse; a.nsplit = 1; a.rows_total = static_cast<int64_t>(B) * Tq * H;
-  if (use_attn_tc(B, Tq, H, D)) {
+  if (use_attn_tc(B, Tq, H, D, scale)) {
     AttnTcArgs t{};
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_WINDOW; t.Ncap1 = Rcap; t.raw_pos0 = raw_pos0; t.W = W;
@@ -964,7 +969,7 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
   a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
   a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
-  if (use_attn_tc(B, Tq, H, D)) {
+  if (use_attn_tc(B, Tq, H, D, scale)) {
     AttnTcArgs t{};
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
@@ -974,7 +979,7 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
                           false);
   }
   const int64_t groups16 = static_cast<int64_t>(B) * Tq * ((H + 15) / 16);
-  if (D == 128 && H <= 128 && !use_wsplit<ATT_RANGE>(groups16, static_cast<int64_t>(Ncap) + W)) {
+  if (D == 128 && H <= 128 && tc_scale_ok(scale) && !use_wsplit<ATT_RANGE>(groups16, static_cast<int64_t>(Ncap) + W)) {
     AttnTcArgs t{};
     t.B = B; t.Tq = Tq; t.H = H; t.scale_log2 = a.scale_log2; t.q_pos0 = q_pos0;
     t.mode1 = ATT_RANGE; t.Ncap1 = Ncap; t.n_valid = n_valid; t.m = m;
