@@ -41,7 +41,19 @@ __device__ __forceinline__ uint32_t warp_kth(const uint32_t (&v)[CAPQ / 32], int
 // Every register array is indexed by compile-time constants (unrolled
 // loops), so it stays in registers.
 template <int CAPQ>
+__device__ __forceinline__ int warp_compact_t(uint32_t* keys, int32_t* ids, int n, int k, uint32_t& T_out);
+
+template <int CAPQ>
 __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* ids, int n, int k, uint32_t* theta) {
+  uint32_t T = 0u;
+  const int r = warp_compact_t<CAPQ>(keys, ids, n, k, T);
+  if (n > k && (threadIdx.x & 31) == 0) *theta = T;
+  return r;
+}
+
+// As warp_compact, with the k-th key returned to every lane (when n > k).
+template <int CAPQ>
+__device__ __forceinline__ int warp_compact_t(uint32_t* keys, int32_t* ids, int n, int k, uint32_t& T_out) {
   constexpr int V = CAPQ / 32;
   const int lane = threadIdx.x & 31;
   if (n <= k) return n;
@@ -92,8 +104,98 @@ __device__ __forceinline__ int warp_compact(uint32_t* keys, int32_t* ids, int n,
     out += __popc(m);
   }
   __syncwarp();
-  if (lane == 0) *theta = T;
+  T_out = T;
   return k;
+}
+
+// Shrink a buffer that is filling up without selecting exactly: one warp
+// histograms its n keys into 256 bins spread linearly over [min, max] of the
+// buffer (a monotone map of the key), finds the highest bin b* such that the
+// bins >= b* hold at least k keys, and keeps exactly the keys in those bins,
+// in buffer (= index) order.  Every key of the buffer's top-k is kept, and
+// the smallest kept key m is a valid threshold for later entries: at least
+// k kept keys are >= m and all have lower indices, so a later entry with
+// key <= m can never enter the top-k.  Returns the new count (>= min(n, k))
+// and sets m_out; falls back to the exact cut when the bins do not separate
+// (many equal keys) and the buffer would stay fuller than `room_left`.
+// hist: 256 words of shared memory private to the warp.
+template <int CAPQ>
+__device__ __forceinline__ int warp_cut(uint32_t* keys, int32_t* ids, int n, int k, int max_keep, uint32_t* hist,
+                                        uint32_t& m_out) {
+  constexpr int V = CAPQ / 32;
+  const int lane = threadIdx.x & 31;
+  uint32_t v[V];
+  int32_t id[V];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < n ? keys[e] : 0u;
+    id[i] = e < n ? ids[e] : 0;
+    if (e < n) { lo = min(lo, v[i]); hi = max(hi, v[i]); }
+  }
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+  __syncwarp();
+  const float inv = 256.f / (static_cast<float>(hi - lo) + 1.f);
+  uint32_t bins[V / 4 > 0 ? V / 4 : 1];  // four 8-bit bin numbers per word
+#pragma unroll
+  for (int i = 0; i < V / 4; ++i) bins[i] = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    const uint32_t bn = min(255u, static_cast<uint32_t>(static_cast<float>(v[i] - lo) * inv));
+    bins[i / 4] |= bn << (8 * (i % 4));
+    if (e < n) atomicAdd(hist + bn, 1u);
+  }
+  __syncwarp();
+  // highest bin b* whose suffix count reaches k (lane L owns bins 8L .. 8L+7)
+  uint32_t h[8], t = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { h[j] = hist[lane * 8 + j]; t += h[j]; }
+  uint32_t above = t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, above, o);
+    if (lane + o < 32) above += y;
+  }
+  uint32_t run = above - t;
+  int bstar = -1;
+  uint32_t keep_n = 0;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (bstar < 0 && run + h[j] >= static_cast<uint32_t>(k)) { bstar = lane * 8 + j; keep_n = run + h[j]; }
+    run += h[j];
+  }
+  int best = __reduce_max_sync(0xffffffffu, bstar);
+  const uint32_t kept = __shfl_sync(0xffffffffu, keep_n, __ffs(__ballot_sync(0xffffffffu, bstar == best)) - 1);
+  __syncwarp();  // everyone has read the histogram before the next use
+  if (best < 0 || static_cast<int>(kept) > max_keep) {
+    uint32_t T = 0u;
+    const int r = warp_compact_t<CAPQ>(keys, ids, n, k, T);
+    m_out = T;
+    return r;
+  }
+  int out = 0;
+  uint32_t mk = 0xFFFFFFFFu;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    const bool keep = e < n && static_cast<int>((bins[i / 4] >> (8 * (i % 4))) & 255u) >= best;
+    const unsigned m = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      const int p = out + __popc(m & ((1u << lane) - 1u));
+      keys[p] = v[i];
+      ids[p] = id[i];
+      mk = min(mk, v[i]);
+    }
+    out += __popc(m);
+  }
+  __syncwarp();
+  m_out = __reduce_min_sync(0xffffffffu, mk);
+  return out;
 }
 
 }  // namespace ftk
@@ -120,7 +222,8 @@ struct IndexTopkTcCfg {
   static constexpr int OFF_KEYS = (Base::OFF_BAR + Base::NBAR * 8 + 64 + 1023) / 1024 * 1024;
   static constexpr int OFF_IDS = OFF_KEYS + NQ * CAPQ * 4;
   static constexpr int OFF_ST = OFF_IDS + NQ * CAPQ * 4;   // theta[NQ], cnt[NQ]
-  static constexpr int SMEM = OFF_ST + NQ * 8 + 1024;
+  static constexpr int OFF_HIST = OFF_ST + NQ * 8;          // 256 words per epilogue warp
+  static constexpr int SMEM = OFF_HIST + 8 * 256 * 4 + 1024;
 };
 
 // Threads: warp 0 TMA, warp 1 TMEM allocation + MMA, warps 2..9 epilogue.
@@ -151,6 +254,7 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
   int32_t* sIds = reinterpret_cast<int32_t*>(smem + X::OFF_IDS);      // [NQ][CAPQ]
   uint32_t* sTheta = reinterpret_cast<uint32_t*>(smem + X::OFF_ST);   // [NQ]
   int* sCnt = reinterpret_cast<int*>(smem + X::OFF_ST + NQ * 4);      // [NQ]
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + X::OFF_HIST);  // [8][256]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z;
@@ -331,9 +435,13 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
         for (int qi = ew; qi < NQ && !*s_abort; qi += 8) {
           const int n = sCnt[qi];
           if (n > X::CAPQ - X::SYNC * C::TILE) {
-            const int nk =
-                ftk::warp_compact<X::CAPQ>(sKeys + qi * X::CAPQ, sIds + qi * X::CAPQ, n, k, sTheta + qi);
-            if (lane == 0) sCnt[qi] = nk;
+            uint32_t th;
+            const int nk = ftk::warp_cut<X::CAPQ>(sKeys + qi * X::CAPQ, sIds + qi * X::CAPQ, n, k,
+                                                  X::CAPQ - X::SYNC * C::TILE, sHist + ew * 256, th);
+            if (lane == 0) {
+              sCnt[qi] = nk;
+              sTheta[qi] = th;
+            }
           }
         }
         tc::named_sync(1, NEPI);
@@ -354,6 +462,293 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
       int32_t* iq = sIds + qi * X::CAPQ;
       n = ftk::warp_compact<X::CAPQ>(kq, iq, n, k, sTheta + qi);
       __syncwarp();
+      int32_t* oi = a.idx + (static_cast<int64_t>(b) * a.Tq + q) * k;
+      float* os = a.score ? a.score + (static_cast<int64_t>(b) * a.Tq + q) * k : nullptr;
+      for (int c = lane; c < k; c += 32) {
+        if (c < n) {
+          const int32_t me = iq[c];
+          int p = 0;
+          for (int d = 0; d < n; ++d) p += iq[d] < me;
+          oi[p] = me;
+          if (os) os[p] = key_to_f32(kq[c]);
+        } else {
+          oi[c] = -1;
+          if (os) os[c] = -INFINITY;
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// Variant with warp-private candidate buffers (16 queries per CTA, k up to
+// CAPB - 32).  Each (query, TMEM lane quadrant) pair has its own buffer,
+// threshold and count, owned by the one epilogue warp that reads that
+// quadrant's accumulator columns of the query: appends need no atomics and
+// compactions no barrier, so the epilogue warps run independently until the
+// end.  A quadrant's buffer holds the top-k of the entries of that quadrant
+// seen so far (its threshold is the k-th of them, a lower bound of the
+// query's k-th); the union of the four buffers therefore contains the
+// query's top-k, which one warp selects exactly at the end.  16 epilogue
+// warps (four per quadrant, four queries each) keep more loads and
+// dependency chains in flight than one warp per SMSP pair.
+template <int HI, int DI, int NQ, int STAGES>
+struct IndexTopkPwCfg {
+  using Base = IndexTcCfg<HI, DI, NQ, STAGES>;
+  static constexpr int EW = 16;                    // epilogue warps
+  static constexpr int NT = 64 + EW * 32;          // + TMA and MMA warps
+  static constexpr int CAPB = 256;                 // slots per (query, quadrant)
+  static constexpr int NB = NQ * 4;                // buffers
+  static constexpr int OFF_KEYS = (Base::OFF_BAR + Base::NBAR * 8 + 64 + 1023) / 1024 * 1024;
+  static constexpr int OFF_IDS = OFF_KEYS + NB * CAPB * 4;
+  static constexpr int OFF_CNT = OFF_IDS + NB * CAPB * 4;   // final count of every buffer
+  static constexpr int OFF_HIST = OFF_CNT + NB * 4;         // 256 words per epilogue warp
+  static constexpr int SMEM = OFF_HIST + EW * 256 * 4 + 1024;
+};
+
+template <int HI, int DI, int NQ, int STAGES>
+__global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
+    k_index_topk_pw(const __grid_constant__ CUtensorMap tmap_k, IndexTopkTcArgs a) {
+  using C = IndexTcCfg<HI, DI, NQ, STAGES>;
+  using X = IndexTopkPwCfg<HI, DI, NQ, STAGES>;
+  constexpr int EW = X::EW;
+  constexpr int NEPI = EW * 32;
+  constexpr int G = EW / 4;              // query groups (epilogue warps per quadrant)
+  constexpr int QG = NQ / G;             // queries per epilogue warp
+  constexpr int COLS = QG * HI;          // accumulator columns per warp
+  constexpr int CAPB = X::CAPB;
+  static_assert(C::NREAL == C::N && COLS % 32 == 0 && NQ % G == 0, "whole 32-column loads");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + C::OFF_A;
+  uint8_t* sB = smem + C::OFF_B;
+  float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
+  int* sVis = reinterpret_cast<int*>(smem + C::OFF_VIS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+  uint32_t* sKeys = reinterpret_cast<uint32_t*>(smem + X::OFF_KEYS);  // [NQ][4][CAPB]
+  int32_t* sIds = reinterpret_cast<int32_t*>(smem + X::OFF_IDS);      // [NQ][4][CAPB]
+  int* sCnt = reinterpret_cast<int*>(smem + X::OFF_CNT);              // [NQ][4]
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + X::OFF_HIST);  // [EW][256]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  // heavy (late) query groups first: they see the most entries
+  const int grp = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+  const int qg0 = grp * NQ;
+  const int qend = min(qg0 + NQ, a.Tq);
+  const int64_t pos0 = __ldg(a.q_pos0 + b);
+  const int nval = __ldg(a.n_valid + b);
+  const int vis_max = visible_entries(pos0 + qend - 1, a.m, nval, a.Ncap);
+  const int vis_min = visible_entries(pos0 + qg0, a.m, nval, a.Ncap);
+  const int ntiles = (vis_max + C::TILE - 1) / C::TILE;
+  const int k = a.k;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { tc::mbar_init(full + i, 1); tc::mbar_init(empty + i, 1); }
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, NEPI); }
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  const int row0 = b * a.Ncap;
+  if (warp == 0 && lane == 0 && ntiles > 0) {
+    tc::tma_prefetch_desc(&tmap_k);
+    for (int t = 0; t < min(STAGES, ntiles); ++t) {
+      tc::mbar_arrive_expect_tx(full + t, C::A_BYTES);
+      tc::tma_load_2d(sA + t * C::A_BYTES, &tmap_k, full + t, 0, row0 + t * C::TILE);
+    }
+  }
+  if (warp == 1) tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+  if (warp >= 2) {
+    const int t = threadIdx.x - 64;
+    constexpr int CPR = DI / 8;
+    for (int u = t; u < C::N * CPR; u += NEPI) {
+      const int n = u / CPR, c = u % CPR;
+      const int qq = qg0 + n / HI, hh = n % HI;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (qq < qend)
+        v = __ldg(reinterpret_cast<const uint4*>(a.qI + ((static_cast<int64_t>(b) * a.Tq + qq) * HI + hh) * DI) + c);
+      const int sw = C::ROWB == 128 ? (c ^ (n & 7)) : (c ^ ((n & 7) >> 1));
+      *reinterpret_cast<uint4*>(sB + (n >> 3) * C::SBO + (n & 7) * C::ROWB + sw * 16) = v;
+    }
+    for (int u = t; u < NQ * HI; u += NEPI) {
+      const int qq = qg0 + u / HI;
+      sW[u] = qq < qend ? __ldg(a.w + (static_cast<int64_t>(b) * a.Tq + qq) * HI + u % HI) : 0.f;
+    }
+    for (int u = t; u < NQ; u += NEPI) {
+      const int qq = qg0 + u;
+      sVis[u] = qq < qend ? visible_entries(pos0 + qq, a.m, nval, a.Ncap) : 0;
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    int issued = min(STAGES, ntiles);
+    if (lane == 0) {
+      for (int t = STAGES; t < ntiles; ++t) {
+        const int s = t % STAGES;
+        if (*s_abort || !tc::mbar_wait(empty + s, ((t / STAGES) & 1) ^ 1, 21)) { *s_abort = 1; break; }
+        tc::mbar_arrive_expect_tx(full + s, C::A_BYTES);
+        tc::tma_load_2d(sA + s * C::A_BYTES, &tmap_k, full + s, 0, row0 + t * C::TILE);
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - STAGES); t < issued; ++t)
+        tc::mbar_wait(full + t % STAGES, (t / STAGES) & 1, 22);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % STAGES, acc = t & 1;
+        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t >> 1) & 1) ^ 1, 23)) { *s_abort = 1; break; }
+        if (*s_abort || !tc::mbar_wait(full + s, (t / STAGES) & 1, 24)) { *s_abort = 1; break; }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + acc * C::N;
+#pragma unroll
+        for (int kk = 0; kk < DI / 16; ++kk) {
+          const uint64_t ad = tc::smem_desc(a_base + s * C::A_BYTES + kk * 32, 16, C::SBO, C::SWZ);
+          const uint64_t bd = tc::smem_desc(b_base + kk * 32, 16, C::SBO, C::SWZ);
+          tc::mma_f16_ss(d, ad, bd, C::IDESC, kk > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(empty + s);
+        tc::mma_commit(tfull + acc);
+        issued = t + 1;
+      }
+      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 25);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue + streaming top-k
+    const int ew = warp - 2;          // epilogue warp 0..EW-1
+    const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
+    const int grpq = ew >> 2;         // queries [grpq*QG, grpq*QG + QG)
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grpq * COLS;
+    const float4* sW4 = reinterpret_cast<const float4*>(sW) + grpq * QG * HI / 4;  // broadcast reads
+    int visr[QG], cnt[QG];
+    float thf[QG];  // threshold test on floats: key(s) > key(theta) <=> s > f(theta); -inf = none yet
+#pragma unroll
+    for (int j = 0; j < QG; ++j) {
+      visr[j] = sVis[grpq * QG + j];
+      thf[j] = -INFINITY;
+      cnt[j] = 0;
+    }
+    auto buf = [&](int j) { return ((grpq * QG + j) * 4 + quarter) * CAPB; };
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t & 1;
+      const bool wok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 26));
+      if (!wok) {
+        *s_abort = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      float v[COLS];
+#pragma unroll
+      for (int c = 0; c < COLS / 32; ++c) {
+        float x[32];
+        tc::tmem_ld32(lane_addr + acc * C::N + c * 32, x);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[c * 32 + i] = x[i];
+      }
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      tc::mbar_arrive(tempty + acc);  // the accumulator is in registers: the next MMA may start
+      const int entry = t * C::TILE + quarter * 32 + lane;
+      const bool all_vis = (t + 1) * C::TILE <= vis_min;  // every query sees the whole tile
+      float sc[QG];
+      bool any = false;
+#pragma unroll
+      for (int j = 0; j < QG; ++j) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h4 = 0; h4 < HI / 4; ++h4) {
+          const float4 wv = sW4[j * HI / 4 + h4];
+          s0 = fmaf(wv.x, fmaxf(v[j * HI + 4 * h4 + 0], 0.f), s0);
+          s1 = fmaf(wv.y, fmaxf(v[j * HI + 4 * h4 + 1], 0.f), s1);
+          s0 = fmaf(wv.z, fmaxf(v[j * HI + 4 * h4 + 2], 0.f), s0);
+          s1 = fmaf(wv.w, fmaxf(v[j * HI + 4 * h4 + 3], 0.f), s1);
+        }
+        const float s = s0 + s1;
+        sc[j] = (all_vis || entry < visr[j]) ? s : -INFINITY;
+        any |= sc[j] > thf[j];
+      }
+      if (__any_sync(0xffffffffu, any)) {  // some entry of this warp passes a threshold
+#pragma unroll
+        for (int j = 0; j < QG; ++j) {
+          const bool take = sc[j] > thf[j];
+          const unsigned msk = __ballot_sync(0xffffffffu, take);
+          if (msk) {  // warp-uniform
+            const int bo = buf(j);
+            if (take) {
+              const int slot = cnt[j] + __popc(msk & ((1u << lane) - 1u));
+              sKeys[bo + slot] = f32_to_key(sc[j]);
+              sIds[bo + slot] = entry;
+            }
+            cnt[j] += __popc(msk);
+            if (cnt[j] > CAPB - 32) {  // the next tile could overflow: cut to a superset of the top-k
+              __syncwarp();
+              uint32_t th;
+              cnt[j] = ftk::warp_cut<CAPB>(sKeys + bo, sIds + bo, cnt[j], k, CAPB - 32, sHist + ew * 256, th);
+              thf[j] = key_to_f32(th);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < QG; ++j) {  // every buffer down to at most k before the merge
+      const int bo = buf(j);
+      __syncwarp();
+      uint32_t T;
+      const int n = *s_abort ? 0 : ftk::warp_compact_t<CAPB>(sKeys + bo, sIds + bo, cnt[j], k, T);
+      if (lane == 0) sCnt[bo / CAPB] = n;
+    }
+    tc::named_sync(1, NEPI);
+    // ---- final: exact top-k of every query over its four buffers, ascending index order ----
+    for (int qi = ew; qi < NQ; qi += EW) {
+      const int q = qg0 + qi;
+      if (q >= qend) continue;
+      uint32_t* kq = sKeys + qi * 4 * CAPB;
+      int32_t* iq = sIds + qi * 4 * CAPB;
+      int n = sCnt[qi * 4];
+      for (int qd = 1; qd < 4; ++qd) {
+        // append list qd behind the running top-k (forward copy: the destination
+        // starts at most k <= CAPB - 32 slots in, below the source), then keep
+        // the top-k of the union
+        const int c = sCnt[qi * 4 + qd];
+        for (int e0 = 0; e0 < c; e0 += 32) {
+          const int e = e0 + lane;
+          uint32_t kv = 0u;
+          int32_t iv = 0;
+          if (e < c) { kv = kq[qd * CAPB + e]; iv = iq[qd * CAPB + e]; }
+          __syncwarp();
+          if (e < c) { kq[n + e] = kv; iq[n + e] = iv; }
+          __syncwarp();
+        }
+        uint32_t T;
+        n = ftk::warp_compact_t<2 * CAPB>(kq, iq, n + c, k, T);
+        __syncwarp();
+      }
+      if (*s_abort) n = 0;
       int32_t* oi = a.idx + (static_cast<int64_t>(b) * a.Tq + q) * k;
       float* os = a.score ? a.score + (static_cast<int64_t>(b) * a.Tq + q) * k : nullptr;
       for (int c = lane; c < k; c += 32) {

@@ -279,6 +279,7 @@ lcc_status launch_index_tc(const IndexArgs& ia, cudaStream_t s) {
 }
 
 unsigned long long g_index_topk_tc_done[2][2] = {};
+unsigned long long g_index_topk_pw_done[2] = {};
 constexpr int kFusedTopkMaxK = 256;
 
 // Prefill: indexer with the streaming top-k in its epilogue (no score buffer).
@@ -287,18 +288,30 @@ lcc_status launch_index_topk_tc(const lcc_bf16* qI, const float* w, int B, int T
                                 const void* kI, const int32_t* n_valid, int Ncap, int m, int k, int32_t* idx,
                                 float* score, cudaStream_t s) {
   constexpr int NQ = 128 / HI, STAGES = 3;
-  using X = IndexTopkTcCfg<HI, DI, NQ, STAGES>;
-  auto kern = k_index_topk_tc<HI, DI, NQ, STAGES>;
   CUtensorMap tm;
   lcc_status st = make_tmap_2d(&tm, kI, DI, static_cast<uint64_t>(B) * Ncap, DI, DI, 128,
                                DI == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, "k_index_topk_tc");
   if (st != LCC_OK) return st;
+  IndexTopkTcArgs a{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, n_valid, Ncap, m, k, idx, score};
+  const int groups = (Tq + NQ - 1) / NQ;
+  if constexpr (NQ == 16) {
+    using P = IndexTopkPwCfg<HI, DI, NQ, STAGES>;
+    if (k <= P::CAPB - 32) {  // warp-private candidate buffers
+      auto kern = k_index_topk_pw<HI, DI, NQ, STAGES>;
+      {
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if ((st = ensure_smem(kern, P::SMEM, g_index_topk_pw_done[DI == 64])) != LCC_OK) return st;
+      }
+      launch_k(kern, dim3(1, groups, B), dim3(P::NT), P::SMEM, s, false, tm, a);
+      return launch_check("k_index_topk_pw");
+    }
+  }
+  using X = IndexTopkTcCfg<HI, DI, NQ, STAGES>;
+  auto kern = k_index_topk_tc<HI, DI, NQ, STAGES>;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if ((st = ensure_smem(kern, X::SMEM, g_index_topk_tc_done[HI == 8][DI == 64])) != LCC_OK) return st;
   }
-  IndexTopkTcArgs a{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, n_valid, Ncap, m, k, idx, score};
-  const int groups = (Tq + NQ - 1) / NQ;
   launch_k(kern, dim3(1, groups, B), dim3(320), X::SMEM, s, false, tm, a);
   return launch_check("k_index_topk_tc");
 }

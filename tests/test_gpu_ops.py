@@ -357,6 +357,15 @@ def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
             assert_close(out[b, i].float().cpu().numpy(), O, f"HCA layer [{b},{i}]")
 
 
+@pytest.mark.parametrize("DI,k", [(64, 200), (32, 128), (64, 240)])
+def test_index_topk_prefill_fused_parity(DI, k):
+    # prefill-shaped calls with 8 indexer heads: k up to 224 uses warp-private candidate buffers per
+    # (query, lane quadrant), larger k the shared per-query buffers; 301 queries leave a ragged
+    # last group, and the visible counts grow along the chunk
+    near, g = _index_case(27, 1, 301, 8, DI, 3000, 4, k, q_pos0=[8000], n_valid=[3000])
+    assert near <= 2
+
+
 def test_index_topk_prefill_fused_zero_score_ties():
     # prefill-shaped calls keep a running top-k inside the indexer; with zero weights every score
     # ties, so each query must keep its lowest visible indices (candidate buffers compact often)
