@@ -471,7 +471,7 @@ class CsaPrefillBench:
     """CSA layer prefill of one 131072-token sequence (pool, indexer + top-k, sparse + window attention)."""
     unit = "tokens/s"
     name = "csa_prefill"
-    dominant = "k_index_topk_tc"
+    dominant = "k_index_topk_pw"
     bound = "tensor"
     graph_steps = 1
 
