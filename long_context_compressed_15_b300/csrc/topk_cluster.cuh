@@ -31,45 +31,6 @@
 
 namespace lcc {
 
-namespace clu {
-__device__ __forceinline__ uint32_t rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t size() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-__device__ __forceinline__ void sync() {
-  arrive();
-  wait();
-}
-// Address of the shared variable `p` of CTA `r` of this cluster.
-__device__ __forceinline__ uint32_t map(const void* p, uint32_t r) {
-  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(p));
-  uint32_t d;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(r));
-  return d;
-}
-__device__ __forceinline__ void st(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-__device__ __forceinline__ uint32_t ld(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t atom_add(uint32_t addr, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-  return old;
-}
-}  // namespace clu
-
 // k-th largest of vals[0..n) (1 <= k <= n), returned to every thread of
 // the CTA (every thread calls this).  Each round histograms the values in
 // the current interval [lo, hi] into 256 bins of width w = ceil((hi-lo+1)/256),

@@ -188,6 +188,27 @@ def test_sparse_attn_parity(H, D, k):
             assert_lse_close(lse[b, i].cpu().numpy(), Lo, f"lse[{b},{i}]")
 
 
+def test_sparse_attn_gather_many_queries_parity():
+    # 300 queries of 128 heads, 130 selected entries each (a ragged last key tile), lists with -1
+    # padding and one-entry lists
+    B, Tq, H, D, Ncap, k = 2, 150, 128, 128, 500, 130
+    q = datagen.normal_bf16(38, 4, (B, Tq, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(38, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(38, 9, (B, Ncap, D))
+    vis = torch.tensor(([Ncap, 3, k, 200, 129, 1] * (B * Tq))[: B * Tq])
+    idx = datagen.random_index_lists(38, 17, vis, k).reshape(B, Tq, k)
+    O, lse = lcc.csa_sparse_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV), idx.to(DEV))
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    for b in range(B):
+        for i in range(Tq):
+            sel = idx[b, i].numpy()
+            sel = sel[sel >= 0]
+            Oo, Lo = oracle.attend(f64(q[b, i]), f64(Kc[b])[sel], f64(Vc[b])[sel])
+            assert_close(O[b, i].cpu().numpy(), Oo, f"O[{b},{i}]")
+            assert_lse_close(lse[b, i].cpu().numpy(), Lo, f"lse[{b},{i}]")
+
+
 def test_sparse_attn_rejects_out_of_range_index():
     B, Tq, H, D, Ncap, k = 1, 1, 64, 128, 50, 8
     q = torch.zeros((B, Tq, H, D), dtype=torch.bfloat16, device=DEV)
@@ -325,6 +346,33 @@ def test_csa_layer_attn_parity(B, Tq, H, D, k, W, Ncap):
             O, L = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
             assert_close(out[b, i].float().cpu().numpy(), O, f"CSA layer [{b},{i}]")
             assert_lse_close(lse[b, i].cpu().numpy(), L, f"CSA layer lse [{b},{i}]")
+
+
+def test_csa_layer_attn_prefill_parity():
+    # a prefill-shaped CSA layer: 301 consecutive queries of 64 heads, 200 selected entries each
+    # (empty, short and full lists) plus the 128-token window of every query
+    B, Tq, H, D, k, W, Ncap = 1, 301, 64, 128, 200, 128, 2000
+    R = Tq + W - 1
+    q = datagen.normal_bf16(39, 4, (B, Tq, H, D), scale=D ** -0.5)
+    Kc = datagen.normal_bf16(39, 8, (B, Ncap, D))
+    Vc = datagen.normal_bf16(39, 9, (B, Ncap, D))
+    Kr = datagen.normal_bf16(39, 1, (B, R, D))
+    Vr = datagen.normal_bf16(39, 2, (B, R, D))
+    vis = torch.tensor(([Ncap, 3, 0, k, 1500, 129] * (B * Tq))[: B * Tq])
+    idx = datagen.random_index_lists(39, 17, vis, k).reshape(B, Tq, k)
+    raw0, qpos = 10000, 10000 + W - 1
+    lse = torch.empty((B, Tq, H), dtype=torch.float32, device=DEV)
+    out = lcc.csa_layer_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV), idx.to(DEV), Kr.to(DEV), Vr.to(DEV),
+                             torch.tensor([qpos], device=DEV), torch.tensor([raw0], device=DEV), W, lse_out=lse)
+    lcc.sync_status()
+    for i in range(Tq):
+        sel = idx[0, i].numpy()
+        sel = sel[sel >= 0]
+        cO, cL = oracle.attend(f64(q[0, i]), f64(Kc[0])[sel], f64(Vc[0])[sel])
+        sw = runs.swa_branch(f64(q[0, i]), qpos + i, f64(Kr[0]), f64(Vr[0]), raw0, W)
+        O, L = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
+        assert_close(out[0, i].float().cpu().numpy(), O, f"CSA layer [{i}]")
+        assert_lse_close(lse[0, i].cpu().numpy(), L, f"CSA layer lse [{i}]")
 
 
 # warp-split kernel for the short lists; 3000 entries take the split-across-CTAs path; 2000 prefill
