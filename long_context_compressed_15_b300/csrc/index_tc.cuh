@@ -78,6 +78,9 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NBAR);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
+  // launched as a programmatic dependent of whatever ran before on the
+  // stream: nothing is read before that grid has completed
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z;
   const int qg0 = a.q0 + blockIdx.y * NQ;                   // first query of this CTA

@@ -264,7 +264,9 @@ lcc_status launch_index_tc_q(const IndexArgs& ia, const CUtensorMap& tm, int bit
   a.tiles_per_split = (tiles + nsplit - 1) / nsplit;
   nsplit = (tiles + a.tiles_per_split - 1) / a.tiles_per_split;
   if (ngroups > 65535) return fail(LCC_ERR_SHAPE, "k_index_tc: %d query groups", ngroups);
-  kern<<<dim3(nsplit, ngroups, ia.B), 192, C::SMEM, s>>>(tm, a);
+  // programmatic dependent launch: the CTAs become resident while the previous
+  // kernel on the stream drains and wait for it in griddepcontrol.wait
+  launch_k(kern, dim3(nsplit, ngroups, ia.B), dim3(192), C::SMEM, s, true, tm, a);
   return launch_check("k_index_tc");
 }
 

@@ -1,0 +1,85 @@
+"""Small, fixed cases of single library calls, sized for a profiler capture.
+
+    python -m long_context_compressed_15_b300.profile_cases <case> [--queries Q]
+
+Each case builds its inputs with the seeded workload generators (``datagen``),
+runs the call twice (the second run is the one to capture after the first
+has warmed the library up) and synchronises.  The inputs are larger than
+the 126 MB L2 where the case streams memory, and a few hundred MB at most
+are held on the device, so a multi-pass capture (``ncu --set full``) of one
+launch finishes in seconds:
+
+    index-topk-prefill   the last Q queries (default 4096) of the 131072-token
+                         CSA prefill: indexer with the fused top-k
+    hca-prefill-attn     the first Q queries (default 4096) of the HCA prefill
+                         chunk: dense compressed entries + window, one softmax
+    csa-decode-index     the CSA decode batch (32 x 16384 entries): indexer
+                         scores only
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import datagen  # noqa: E402
+from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, T_KI, T_QI, T_W  # noqa: E402
+
+from . import hca_layer_attn, lightning_index_scores, lightning_index_topk, load  # noqa: E402
+
+
+def index_topk_prefill(dev, nq):
+    c = CsaPrefill()
+    q0 = c.T - nq
+    qI = datagen.normal_bf16(c.seed, T_QI, (1, nq, c.HI, c.DI), device=dev)
+    w = datagen.uniform_f32(c.seed, T_W, (1, nq, c.HI), device=dev)
+    kI = datagen.normal_bf16(c.seed, T_KI, (1, c.N, c.DI), device=dev)
+    idx = torch.empty((1, nq, c.k), dtype=torch.int32, device=dev)
+    return lambda: lightning_index_topk(qI, w, q0, kI, c.N, c.m, c.k, idx=idx)
+
+
+def hca_prefill_attn(dev, nq):
+    c = HcaPrefill()
+    g = c.make(dev, with_q=False)
+    q = datagen.normal_bf16(c.seed + 101, 4, (1, nq, c.H, c.D), c.q_scale, device=dev)
+    out = torch.empty((1, nq, c.H, c.D), dtype=torch.bfloat16, device=dev)
+    return lambda: hca_layer_attn(q, g["Kc"], g["Vc"], c.Ncap, c.m, g["Kr"], g["Vr"], c.q_pos0, c.raw_pos0, c.W,
+                                  out=out)
+
+
+def csa_decode_index(dev, nq):
+    c = CsaDecode()
+    s = c.make(dev)
+    pos = torch.full((c.B,), c.q_pos, dtype=torch.int64, device=dev)
+    nval = torch.full((c.B,), c.N, dtype=torch.int32, device=dev)
+    scores = torch.empty((c.B, 1, c.N), dtype=torch.float32, device=dev)
+    return lambda: lightning_index_scores(s["qI"], s["w"], pos, s["kI"], nval, 4, scores=scores)
+
+
+CASES = {"index-topk-prefill": index_topk_prefill, "hca-prefill-attn": hca_prefill_attn,
+         "csa-decode-index": csa_decode_index}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--queries", type=int, default=4096)
+    args = ap.parse_args(argv)
+    load()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    run = CASES[args.case](dev, args.queries)
+    for _ in range(2):
+        run()
+    torch.cuda.synchronize()
+    print(f"{args.case}: ok")
+
+
+if __name__ == "__main__":
+    main()

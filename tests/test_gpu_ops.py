@@ -377,9 +377,10 @@ def test_csa_layer_attn_prefill_parity():
 
 # warp-split kernel for the short lists; 3000 entries take the split-across-CTAs path; 2000 prefill
 # queries fill enough CTAs for the single-pass kernel that writes bf16 directly
+# 8 decode sequences of 2000 entries + window (ragged visible counts): the tensor-core split-KV path
 @pytest.mark.parametrize("B,Tq,H,D,m,W,Ncap", [(3, 1, 64, 128, 128, 128, 700), (1, 300, 8, 64, 4, 32, 700),
                                                (2, 9, 64, 128, 4, 128, 700), (3, 1, 64, 128, 128, 128, 3000),
-                                               (1, 2000, 64, 128, 4, 128, 600)])
+                                               (1, 2000, 64, 128, 4, 128, 600), (8, 1, 64, 128, 128, 128, 2000)])
 def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
     R = 300 if Tq < 300 else Tq
     q = datagen.normal_bf16(37, 4, (B, Tq, H, D), scale=D ** -0.5)
@@ -387,13 +388,14 @@ def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
     Vc = datagen.normal_bf16(37, 9, (B, Ncap, D))
     Kr = datagen.normal_bf16(37, 1, (B, R, D))
     Vr = datagen.normal_bf16(37, 2, (B, R, D))
-    n_valid = [Ncap, 37, 0][:B] if Tq == 1 else [Ncap] * B
+    n_valid = ([Ncap, 37, 0] * B)[:B] if Tq == 1 else [Ncap] * B
     # decode: queries far into the context; prefill: the raw buffer starts at 0 and queries at 0
     qpos = [m * Ncap + 5] * B if Tq == 1 else [0] * B
     raw0 = [qpos[b] + Tq - R + 3 for b in range(B)] if Tq == 1 else [0] * B
+    lse = torch.empty((B, Tq, H), dtype=torch.float32, device=DEV)
     out = lcc.hca_layer_attn(q.to(DEV), Kc.to(DEV), Vc.to(DEV),
                              torch.tensor(n_valid, dtype=torch.int32, device=DEV), m, Kr.to(DEV), Vr.to(DEV),
-                             torch.tensor(qpos, device=DEV), torch.tensor(raw0, device=DEV), W)
+                             torch.tensor(qpos, device=DEV), torch.tensor(raw0, device=DEV), W, lse_out=lse)
     lcc.sync_status()
     rows = range(Tq) if Tq <= 300 else sorted(set(range(0, Tq, 7)) | {Tq - 1})
     for b in range(B):
@@ -401,8 +403,9 @@ def test_hca_layer_attn_parity(B, Tq, H, D, m, W, Ncap):
             t = qpos[b] + i
             h = runs.hca_branch(f64(q[b, i]), t, f64(Kc[b]), f64(Vc[b]), m, n_valid=n_valid[b])
             sw = runs.swa_branch(f64(q[b, i]), t, f64(Kr[b]), f64(Vr[b]), raw0[b], W)
-            O, _ = oracle.merge([h["O"], sw["O"]], [h["lse"], sw["lse"]])
+            O, L = oracle.merge([h["O"], sw["O"]], [h["lse"], sw["lse"]])
             assert_close(out[b, i].float().cpu().numpy(), O, f"HCA layer [{b},{i}]")
+            assert_lse_close(lse[b, i].cpu().numpy(), L, f"HCA layer lse [{b},{i}]")
 
 
 @pytest.mark.parametrize("DI,k", [(64, 200), (32, 128), (64, 240)])
