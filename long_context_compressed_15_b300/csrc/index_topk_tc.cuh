@@ -675,7 +675,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       const int entry = t * C::TILE + quarter * 32 + lane;
       const bool all_vis = (t + 1) * C::TILE <= vis_min;  // every query sees the whole tile
       float sc[QG];
-      bool any = false;
+      unsigned anyq = 0u;  // bit j: this lane's entry passes query j's threshold
 #pragma unroll
       for (int j = 0; j < QG; ++j) {
         float s0 = 0.f, s1 = 0.f;
@@ -689,14 +689,16 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
         }
         const float s = s0 + s1;
         sc[j] = (all_vis || entry < visr[j]) ? s : -INFINITY;
-        any |= sc[j] > thf[j];
+        anyq |= (sc[j] > thf[j] ? 1u : 0u) << j;
       }
-      if (__any_sync(0xffffffffu, any)) {  // some entry of this warp passes a threshold
+      const unsigned wq = __reduce_or_sync(0xffffffffu, anyq);  // queries with a taker in this warp
+      if (wq) {
 #pragma unroll
         for (int j = 0; j < QG; ++j) {
-          const bool take = sc[j] > thf[j];
+          if (!((wq >> j) & 1u)) continue;  // warp-uniform
+          const bool take = (anyq >> j) & 1u;
           const unsigned msk = __ballot_sync(0xffffffffu, take);
-          if (msk) {  // warp-uniform
+          {
             const int bo = buf(j);
             if (take) {
               const int slot = cnt[j] + __popc(msk & ((1u << lane) - 1u));

@@ -676,8 +676,8 @@ lcc_status tc_decode_attn(AttnTcArgs t, int D, int64_t keys, const bf16* q, cons
 }
 
 unsigned long long g_wsplit_done[2][2] = {};
-constexpr int kWsplitWarps = 16;
-constexpr int kWsplitTile = 16;   // keys per warp tile
+constexpr int kWsplitWarps = 8;
+constexpr int kWsplitTile = 32;   // keys per warp tile
 
 // Short key lists with few (query, 16-head) groups: warps of one CTA split
 // the key tiles and combine in shared memory (no workspace, one launch).

@@ -3,11 +3,10 @@
     python -m long_context_compressed_15_b300.profile_cases <case> [--queries Q]
 
 Each case builds its inputs with the seeded workload generators (``datagen``),
-runs the call twice (the second run is the one to capture after the first
-has warmed the library up) and synchronises.  The inputs are larger than
-the 126 MB L2 where the case streams memory, and a few hundred MB at most
-are held on the device, so a multi-pass capture (``ncu --set full``) of one
-launch finishes in seconds:
+runs the call twice and synchronises (capture the first launch: ncu flushes
+the caches before each replay pass, so its DRAM figures are cold-cache
+reads).  A few hundred MB at most are held on the device, so a multi-pass
+capture (``ncu --set full``) of one launch finishes in seconds:
 
     index-topk-prefill   the last Q queries (default 4096) of the 131072-token
                          CSA prefill: indexer with the fused top-k
