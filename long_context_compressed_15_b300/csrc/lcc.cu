@@ -16,6 +16,7 @@
 #include "merge.cuh"
 #include "attn.cuh"
 #include "attn_tc.cuh"
+#include "attn_gather_tc.cuh"
 #include "index.cuh"
 #include "index_tc.cuh"
 #include "index_topk_tc.cuh"
@@ -593,6 +594,55 @@ bool use_attn_tc(int B, int Tq, int H, int D, float scale) {
          static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 127) / 128) >= num_sms();
 }
 
+// CSA sparse attention (+ window) on the tensor cores: H = 64 or 128 (whole
+// queries per 128-row item), enough items for every SM, 32-bit row numbers.
+unsigned long long g_attn_gather_done = 0;
+
+bool use_gather_tc(int B, int Tq, int H, int D, float scale, int Ncap, int Rcap) {
+  const int64_t items = static_cast<int64_t>(B) * ((static_cast<int64_t>(Tq) * H + 127) / 128);
+  return D == 128 && (H == 64 || H == 128) && tc_scale_ok(scale) && Ncap > 0 && items >= num_sms() &&
+         items <= 0x7FFFFFFF && static_cast<int64_t>(B) * Ncap < (int64_t(1) << 31) &&
+         static_cast<int64_t>(B) * Rcap < (int64_t(1) << 31) &&
+         static_cast<int64_t>(B) * Tq * H < (int64_t(1) << 31);
+}
+
+lcc_status launch_attn_gather_tc(AttnGatherArgs a, const bf16* q, const bf16* Kc, const bf16* Vc, int64_t kv_rs,
+                                 const bf16* Kr, const bf16* Vr, int64_t r_rs, cudaStream_t s, bool pdl) {
+  using Cf = AttnGatherCfg;
+  constexpr int D = Cf::D;
+  CUtensorMap tq, tk, tv, tkw, tvw;
+  const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Tq * a.H;
+  lcc_status st = make_tmap_2d(&tq, q, D, qrows, D, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_gather_tc q");
+  if (st != LCC_OK) return st;
+  const uint64_t r1 = static_cast<uint64_t>(a.B) * a.Ncap;
+  // gathered rows: one-row boxes (tile::gather4 fetches four rows per copy)
+  if ((st = make_tmap_2d(&tk, Kc, D, r1, kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_gather_tc K")) != LCC_OK)
+    return st;
+  if ((st = make_tmap_2d(&tv, Vc, D, r1, kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_gather_tc V")) != LCC_OK)
+    return st;
+  if (a.win) {
+    const uint64_t r2 = static_cast<uint64_t>(a.B) * (a.Rcap > 0 ? a.Rcap : 1);
+    if ((st = make_tmap_2d(&tkw, Kr, D, r2, r_rs, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_gather_tc Kw")) !=
+        LCC_OK)
+      return st;
+    if ((st = make_tmap_2d(&tvw, Vr, D, r2, r_rs, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_gather_tc Vw")) !=
+        LCC_OK)
+      return st;
+  } else {
+    tkw = tk;
+    tvw = tv;
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(k_attn_gather_tc, Cf::SMEM, g_attn_gather_done)) != LCC_OK) return st;
+  }
+  a.tiles_q = static_cast<int>((static_cast<int64_t>(a.Tq) * a.H + 127) / 128);
+  const int64_t items = static_cast<int64_t>(a.B) * a.tiles_q;
+  const unsigned grid = static_cast<unsigned>(items < num_sms() ? items : num_sms());
+  launch_k(k_attn_gather_tc, dim3(grid), dim3(192), Cf::SMEM, s, pdl, tq, tk, tv, tkw, tvw, a);
+  return launch_check("k_attn_gather_tc");
+}
+
 // src1 (K1/V1, rows kv_rs1 apart, Ncap1 per batch) and optional window src2.
 lcc_status launch_attn_tc(AttnTcArgs a, const bf16* q, const bf16* K1, const bf16* V1, int64_t kv_rs1,
                           const bf16* K2, const bf16* V2, int64_t kv_rs2, int nsplit, cudaStream_t s, bool pdl) {
@@ -768,6 +818,14 @@ lcc_status lcc_csa_sparse_attn(const lcc_bf16* q, int B, int Tq, int H, int D, f
   a.kv_bs = static_cast<int64_t>(Ncap) * kv_rstride; a.kv_rs = kv_rstride; a.Ncap = Ncap;
   a.idx = idx; a.k = k;
   a.O = O; a.lse = lse; a.nsplit = 1; a.rows_total = static_cast<int64_t>(B) * Tq * H;
+  if (use_gather_tc(B, Tq, H, D, scale, Ncap, 0)) {
+    AttnGatherArgs g{};
+    g.B = B; g.Tq = Tq; g.H = H; g.scale_log2 = a.scale_log2;
+    g.idx = idx; g.k = k; g.Ncap = Ncap; g.win = 0;
+    g.O = O; g.lse = lse;
+    return launch_attn_gather_tc(g, a.q, a.K, a.V, kv_rstride, nullptr, nullptr, 0,
+                                 static_cast<cudaStream_t>(stream), false);
+  }
   const int rows = H <= 16 ? 16 : 64;
   const int hblocks = (H + rows - 1) / rows;
   if (static_cast<int64_t>(Tq) * hblocks > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many queries", name);
@@ -904,6 +962,15 @@ lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int T
   a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
   a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
+  if (use_gather_tc(B, Tq, H, D, scale, Ncap, Rcap)) {
+    AttnGatherArgs g{};
+    g.B = B; g.Tq = Tq; g.H = H; g.scale_log2 = a.scale_log2; g.q_pos0 = q_pos0;
+    g.idx = idx; g.k = k; g.Ncap = Ncap;
+    g.win = 1; g.Rcap = Rcap; g.raw_pos0 = raw_pos0; g.W = W;
+    g.out_bf16 = reinterpret_cast<bf16*>(out); g.lse = lse_out;
+    return launch_attn_gather_tc(g, a.q, a.K, a.V, kv_rstride, a.K2, a.V2, r_rstride,
+                                 static_cast<cudaStream_t>(stream), pdl);
+  }
   const int rows = H <= 16 ? 16 : 64;
   const int hblocks = (H + rows - 1) / rows;
   if (static_cast<int64_t>(Tq) * hblocks > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many queries", name);

@@ -14,6 +14,9 @@ capture (``ncu --set full``) of one launch finishes in seconds:
                          chunk: dense compressed entries + window, one softmax
     csa-decode-index     the CSA decode batch (32 x 16384 entries): indexer
                          scores only
+    csa-prefill-attn     the first Q queries (default 4096) of the CSA prefill
+                         at the end of the 131072-token sequence: 128 selected
+                         entries per query + the window, one softmax
 """
 from __future__ import annotations
 
@@ -30,7 +33,7 @@ if ROOT not in sys.path:
 import datagen  # noqa: E402
 from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, T_KI, T_QI, T_W  # noqa: E402
 
-from . import hca_layer_attn, lightning_index_scores, lightning_index_topk, load  # noqa: E402
+from . import csa_layer_attn, hca_layer_attn, lightning_index_scores, lightning_index_topk, load  # noqa: E402
 
 
 def index_topk_prefill(dev, nq):
@@ -61,8 +64,26 @@ def csa_decode_index(dev, nq):
     return lambda: lightning_index_scores(s["qI"], s["w"], pos, s["kI"], nval, 4, scores=scores)
 
 
+def csa_prefill_attn(dev, nq):
+    c = CsaPrefill()
+    t0 = c.T - nq  # the last nq queries of the sequence: every list holds k entries
+    q = datagen.normal_bf16(c.seed, 4, (1, nq, c.H, c.D), c.q_scale, device=dev)
+    Kc = datagen.normal_bf16(c.seed, 8, (1, c.N, c.D), device=dev)
+    Vc = datagen.normal_bf16(c.seed, 9, (1, c.N, c.D), device=dev)
+    R = nq + c.W - 1
+    Kr = datagen.normal_bf16(c.seed, 10, (1, R, c.D), device=dev)
+    Vr = datagen.normal_bf16(c.seed, 11, (1, R, c.D), device=dev)
+    # k distinct entries per query spread over the cache: one per stride, at a per-query offset
+    stride = c.N // c.k
+    off = (torch.arange(nq, device=dev, dtype=torch.int64) * 2654435761) % stride
+    idx = (torch.arange(c.k, device=dev, dtype=torch.int64)[None, :] * stride + off[:, None])
+    idx = idx.to(torch.int32).reshape(1, nq, c.k)
+    out = torch.empty((1, nq, c.H, c.D), dtype=torch.bfloat16, device=dev)
+    return lambda: csa_layer_attn(q, Kc, Vc, idx, Kr, Vr, t0, t0 - (c.W - 1), c.W, out=out)
+
+
 CASES = {"index-topk-prefill": index_topk_prefill, "hca-prefill-attn": hca_prefill_attn,
-         "csa-decode-index": csa_decode_index}
+         "csa-decode-index": csa_decode_index, "csa-prefill-attn": csa_prefill_attn}
 
 
 def main(argv=None):
