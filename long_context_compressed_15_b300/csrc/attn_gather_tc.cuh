@@ -12,9 +12,11 @@
 // rows of query B are masked, as are slots marked -1) followed by the window
 // tiles (plain TMA tiles of raw rows, shared by the item's queries).
 // Roles (192 threads):
-//   warp 4 (producer)  Q of each item into one of two buffers; K tiles into a
-//                      two-stage ring, V tiles into one stage, V one tile
-//                      behind K;
+//   warp 4 (producer)  Q of each item (one buffer, reloaded once the item's
+//                      last Q K^T has run); K and V tiles into two-stage
+//                      rings, V one tile behind K (a gathered tile takes
+//                      several times as long to land as a window tile, so
+//                      neither ring may serialise on it);
 //   warp 5 (MMA)       S[g] = Q K[g]^T into one of two TMEM buffers, then
 //                      O += P[g-1] V[g-1] into the TMEM accumulator of the
 //                      item of tile g-1 (two accumulators: the epilogue of
@@ -65,9 +67,9 @@ struct AttnGatherCfg {
   static constexpr int D = 128;
   static constexpr int HALF = 128 * 64 * 2;   // one 64-column swizzled half: 16 KB
   static constexpr int OP = 2 * HALF;         // 128 rows x 128 columns bf16
-  static constexpr int OFF_Q = 0;             // two buffers
-  static constexpr int OFF_K = 2 * OP;        // two stages
-  static constexpr int OFF_V = 4 * OP;        // one stage
+  static constexpr int OFF_Q = 0;             // one buffer
+  static constexpr int OFF_K = 1 * OP;        // two stages
+  static constexpr int OFF_V = 3 * OP;        // two stages
   static constexpr int OFF_P = 5 * OP;        // two buffers
   static constexpr int OFF_BAR = 7 * OP;
   static constexpr int NBAR = 23;
@@ -121,12 +123,13 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars;        // [2]
-  uint64_t* q_empty = bars + 2;   // [2]
-  uint64_t* k_full = bars + 4;    // [2]
-  uint64_t* k_empty = bars + 6;   // [2]
-  uint64_t* v_full = bars + 8;    // [1]
-  uint64_t* v_empty = bars + 9;   // [1]
+  uint64_t* q_full = bars;        // [1]
+  uint64_t* q_empty = bars + 1;   // [1]
+  uint64_t* k_full = bars + 2;    // [2]
+  uint64_t* k_empty = bars + 4;   // [2]
+  uint64_t* v_full = bars + 6;    // [2]
+  uint64_t* v_empty = bars + 8;   // [2]
+  // bars + 10 .. : S, P, O and the final MMA barrier
   uint64_t* s_full = bars + 10;   // [2]
   uint64_t* s_free = bars + 12;   // [2]
   uint64_t* p_full = bars + 14;   // [2]
@@ -143,11 +146,13 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
+    tc::mbar_init(q_full, 1);
+    tc::mbar_init(q_empty, 1);
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(q_full + i, 1);
-      tc::mbar_init(q_empty + i, 1);
       tc::mbar_init(k_full + i, 32);  // one arrival per producer lane
       tc::mbar_init(k_empty + i, 1);
+      tc::mbar_init(v_full + i, 32);
+      tc::mbar_init(v_empty + i, 1);
       tc::mbar_init(s_full + i, 1);
       tc::mbar_init(s_free + i, 128);
       tc::mbar_init(p_full + i, 128);
@@ -155,8 +160,6 @@ __global__ void __launch_bounds__(192, 1)
       tc::mbar_init(o_full + i, 1);
       tc::mbar_init(o_free + i, 128);
     }
-    tc::mbar_init(v_full, 32);
-    tc::mbar_init(v_empty, 1);
     tc::mbar_init(mma_done, 1);
     *s_abort = 0;
     tc::fence_barrier_init();
@@ -233,12 +236,11 @@ __global__ void __launch_bounds__(192, 1)
     bool have_prev = false, pok = true;
     for (int it = blockIdx.x; pok && it < nitems; it += gridDim.x, ++il) {
       const GItem gi = gather_item(a, it);
-      const int qb = il & 1;
-      if (!wait0(q_empty + qb, ((il >> 1) & 1) ^ 1, 31)) { pok = false; break; }
+      if (!wait0(q_empty, (il & 1) ^ 1, 31)) { pok = false; break; }
       if (lane == 0) {
-        tc::mbar_arrive_expect_tx(q_full + qb, C::OP);
+        tc::mbar_arrive_expect_tx(q_full, C::OP);
         const int qy = static_cast<int>(static_cast<int64_t>(gi.b) * rows_b + gi.row0);
-        for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(sQ + qb * C::OP + h * C::HALF, &tmQ, q_full + qb, h * 64, qy);
+        for (int h = 0; h < D / 64; ++h) tc::tma_load_2d(sQ + h * C::HALF, &tmQ, q_full, h * 64, qy);
       }
       const int T = gi.T1 + gi.T2;
       for (int t = 0; t < T; ++t) {
@@ -248,8 +250,8 @@ __global__ void __launch_bounds__(192, 1)
         load(cur, false, sK + s * C::OP, k_full + s);
         ++nk;
         if (have_prev) {  // V one tile behind K
-          if (!wait0(v_empty, (nv & 1) ^ 1, 33)) { pok = false; break; }
-          load(prev, true, sV, v_full);
+          if (!wait0(v_empty + (nv & 1), ((nv >> 1) & 1) ^ 1, 33)) { pok = false; break; }
+          load(prev, true, sV + (nv & 1) * C::OP, v_full + (nv & 1));
           ++nv;
         }
         prev = cur;
@@ -257,8 +259,8 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     if (pok && have_prev) {  // V of the last tile
-      if (wait0(v_empty, (nv & 1) ^ 1, 33)) {
-        load(prev, true, sV, v_full);
+      if (wait0(v_empty + (nv & 1), ((nv >> 1) & 1) ^ 1, 33)) {
+        load(prev, true, sV + (nv & 1) * C::OP, v_full + (nv & 1));
         ++nv;
       } else {
         pok = false;
@@ -267,9 +269,9 @@ __global__ void __launch_bounds__(192, 1)
     if (!pok && lane == 0) *s_abort = 1;
     // every copy this CTA started has landed before it may exit
     if (lane == 0) {
-      for (uint32_t i = il > 2 ? il - 2 : 0; i < il; ++i) tc::mbar_wait(q_full + (i & 1), (i >> 1) & 1, 34);
+      if (il > 0) tc::mbar_wait(q_full, (il - 1) & 1, 34);
       for (uint32_t i = nk > 2 ? nk - 2 : 0; i < nk; ++i) tc::mbar_wait(k_full + (i & 1), (i >> 1) & 1, 34);
-      if (nv > 0) tc::mbar_wait(v_full, (nv - 1) & 1, 34);
+      for (uint32_t i = nv > 2 ? nv - 2 : 0; i < nv; ++i) tc::mbar_wait(v_full + (i & 1), (i >> 1) & 1, 34);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -283,7 +285,8 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = true;
       auto issue_pv = [&](const PvRef& p) {
         const int pb = p.g & 1, ob = p.il & 1;
-        if (*s_abort || !tc::mbar_wait(p_full + pb, (p.g >> 1) & 1, 41) || !tc::mbar_wait(v_full, p.g & 1, 42)) {
+        if (*s_abort || !tc::mbar_wait(p_full + pb, (p.g >> 1) & 1, 41) ||
+            !tc::mbar_wait(v_full + (p.g & 1), (p.g >> 1) & 1, 42)) {
           ok = false;
           return;
         }
@@ -298,11 +301,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int kk = 0; kk < 8; ++kk) {  // 128 keys in steps of 16
           const uint32_t poff = (kk >> 2) * C::HALF + (kk & 3) * 32;
           tc::mma_f16_ss(tmem_o, tc::smem_desc(pa + pb * C::OP + poff, 16, 1024, tc::SW_128B),
-                         tc::smem_desc(va + kk * 2048, C::HALF, 1024, tc::SW_128B), C::IDESC_O,
+                         tc::smem_desc(va + (p.g & 1) * C::OP + kk * 2048, C::HALF, 1024, tc::SW_128B), C::IDESC_O,
                          (!p.first || kk > 0) ? 1u : 0u);
         }
         tc::mma_commit(p_free + pb);
-        tc::mma_commit(v_empty);
+        tc::mma_commit(v_empty + (p.g & 1));
         if (p.last) tc::mma_commit(o_full + ob);
       };
       uint32_t g = 0, il = 0;
@@ -310,9 +313,8 @@ __global__ void __launch_bounds__(192, 1)
       bool have_prev = false;
       for (int it = blockIdx.x; ok && it < nitems; it += gridDim.x, ++il) {
         const GItem gi = gather_item(a, it);
-        const int qb = il & 1;
         const int T = gi.T1 + gi.T2;
-        if (*s_abort || !tc::mbar_wait(q_full + qb, (il >> 1) & 1, 44)) { ok = false; break; }
+        if (*s_abort || !tc::mbar_wait(q_full, il & 1, 44)) { ok = false; break; }
         for (int t = 0; ok && t < T; ++t, ++g) {
           const int s = g & 1, sb = g & 1;
           if (*s_abort || !tc::mbar_wait(k_full + s, (g >> 1) & 1, 45) ||
@@ -321,12 +323,12 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * C::HALF + (kk & 3) * 32;
-            tc::mma_f16_ss(tmem + sb * 128, tc::smem_desc(qa + qb * C::OP + off, 16, 1024, tc::SW_128B),
+            tc::mma_f16_ss(tmem + sb * 128, tc::smem_desc(qa + off, 16, 1024, tc::SW_128B),
                            tc::smem_desc(ka + s * C::OP + off, 16, 1024, tc::SW_128B), C::IDESC_S, kk > 0);
           }
           tc::mma_commit(s_full + sb);
           tc::mma_commit(k_empty + s);
-          if (t == T - 1) tc::mma_commit(q_empty + qb);
+          if (t == T - 1) tc::mma_commit(q_empty);  // the next item's Q may be loaded
           if (have_prev) issue_pv(prev);  // P V of the previous tile (possibly of the previous item)
           prev = PvRef{g, il, t == 0, t == T - 1};
           have_prev = true;
@@ -372,15 +374,14 @@ __global__ void __launch_bounds__(192, 1)
         // gathered tile: owner query and its occupied slots (loaded before the wait)
         const bool gt = t < gi.T1;
         const bool mine = gt && row_ok && q - gi.q_first == t / gi.tpq;  // warp-uniform (H >= 32)
-        uint32_t vm[4] = {0u, 0u, 0u, 0u};
+        int ev[4] = {-1, -1, -1, -1};  // requested now, consumed after S has been read
         if (mine) {
           const int32_t* irow = a.idx + (static_cast<int64_t>(gi.b) * a.Tq + q) * a.k;
           const int kb = t % gi.tpq;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int c = kb * 128 + lane + 32 * i;
-            const int e = c < a.k ? __ldg(irow + c) : -1;
-            vm[i] = __ballot_sync(0xffffffffu, e >= 0 && e < a.Ncap);
+            if (c < a.k) ev[i] = __ldg(irow + c);
           }
         }
         ok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(s_full + sb, (g >> 1) & 1, 48));
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(192, 1)
         uint32_t km[4];
         if (gt) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) km[i] = mine ? vm[i] : 0u;
+          for (int i = 0; i < 4; ++i) km[i] = mine ? __ballot_sync(0xffffffffu, ev[i] >= 0 && ev[i] < a.Ncap) : 0u;
         } else {
           const int j0 = gi.rlo2 + (t - gi.T1) * 128;
           const int cl = max(0, lo2 - j0), ch = min(128, max(0, hi2 - j0));
