@@ -167,12 +167,6 @@ __device__ __forceinline__ uint32_t atom_add(uint32_t addr, uint32_t v) {
   asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
   return old;
 }
-__device__ __forceinline__ float4 ld_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
-  return v;
-}
 }  // namespace clu
 
 // Visible compressed entries for the query at absolute position t.
