@@ -23,7 +23,7 @@ follows.  Sources (web pages, cited by title and section):
           lightning indexer / CSA2, the FP4 global KV cache and SWA Bounded
           Replay.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   R1 one fp32 gate logit per token, shared by K and V; the pooled entry is
      stored in bf16 (round to nearest even) and later steps use the stored value;
   R2 entry j (tokens j*m .. j*m+m-1) is visible to the query at position t
