@@ -518,11 +518,34 @@ class CsaPrefillBench:
         return [g["K"], g["V"], g["gate"], g["q"], g["qI"], g["w"], g["kI"]], self.plan.out
 
     def extra(self):
-        c = self.cfg
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
         t = np.arange(c.T, dtype=np.int64)
         sel = np.minimum((t + 1) // c.m, c.k).sum()
-        return {"indexer_tflop": round(self.dominant_work() / 1e12, 3),
-                "attention_tflop": round(4.0 * c.H * c.D * (sel + _window_pairs(c.T, c.W)) / 1e12, 3)}
+        d = {"indexer_tflop": round(self.dominant_work() / 1e12, 3),
+             "attention_tflop": round(4.0 * c.H * c.D * (sel + _window_pairs(c.T, c.W)) / 1e12, 3)}
+        # the pooling kernel alone (HBM-bound), each launch after an L2 flush
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=g["K"].device)
+        stream = torch.cuda.current_stream()
+        times = []
+        for i in range(6):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            lcc.csa_compress(g["K"], g["V"], g["gate"], self.Kc, self.Vc)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 2:
+                times.append(e0.elapsed_time(e1) / 1e3)
+        del flush
+        tp = float(np.median(times))
+        nbytes = c.B * (c.T * c.D * 2 * 2 + c.T * 4 + c.N * c.D * 2 * 2)  # K, V, gates in; pooled K, V out
+        hbm = peaks()["hbm_gbs"]
+        d["pool"] = {"kernel": "k_pool_small<4,128>", "bound": "hbm", "bytes": nbytes, "launch_us": round(tp * 1e6, 3),
+                     "achieved_gbs": round(nbytes / tp / 1e9, 1), "frac": round(nbytes / tp / 1e9 / hbm, 4),
+                     "timing": "one launch after an L2 flush, median of 4"}
+        return d
 
 
 class HcaPrefillBench:
