@@ -302,6 +302,7 @@ class PairDecode:
             Kr=normal_bf16(s, T_KR, (B, self.R, D), device=device),
             Vr=normal_bf16(s, T_VR, (B, self.R, D), device=device),
             gate=normal_f32(s, T_GATE, (B, self.R), device=device),
+            gate_h=normal_f32(s, T_GATE_H, (B, self.R), device=device),
             Kc_h=normal_bf16(s, T_KC_H, (B, self.N_hca, D), device=device),
             Vc_h=normal_bf16(s, T_VC_H, (B, self.N_hca, D), device=device),
             Kr_h=normal_bf16(s, T_KR_H, (B, self.R, D), device=device),

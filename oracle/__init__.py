@@ -34,7 +34,20 @@ Readings where the pages are silent:
      included) that are present in the raw buffer;
   R6 branches merge by log-sum-exp; an empty branch has lse = -inf, O = 0;
   R7 NVFP4: e2m1 value times the e4m3 scale of its group of 16, element 2i in
-     the low nibble of byte i, no per-tensor scale.
+     the low nibble of byte i, no per-tensor scale;
+  R8 queries of workloads whose query scale is unstated are N(0,1)/sqrt(128)
+     with softmax scale 1;
+  R9 decode windows: the CSA decode window is the W raw tokens ending at the
+     query; in the layer-pair decode each layer keeps its own raw buffer,
+     caches and (CSA) indexer keys, both attend with the shared query, the
+     step-s token sits at raw row W+s (position ctx+s), and a block that the
+     token completes (position+1 divisible by m) is pooled from raw rows
+     W+s+1-m .. W+s into entry (ctx+s+1)/m - 1 before that step attends;
+     an HCA prefill chunk starting at position ctx (a multiple of m) sees the
+     W-1 raw tokens before it plus itself, and its blocks are pooled from raw
+     row W-1 onward into entries ctx/m, ctx/m + 1, ...;
+  R10 the 2048-token prefill pools its CSA and HCA entries from the same raw
+     K/V and gates.
 
 Parity unpinned: the pages print no worked numeric example and no model
 dimensions, so the model-level figures (27% of V3.2's per-token FLOPs, ~10%

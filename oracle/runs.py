@@ -121,8 +121,11 @@ def hca_decode(inp, cfg, batches=None):
 def hca_prefill(inp, cfg, i_rows, q_rows):
     """Sampled queries of the 32768-token chunk appended to the 1M context.
 
-    The chunk's 256 blocks are pooled from the raw buffer (rows W-1 ..) into
-    entries N0 .. N0+255 first; query i sits at position ctx + i.
+    Reading R9: the raw buffer holds the W-1 tokens before the chunk, then
+    the chunk; the chunk's blocks are pooled from raw row W-1 onward into
+    entries N0, N0+1, ... first ([HYBRID]: HCA pools 128 consecutive tokens
+    per entry); query i sits at position ctx + i and sees every complete
+    block plus its window ([VIDEO] "Explained simply": the last 128 tokens).
     """
     Kr, Vr, gate = f64(inp["Kr"][0]), f64(inp["Vr"][0]), f64(inp["gate"][0])
     r0 = cfg.W - 1
@@ -140,15 +143,20 @@ def hca_prefill(inp, cfg, i_rows, q_rows):
 
 
 def pair_decode(inp, cfg, steps=None, batches=None, kI=None, kc_rows=None):
-    """The interleaved CSA/HCA layer pair, decoded step by step.
+    """The interleaved CSA/HCA layer pair, decoded step by step (reading R9).
 
     Step s: the new token (raw row W+s of each layer, position ctx+s) joins
-    both raw buffers; when it completes a CSA block (position+1 divisible by
-    4) the block is pooled into entry (ctx+s+1)/4 - 1 before attention; then
-    the shared query attends through the CSA layer and through the HCA layer.
+    both raw buffers; when it completes a block of a layer (position+1
+    divisible by that layer's m) the block -- raw rows W+s+1-m .. W+s -- is
+    pooled into entry (ctx+s+1)/m - 1 before attention ([HYBRID]: entries
+    are pools of m consecutive tokens; reading R2: an entry is visible once
+    its block is complete); then the shared query attends through the CSA
+    layer and through the HCA layer.  At a 1M-token context no HCA block
+    completes within 64 steps, but the schedule is the same for both layers.
     kI: optional decoded indexer keys [B, Ncap, DI] (fp64) to avoid repeated
     NVFP4 decoding; kc_rows(b, rows) -> (Kc rows, Vc rows) fp64 may replace
-    inp["Kc"] / inp["Vc"] for precompressed entries.
+    inp["Kc"] / inp["Vc"] for precompressed entries.  inp["gate_h"] (HCA
+    gate logits per raw row) is needed only when an HCA block completes.
     """
     steps = range(cfg.steps) if steps is None else steps
     batches = range(cfg.B) if batches is None else batches
@@ -160,16 +168,22 @@ def pair_decode(inp, cfg, steps=None, batches=None, kI=None, kc_rows=None):
         Kr_h, Vr_h = f64(inp["Kr_h"][b]), f64(inp["Vr_h"][b])
         Kc_h, Vc_h = f64(inp["Kc_h"][b]), f64(inp["Vc_h"][b])
         # entries pooled during the run (reading R1: stored in bf16)
-        new_K, new_V = {}, {}
+        new_K, new_V, new_Kh, new_Vh = {}, {}, {}, {}
         last = max(steps) if len(steps) else -1
         for s in range(last + 1):
             pos = cfg.ctx + s
+            r1 = cfg.W + s + 1                       # one past the new token's raw row
             if (pos + 1) % cfg.m_csa == 0:
                 j = (pos + 1) // cfg.m_csa - 1
-                r1 = cfg.W + s + 1
                 kc, vc = pool(Kr[r1 - cfg.m_csa:r1], Vr[r1 - cfg.m_csa:r1],
                               gate[r1 - cfg.m_csa:r1], cfg.m_csa)
                 new_K[j], new_V[j] = kc[0], vc[0]
+            if (pos + 1) % cfg.m_hca == 0:
+                j = (pos + 1) // cfg.m_hca - 1
+                gh = f64(inp["gate_h"][b])
+                kc, vc = pool(Kr_h[r1 - cfg.m_hca:r1], Vr_h[r1 - cfg.m_hca:r1],
+                              gh[r1 - cfg.m_hca:r1], cfg.m_hca)
+                new_Kh[j], new_Vh[j] = kc[0], vc[0]
             if s not in steps:
                 continue
             q, qI, w = f64(inp["q"][s, b]), f64(inp["qI"][s, b]), f64(inp["w"][s, b])
@@ -187,10 +201,15 @@ def pair_decode(inp, cfg, steps=None, batches=None, kI=None, kc_rows=None):
             cO, cL = attend(q, np.concatenate([Ko, Kn]), np.concatenate([Vo, Vn]))
             rows = window_positions(pos, cfg.W, cfg.raw_pos0, cfg.W + s + 1) - cfg.raw_pos0
             sO, sL = attend(q, Kr[rows], Vr[rows])
-            hO, hL = attend(q, Kc_h[:visible_count(pos, cfg.m_hca, cfg.N_hca)],
-                            Vc_h[:visible_count(pos, cfg.m_hca, cfg.N_hca)])
+            nvh = visible_count(pos, cfg.m_hca, cfg.N_hca + len(new_Kh))
+            Kh = np.concatenate([Kc_h[:min(nvh, cfg.N_hca)],
+                                 np.array([new_Kh[j] for j in range(cfg.N_hca, nvh)]).reshape(-1, cfg.D)])
+            Vh = np.concatenate([Vc_h[:min(nvh, cfg.N_hca)],
+                                 np.array([new_Vh[j] for j in range(cfg.N_hca, nvh)]).reshape(-1, cfg.D)])
+            hO, hL = attend(q, Kh, Vh)
             shO, shL = attend(q, Kr_h[rows], Vr_h[rows])
             out[(s, b)] = dict(idx=idx, scores=sc, kth=kth,
                                csa=merge([cO, sO], [cL, sL]), hca=merge([hO, shO], [hL, shL]),
-                               new_entries={j: (new_K[j], new_V[j]) for j in new_K})
+                               new_entries={j: (new_K[j], new_V[j]) for j in new_K},
+                               new_entries_h={j: (new_Kh[j], new_Vh[j]) for j in new_Kh})
     return out

@@ -331,3 +331,98 @@ def test_page_facts_match_workloads():
     assert PairDecode().m_hca // PairDecode().m_csa == f["hca_lighter_than_csa"]["value"]
     for c in (CsaDecode(), CsaPrefill(), PairDecode()):
         assert c.k == f["csa_topk_typical"]["value"] and c.W == f["window_tokens"]["value"]
+
+
+# ---------------------------------------------------------------------------
+# layer compositions over time: every expected value below comes from one
+# contiguous token sequence pooled in full (oracle.pool over the whole
+# sequence) and the branch functions pinned above, applied at each absolute
+# position; the compositions under test instead pool blocks out of raw
+# buffers at offsets of their own.  [HYBRID] "두 가지 압축 전략: CSA 및 HCA":
+# entries pool m consecutive tokens and the window branch runs beside them;
+# [VIDEO] "쉽게 이해하기": the window is the most recent tokens (128 in the
+# model).  These fix reading R9 (where each new token sits in the raw buffer,
+# which raw rows a completed block pools, and from which step on the new
+# entry is visible).
+# ---------------------------------------------------------------------------
+def _bits(x):
+    return oracle.f64_to_bf16_bits(x)
+
+
+def test_pair_decode_matches_full_sequence_pooling():
+    from datagen.workloads import PairDecode
+    cfg = PairDecode(B=1, ctx=16, steps=9, D=8, H=2, HI=2, DI=16, k=3, W=4, m_csa=4, m_hca=8)
+    L = cfg.ctx + cfg.steps                                   # 25 tokens in all
+    K, V, g = _bf16_grid((L, cfg.D)), _bf16_grid((L, cfg.D)), rng.standard_normal(L)
+    Kh, Vh, gh = _bf16_grid((L, cfg.D)), _bf16_grid((L, cfg.D)), rng.standard_normal(L)
+    kI = _bf16_grid((cfg.Ncap_csa, cfg.DI))
+    q = _bf16_grid((cfg.steps, 1, cfg.H, cfg.D), 0.5)
+    qI = _bf16_grid((cfg.steps, 1, cfg.HI, cfg.DI))
+    w = rng.uniform(0, 1, (cfg.steps, 1, cfg.HI))
+    # whole-sequence pooling: every entry that exists at the end of the run
+    Kc_all, Vc_all = oracle.pool(K, V, g, cfg.m_csa)          # 6 entries
+    Kh_all, Vh_all = oracle.pool(Kh, Vh, gh, cfg.m_hca)       # 3 entries (the last completes at step 7)
+    assert len(Kc_all) == cfg.Ncap_csa and len(Kh_all) == 3
+    r0 = cfg.ctx - cfg.W                                      # raw buffers start W tokens before ctx
+    inp = dict(Kr=_bits(K[None, r0:]), Vr=_bits(V[None, r0:]), gate=g[None, r0:],
+               Kr_h=_bits(Kh[None, r0:]), Vr_h=_bits(Vh[None, r0:]), gate_h=gh[None, r0:],
+               Kc=_bits(Kc_all[None, :cfg.N_csa]), Vc=_bits(Vc_all[None, :cfg.N_csa]),
+               Kc_h=_bits(Kh_all[None, :cfg.N_hca]), Vc_h=_bits(Vh_all[None, :cfg.N_hca]),
+               q=_bits(q), qI=_bits(qI), w=w)
+    got = runs.pair_decode(inp, cfg, kI=kI[None])
+    seen_csa, seen_hca = [], []
+    for s in range(cfg.steps):
+        t = cfg.ctx + s
+        c = runs.csa_branch(q[s, 0], t, qI[s, 0], w[s, 0], kI, Kc_all, Vc_all, cfg.m_csa, cfg.k)
+        sw = runs.swa_branch(q[s, 0], t, K, V, 0, cfg.W)
+        h = runs.hca_branch(q[s, 0], t, Kh_all, Vh_all, cfg.m_hca)
+        swh = runs.swa_branch(q[s, 0], t, Kh, Vh, 0, cfg.W)
+        want_c = oracle.merge([c["O"], sw["O"]], [c["lse"], sw["lse"]])
+        want_h = oracle.merge([h["O"], swh["O"]], [h["lse"], swh["lse"]])
+        r = got[(s, 0)]
+        assert np.array_equal(r["idx"], c["idx"]), s
+        np.testing.assert_allclose(r["scores"], c["scores"], atol=1e-12)
+        for a, b in ((r["csa"], want_c), (r["hca"], want_h)):
+            np.testing.assert_allclose(a[0], b[0], atol=1e-12)
+            np.testing.assert_allclose(a[1], b[1], atol=1e-12)
+        seen_csa.append(c["n_visible"])
+        seen_hca.append(h["n_visible"])
+        assert sw["n_keys"] == cfg.W
+    # the schedule: CSA entry 4 becomes visible at position 19 (step 3), entry 5 at
+    # position 23 (step 7); HCA entry 2 at position 23 (step 7)
+    assert seen_csa == [4, 4, 4, 5, 5, 5, 5, 6, 6]
+    assert seen_hca == [2, 2, 2, 2, 2, 2, 2, 3, 3]
+    new = got[(cfg.steps - 1, 0)]
+    assert sorted(new["new_entries"]) == [4, 5] and sorted(new["new_entries_h"]) == [2]
+    np.testing.assert_array_equal(new["new_entries"][5][0], Kc_all[5])
+    np.testing.assert_array_equal(new["new_entries_h"][2][1], Vh_all[2])
+
+
+def test_hca_prefill_matches_full_sequence_pooling():
+    from datagen.workloads import HcaPrefill
+    cfg = HcaPrefill(ctx=32, Tc=24, N0=4, D=8, H=2, W=4, m=8)
+    L = cfg.ctx + cfg.Tc                                       # 56 tokens in all
+    K, V, g = _bf16_grid((L, cfg.D)), _bf16_grid((L, cfg.D)), rng.standard_normal(L)
+    q = _bf16_grid((cfg.Tc, cfg.H, cfg.D), 0.5)
+    Kc_all, Vc_all = oracle.pool(K, V, g, cfg.m)               # 7 entries
+    assert len(Kc_all) == cfg.Ncap
+    r0 = cfg.raw_pos0                                          # W-1 tokens before the chunk
+    Kc0 = np.zeros((1, cfg.Ncap, cfg.D))
+    Kc0[0, :cfg.N0] = Kc_all[:cfg.N0]
+    Vc0 = np.zeros((1, cfg.Ncap, cfg.D))
+    Vc0[0, :cfg.N0] = Vc_all[:cfg.N0]
+    inp = dict(Kr=_bits(K[None, r0:]), Vr=_bits(V[None, r0:]), gate=g[None, r0:],
+               Kc=_bits(Kc0), Vc=_bits(Vc0))
+    rows = list(range(cfg.Tc))
+    got = runs.hca_prefill(inp, cfg, rows, _bits(q))
+    np.testing.assert_array_equal(got["Kc_new"], Kc_all[cfg.N0:])
+    np.testing.assert_array_equal(got["Vc_new"], Vc_all[cfg.N0:])
+    for i in rows:
+        t = cfg.ctx + i
+        h = runs.hca_branch(q[i], t, Kc_all, Vc_all, cfg.m)
+        sw = runs.swa_branch(q[i], t, K, V, 0, cfg.W)
+        want = oracle.merge([h["O"], sw["O"]], [h["lse"], sw["lse"]])
+        r = got["rows"][i]
+        assert r["hca"]["n_visible"] == (t + 1) // cfg.m
+        np.testing.assert_allclose(r["layer"][0], want[0], atol=1e-12)
+        np.testing.assert_allclose(r["layer"][1], want[1], atol=1e-12)
