@@ -140,11 +140,14 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w,
  * lcc_lightning_index_topk, minus the workspace: the scratch lives in a
  * fixed 8 MiB array inside the library (8388608 bytes of device memory that
  * every GPU loading the library keeps until the process exits).
- *  - Queries are processed in chunks sized to that array; a request whose
- *    single query row needs more than 8 MiB (per batch row: Ncap*4 bytes of
- *    scores, ceil(Ncap/16)*4 bytes of group maxima, 8 bytes of counters and,
- *    when Ncap > 16384, ceil(Ncap/16384)*(4 + 8192) bytes of candidate
- *    lists; each array rounded up to 256 bytes) is rejected with
+ *  - Requests with bf16 keys, Tq*HI > 16 and k <= 256 (prefill shapes) run
+ *    the indexer with the top-k fused into its epilogue, which needs no
+ *    scratch: they have no size limit and leave the array untouched.
+ *  - Other requests are processed in query chunks sized to that array; one
+ *    whose single query row needs more than 8 MiB (per batch row: Ncap*4
+ *    bytes of scores, ceil(Ncap/16)*4 bytes of group maxima, 8 bytes of
+ *    counters and, when Ncap > 16384, ceil(Ncap/16384)*(4 + 8192) bytes of
+ *    candidate lists; each array rounded up to 256 bytes) is rejected with
  *    LCC_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on each device looks up the array's device address
  *    (and sets kernel attributes); make that first call before any stream

@@ -225,7 +225,9 @@ def lightning_index_topk_noalloc(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None
 
     The library keeps its scratch in a fixed 8 MiB device array shared by all
     calls (overlapping calls race; make the first call on a device before any
-    graph capture).  idx must be passed in so that nothing is allocated here.
+    graph capture); prefill-shaped requests (bf16 keys, Tq*HI > 16, k <= 256)
+    take the fused top-k and use no scratch.  idx must be passed in so that
+    nothing is allocated here.
     """
     _need(qI, torch.bfloat16, "qI", 4)
     _need(w, torch.float32, "w", 3)

@@ -1144,6 +1144,11 @@ extern "C" lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const
   lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
   if (st != LCC_OK) return st;
   if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
+  // prefill-shaped requests take the indexer with the top-k fused into its
+  // epilogue: no scratch at all, so no size limit either
+  if (use_fused_topk(fmt, Tq, HI, k))
+    return run_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx, score, nullptr,
+                          Tq, static_cast<cudaStream_t>(stream));
   // bytes one query row of every batch needs: scores, group maxima, candidates, counters
   const size_t per_q = index_ws_rows(B, Ncap).total;
   if (per_q > kNoAllocScratchBytes)
