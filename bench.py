@@ -185,6 +185,39 @@ def ncu_traffic(kernel: str, workload: str):
     return d.get("dram_bytes_per_launch")
 
 
+def _oracle_worker(job):
+    """One oracle process: its share of the sampled queries, single-threaded."""
+    name, budget_s, max_queries, first, stride = job
+    torch.set_num_threads(1)
+    return WORKLOADS[name]().oracle_sample(budget_s, max_queries, first=first, stride=stride)
+
+
+def oracle_on_host_cores(name, budget_s, max_queries=None):
+    """The fp64 oracle on every host core this process may use: one spawned
+    single-threaded process per core (up to 32), each on its own batch rows.
+    Returns (queries, aggregate queries/s, description, workers, cpu_count)."""
+    import multiprocessing as mp
+    ncpu = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    nw = max(1, min(ncpu, 32))
+    per = None if max_queries is None else max(1, -(-max_queries // nw))
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        # spawn, not fork: this process has already used the GPU
+        with mp.get_context("spawn").Pool(nw) as pool:
+            res = pool.map(_oracle_worker, [(name, budget_s, per, i, nw) for i in range(nw)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    n = sum(r[0] for r in res)
+    rate = sum(r[0] / r[1] for r in res if r[1] > 0)
+    return n, rate, f"{n} {res[0][2]}; {nw} single-threaded worker processes", nw, os.cpu_count()
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -262,7 +295,7 @@ class CsaDecodeBench:
         from long_context_compressed_15_b300.layers import CsaLayerPlan
         c = self.cfg
         self.sets = [c.make(dev, rot=r) for r in range(NSETS)]
-        self.plan = CsaLayerPlan(c.B, 1, c.H, c.D, c.N, c.k, c.W, device=dev)
+        self.plan = CsaLayerPlan(c.B, 1, c.H, c.D, c.N, c.k, c.W, device=dev, m=c.m)
         self.pos = torch.full((c.B,), c.q_pos, dtype=torch.int64, device=dev)
         self.raw0 = torch.full((c.B,), c.raw_pos0, dtype=torch.int64, device=dev)
         self.nval = torch.full((c.B,), c.N, dtype=torch.int32, device=dev)
@@ -284,11 +317,17 @@ class CsaDecodeBench:
         import long_context_compressed_15_b300 as lcc
         for i in range(i0, i0 + n):
             s = self.sets[i % NSETS]
-            lcc.lightning_index_scores(s["qI"], s["w"], self.pos, s["kI"], self.nval, 4, scores=self.scores)
+            lcc.lightning_index_scores(s["qI"], s["w"], self.pos, s["kI"], self.nval, self.cfg.m, scores=self.scores)
 
     def dominant_work(self):
+        """Algorithmic bytes of one indexer launch: keys, indexer query and head weights."""
         c = self.cfg
-        return c.B * (c.N * c.DI * 2 + c.HI * c.DI * 2 + c.HI * 4 + c.N * 4)
+        return c.B * (c.N * c.DI * 2 + c.HI * c.DI * 2 + c.HI * 4)
+
+    def dominant_extra_bytes(self):
+        """Bytes the launch also moves that the roofline does not count: the fp32 scores it writes."""
+        c = self.cfg
+        return c.B * c.N * 4
 
     # end to end: the step's queries come from pinned host memory, the layer output goes back
     def e2e_io(self):
@@ -296,7 +335,8 @@ class CsaDecodeBench:
         return [s["q"], s["qI"], s["w"]], self.plan.out
 
     # fp64 oracle on a bounded sample of the workload
-    def oracle_sample(self, budget_s, max_queries=None):
+    def oracle_sample(self, budget_s, max_queries=None, first=0, stride=1):
+        """fp64 oracle on decode queries of batch rows first, first+stride, ... (cycling)."""
         import datagen
         import oracle
         from datagen import workloads as wl
@@ -304,7 +344,7 @@ class CsaDecodeBench:
         c = self.cfg
         s = c.seed
         done, t_oracle = 0, 0.0
-        b = 0
+        b = first
         while t_oracle < budget_s and (max_queries is None or done < max_queries):
             bb = b % c.B
             kI = _host_rows(s, wl.T_KI, bb, c.N, c.DI)
@@ -325,9 +365,26 @@ class CsaDecodeBench:
             oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
             t_oracle += time.perf_counter() - t0
             done += 1
-            b += 1
-        return done, t_oracle, f"{done} decode queries of the batch (inputs regenerated on the host, untimed)"
+            b += stride
+        return done, t_oracle, "decode queries of the batch (inputs regenerated on the host, untimed)"
 
+
+
+class DsaDecodeBench(CsaDecodeBench):
+    """The DSA comparator of csa_decode: the same batch and context with m = 1, so
+    the indexer scores all 65536 raw tokens of each sequence (4x the entries)."""
+    name = "dsa_decode"
+
+    def __init__(self):
+        from datagen.workloads import DsaDecode
+        self.cfg = DsaDecode()
+
+    def config(self):
+        d = super().config()
+        d["workload"] = ("dsa_decode: the DSA comparator of csa_decode -- CSA layer decode with m=1 (the "
+                         "indexer scores all 65536 raw tokens), batch 32, bf16 indexer keys 8x64, top-128, "
+                         "window 128, 64 heads x 128")
+        return d
 
 
 def _host_rows(seed, tid, b, n, d, scale=1.0):
@@ -418,33 +475,35 @@ class PairDecodeBench:
         return self.cfg.B
 
     def setup(self, dev):
-        from long_context_compressed_15_b300.layers import CsaLayerPlan, HcaLayerPlan
+        from long_context_compressed_15_b300.layers import PairDecodePlan
         c = self.cfg
-        self.g = c.make(dev)
-        self.csa = CsaLayerPlan(c.B, 1, c.H, c.D, c.Ncap_csa, c.k, c.W, device=dev)
-        self.hca = HcaLayerPlan(c.B, 1, c.H, c.D, c.N_hca, c.W, device=dev)
-        self.nval = torch.full((c.B,), c.N_csa, dtype=torch.int32, device=dev)
-        self.nval_h = torch.full((c.B,), c.N_hca, dtype=torch.int32, device=dev)
-        self.pos = [torch.full((c.B,), c.ctx + s, dtype=torch.int64, device=dev) for s in range(c.steps)]
-        self.raw0 = torch.full((c.B,), c.raw_pos0, dtype=torch.int64, device=dev)
+        g = self.g = c.make(dev)
+        B, W = c.B, c.W
+        self.plan = PairDecodePlan(B, c.H, c.D, c.Ncap_csa, c.N_hca, c.k, W, device=dev)
+        raw0 = torch.full((B,), c.raw_pos0, dtype=torch.int64, device=dev)
+        # caches as they stand before step 0 (each step's token is appended by the library)
+        self.csa_c = dict(Kr=g["Kr"], Vr=g["Vr"], gate=g["gate"], raw_pos0=raw0, Kc=g["Kc"], Vc=g["Vc"],
+                          n_valid=torch.full((B,), c.N_csa, dtype=torch.int32, device=dev), kI=g["kI_packed"],
+                          kI_scale=g["kI_scale"])
+        self.hca_c = dict(Kr=g["Kr_h"], Vr=g["Vr_h"], gate=g["gate_h"], raw_pos0=raw0, Kc=g["Kc_h"], Vc=g["Vc_h"],
+                          n_valid=torch.full((B,), c.N_hca, dtype=torch.int32, device=dev))
+        self.pos = [torch.full((B,), c.ctx + s, dtype=torch.int64, device=dev) for s in range(c.steps)]
+        self.new = []
+        for s in range(c.steps):
+            r = W + s
+            j = min((c.ctx + s + 1) // c.m_csa - 1, c.Ncap_csa - 1)   # entry this token would complete
+            self.new.append((
+                dict(k=g["Kr"][:, r].contiguous(), v=g["Vr"][:, r].contiguous(), g=g["gate"][:, r].contiguous(),
+                     kI=g["kI_packed"][:, j].contiguous(), kI_scale=g["kI_scale"][:, j].contiguous()),
+                dict(k=g["Kr_h"][:, r].contiguous(), v=g["Vr_h"][:, r].contiguous(),
+                     g=g["gate_h"][:, r].contiguous())))
         self.scores = torch.empty((c.B, 1, c.Ncap_csa), dtype=torch.float32, device=dev)
 
     def _step(self, s):
-        import long_context_compressed_15_b300 as lcc
-        c, g = self.cfg, self.g
-        pos = c.ctx + s
-        if s == 0:
-            self.nval.fill_(c.N_csa)
-        if (pos + 1) % c.m_csa == 0:
-            j = (pos + 1) // c.m_csa - 1
-            r1 = c.W + s + 1
-            lcc.csa_compress(g["Kr"][:, r1 - 4:r1], g["Vr"][:, r1 - 4:r1], g["gate"][:, r1 - 4:r1],
-                             g["Kc"][:, j:j + 1], g["Vc"][:, j:j + 1], n_blocks=1)
-            self.nval.add_(1)
-        q = g["q"][s][:, None]
-        self.csa(q, g["qI"][s][:, None], g["w"][s][:, None], self.pos[s], g["kI_packed"], self.nval, g["Kc"],
-                 g["Vc"], g["Kr"], g["Vr"], self.raw0, kI_scale=g["kI_scale"])
-        self.hca(q, self.pos[s], g["Kc_h"], g["Vc_h"], self.nval_h, g["Kr_h"], g["Vr_h"], self.raw0)
+        g = self.g
+        new_c, new_h = self.new[s]
+        self.plan(self.pos[s], g["q"][s][:, None], g["qI"][s][:, None], g["w"][s][:, None], new_c, new_h,
+                  self.csa_c, self.hca_c)
 
     def run_steps(self, i0, n):
         for i in range(i0, i0 + n):
@@ -459,12 +518,19 @@ class PairDecodeBench:
                                        c.N_csa, c.m_csa, kI_scale=g["kI_scale"], scores=self.scores)
 
     def dominant_work(self):
+        """Algorithmic bytes of one indexer launch: NVFP4 keys + scales, indexer query, head weights."""
         c = self.cfg
-        return c.B * (c.N_csa * (c.DI // 2 + c.DI // 16) + c.HI * c.DI * 2 + c.HI * 4 + c.N_csa * 4)
+        return c.B * (c.N_csa * (c.DI // 2 + c.DI // 16) + c.HI * c.DI * 2 + c.HI * 4)
+
+    def dominant_extra_bytes(self):
+        c = self.cfg
+        return c.B * c.N_csa * 4
 
     def e2e_io(self):
         g = self.g
-        return [g["q"][0], g["qI"][0], g["w"][0]], self.hca.out
+        new_c, new_h = self.new[0]
+        return [g["q"][0], g["qI"][0], g["w"][0], new_c["k"], new_c["v"], new_c["g"], new_h["k"], new_h["v"],
+                new_h["g"]], self.plan.hca.out
 
 
 class CsaPrefillBench:
@@ -600,8 +666,24 @@ class HcaPrefillBench:
         return [g["Kr"], g["Vr"], g["gate"], g["q"]], self.plan.out
 
 
-WORKLOADS = {"csa_decode": CsaDecodeBench, "hca_decode": HcaDecodeBench, "pair_decode": PairDecodeBench,
-             "csa_prefill": CsaPrefillBench, "hca_prefill": HcaPrefillBench}
+WORKLOADS = {"csa_decode": CsaDecodeBench, "dsa_decode": DsaDecodeBench, "hca_decode": HcaDecodeBench,
+             "pair_decode": PairDecodeBench, "csa_prefill": CsaPrefillBench, "hca_prefill": HcaPrefillBench}
+
+
+def dsa_comparison(csa, dsa):
+    """CSA (m=4) against the DSA comparator (m=1) on the same decode batch: measured
+    step times and the algorithmic indexer bytes / FLOPs and cache bytes per token."""
+    from datagen.workloads import CsaDecode, DsaDecode
+    c, d = CsaDecode(), DsaDecode()
+    kv_row = 2 * c.D * 2
+    idx_c, idx_d = c.N * c.DI * 2, d.N * d.DI * 2
+    return {"step_time_ratio_csa_over_dsa": round(csa["ms_per_step"] / dsa["ms_per_step"], 4),
+            "indexer_bytes_ratio": round(idx_c / idx_d, 4),
+            "indexer_flops_ratio": round((2 * c.HI * c.DI * c.N) / (2 * d.HI * d.DI * d.N), 4),
+            "cache_bytes_per_token": {"csa_m4_bf16_keys": (kv_row + c.DI * 2) / 4,
+                                      "csa_m4_nvfp4_keys": (kv_row + c.DI // 2 + c.DI // 16) / 4,
+                                      "hca_m128": kv_row / 128, "dsa_m1_bf16_keys": kv_row + d.DI * 2},
+            "note": "same batch, context, k and window; cache bytes exclude the fixed raw window"}
 
 
 # ---------------------------------------------------------------------------
@@ -640,9 +722,13 @@ def roofline_of(wb, stream, reps_hint, pk):
         achieved, peak, unit = work / td / 1e9, pk["hbm_gbs"], "GB/s"
     else:
         achieved, peak, unit = work / td / 1e12, pk["bf16_tflops"], "TFLOP/s"
-    return {"bound": wb.bound, "kernel": wb.dominant, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wb.dominant, wb.name),
-            "peak_source": pk["source"], "launch_us": round(td * 1e6, 3)}
+    d = {"bound": wb.bound, "kernel": wb.dominant, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(wb.dominant, wb.name),
+         "peak_source": pk["source"], "launch_us": round(td * 1e6, 3), "work_per_launch": work}
+    if hasattr(wb, "dominant_extra_bytes"):
+        d["extra_bytes"] = wb.dominant_extra_bytes()
+        d["extra_note"] = "bytes the launch also writes (fp32 scores for the top-k), not counted in achieved"
+    return d
 
 
 def e2e_of(wb, ws, n_steps):
@@ -734,6 +820,19 @@ def run_ours(args, ws, rank, local):
     t = max_over_ranks(t, ws)
     value = wb.units_per_step() * args.steps * ws / t
 
+    # the same step repeated for at least 0.3 s, with its own clock samples, to
+    # steady a short headline region
+    n_rep = G * max(1, int(math.ceil(0.3 / max(t / args.steps, 1e-9) / G)))
+    clocks_r = ClockSampler(torch.cuda.current_device())
+    runs_r = sch.runs(n_rep)
+    clocks_r.start()
+    t_rep = time_graph(runs_r, stream, on_enqueued=clocks_r.sample_now)
+    ck_r = clocks_r.stop()
+    lcc.sync_status()
+    t_rep = max_over_ranks(t_rep, ws)
+    repeat = {"steps": n_rep, "seconds": round(t_rep, 4), "value": round(wb.units_per_step() * n_rep * ws / t_rep, 1),
+              "ms_per_step": round(t_rep / n_rep * 1e3, 5), "clocks": ck_r}
+
     roofline = roofline_of(wb, stream, max(4, min(64, args.steps // G)), pk)
     if hasattr(wb, "step_bytes"):
         roofline["step_hbm_gbs"] = round(wb.step_bytes() * args.steps / t / 1e9, 1)
@@ -742,14 +841,15 @@ def run_ours(args, ws, rank, local):
     line = {"metric": METRIC, "value": round(value, 1), "unit": wb.unit, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t / args.steps * 1e3, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": wb.config(), "clocks": ck, "e2e": e2e,
+            "config": wb.config(), "clocks": ck, "repeat": repeat, "e2e": e2e,
             "gpu_launches": int(round(launches_per_step * args.steps)), "roofline": roofline}
     if hasattr(wb, "extra"):
         line["config"].update(wb.extra())
     if rank == 0 and not args.no_cpu_baseline and hasattr(wb, "oracle_sample"):
-        n, tc, what = wb.oracle_sample(args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(n / tc, 3), "unit": wb.unit, "cores": blas_threads(),
-                                "kind": "oracle", "sample": what}
+        n, rate, what, nw, ncpu = oracle_on_host_cores(args.workload, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(rate, 3), "unit": wb.unit, "cores": nw, "host_cpu_count": ncpu,
+                                "kind": "oracle", "sample": f"about {args.cpu_budget:g} s of oracle work per "
+                                f"worker: {what}"}
     if not args.no_secondary:
         del wb, sch
         torch.cuda.synchronize()
@@ -758,6 +858,9 @@ def run_ours(args, ws, rank, local):
         for name in WORKLOADS:
             if name != args.workload:
                 line["workloads"][name] = measure_secondary(name, dev, stream, pk)
+        w = line["workloads"]
+        if args.workload == "csa_decode" and "dsa_decode" in w:
+            w["dsa_decode"]["vs_csa_decode"] = dsa_comparison({"ms_per_step": line["ms_per_step"]}, w["dsa_decode"])
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -773,17 +876,16 @@ def run_reference(args, ws, rank):
     per_step = 1
     wb.oracle_sample(float("inf"), max_queries=min(args.warmup, 3) * per_step)
     t0 = time.perf_counter()
-    n, tc, what = wb.oracle_sample(float("inf"), max_queries=args.steps * per_step)
+    n, value, what, nw, ncpu = oracle_on_host_cores(args.workload, float("inf"), max_queries=args.steps * per_step)
     wall = time.perf_counter() - t0
-    value = n / tc
-    cores = blas_threads()
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": wb.unit, "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tc / args.steps * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step / value * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": wb.config(),
-            "cpu_baseline": {"value": round(value, 3), "unit": wb.unit, "cores": cores, "kind": "oracle",
-                             "sample": f"one query of the batch per step; {what}"},
-            "e2e": {"value": round(n / wall, 3), "unit": wb.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": round(value, 3), "unit": wb.unit, "cores": nw, "host_cpu_count": ncpu,
+                             "kind": "oracle", "sample": f"one query of the batch per step; {what}"},
+            "e2e": {"value": round(n / wall, 3), "unit": wb.unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                    "note": "queries / wall time of the whole sampled run, process start-up included"}}
     print(json.dumps(line), flush=True)
 
 

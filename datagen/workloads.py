@@ -29,6 +29,7 @@ T_K, T_V, T_GATE, T_Q, T_QI, T_W, T_KI = 1, 2, 3, 4, 5, 6, 7
 T_KC, T_VC, T_KR, T_VR = 8, 9, 10, 11
 T_KC_H, T_VC_H, T_KR_H, T_VR_H, T_GATE_H = 12, 13, 14, 15, 16
 T_IDX = 17
+T_RQ, T_RQI, T_RW = 18, 19, 20
 
 QSCALE_128 = 1.0 / math.sqrt(128.0)
 
@@ -109,6 +110,51 @@ class CsaDecode:
             kI=normal_bf16(s, T_KI, (B, N, self.DI), device=device),
             Kr=normal_bf16(s, T_KR, (B, self.W, self.D), device=device),
             Vr=normal_bf16(s, T_VR, (B, self.W, self.D), device=device),
+            q=normal_bf16(s, T_Q, (B, 1, self.H, self.D), self.q_scale, device=device),
+            qI=normal_bf16(s, T_QI, (B, 1, self.HI, self.DI), device=device),
+            w=uniform_f32(s, T_W, (B, 1, self.HI), device=device),
+        )
+
+
+@dataclass(frozen=True)
+class DsaDecode:
+    """The DSA comparator of the CSA decode: the same 32 sequences and 65536-token
+    context, but every raw token is its own entry (m = 1), so the indexer scores
+    all 65536 tokens; the window rows are the cache's last W rows."""
+    seed: int = 5
+    B: int = 32
+    ctx: int = 65536
+    D: int = 128
+    H: int = 64
+    HI: int = 8
+    DI: int = 64
+    k: int = 128
+    W: int = 128
+    m: int = 1
+    q_scale: float = QSCALE_128
+
+    @property
+    def N(self):
+        return self.ctx // self.m
+
+    @property
+    def q_pos(self):
+        return self.ctx - 1
+
+    @property
+    def raw_pos0(self):
+        return self.ctx - self.W
+
+    def make(self, device="cpu", rot=0):
+        s = self.seed + 7919 * rot
+        B, N = self.B, self.N
+        Kc = normal_bf16(s, T_KC, (B, N, self.D), device=device)
+        Vc = normal_bf16(s, T_VC, (B, N, self.D), device=device)
+        return dict(
+            Kc=Kc, Vc=Vc,
+            kI=normal_bf16(s, T_KI, (B, N, self.DI), device=device),
+            Kr=Kc[:, N - self.W:].contiguous(),
+            Vr=Vc[:, N - self.W:].contiguous(),
             q=normal_bf16(s, T_Q, (B, 1, self.H, self.D), self.q_scale, device=device),
             qI=normal_bf16(s, T_QI, (B, 1, self.HI, self.DI), device=device),
             w=uniform_f32(s, T_W, (B, 1, self.HI), device=device),
@@ -312,10 +358,21 @@ class PairDecode:
             w=uniform_f32(s, T_W, (self.steps, B, self.HI), device=device),
         )
 
+    def make_replay(self, R, device="cpu"):
+        """Queries of the last R context tokens (positions ctx-R .. ctx-1), [R, B, ...]:
+        the inputs of a bounded replay of the window state."""
+        s, B = self.seed, self.B
+        return dict(
+            rq=normal_bf16(s, T_RQ, (R, B, self.H, self.D), self.q_scale, device=device),
+            rqI=normal_bf16(s, T_RQI, (R, B, self.HI, self.DI), device=device),
+            rw=uniform_f32(s, T_RW, (R, B, self.HI), device=device),
+        )
+
 
 WORKLOADS = {
     "tiny_prefill": TinyPrefill,
     "csa_decode": CsaDecode,
+    "dsa_decode": DsaDecode,
     "csa_prefill": CsaPrefill,
     "hca_decode": HcaDecode,
     "hca_prefill": HcaPrefill,

@@ -87,6 +87,81 @@ lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* g
                             int64_t kv_bstride, int64_t gate_bstride,
                             lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
                             void* stream);                      /* m = 128 */
+/* The same for any supported ratio m in {1, 4, 128}.  m = 1 makes every
+ * token its own entry (the softmax over one logit is 1, so Kc = K exactly):
+ * the cache of the DSA comparator, whose indexer scores every raw token
+ * ([THREAD] "주요 댓글": DSA keeps the full KV and runs the light indexer over
+ * all of it, then attends only to the selected tokens). */
+lcc_status lcc_compress(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate,
+                        int B, int n_blocks, int D,
+                        int64_t kv_bstride, int64_t gate_bstride,
+                        lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
+                        void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Query / KV prologue ([HYBRID]: both mechanisms use MQA with shared KV
+ * projections, apply query and KV normalisation and use partial RoPE).  For
+ * every token (b, t) at position p = pos0[b] + t:
+ *   RMSNorm(x) = x / sqrt(mean_c(x_c^2) + eps) * gamma   (over the D channels)
+ *   q_out[b,t,h] = RoPE_p(RMSNorm(q[b,t,h]) with gamma_q)   for every head h
+ *   k_out[b,t]   = RoPE_p(RMSNorm(k[b,t])   with gamma_k)
+ *   v_out[b,t]   = RMSNorm(v[b,t]) with gamma_v              (no rotation)
+ * RoPE_p rotates the last d_rope channels in pairs (c, c + d_rope/2),
+ * c = D-d_rope .. D-d_rope/2-1, pair i by the angle p * rope_base^(-2i/d_rope):
+ *   (x1, x2) -> (x1 cos - x2 sin, x2 cos + x1 sin); the other channels pass.
+ * Arithmetic in fp32 (the angle reduced modulo 2*pi in double precision),
+ * outputs rounded to bf16 (nearest even).
+ * q: [B, T, H, D] bf16; k, v: [B, T, D] bf16 (v, v_out, gamma_v may all be
+ * NULL); gammas: [D] fp32; pos0: [B] int64 device array.  Outputs may alias
+ * their inputs (in place).  D in {64, 128}; 1 <= H <= 128; d_rope a multiple
+ * of 16 in [0, D]; eps >= 0; rope_base > 1.
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_qkv_prologue(const lcc_bf16* q, const lcc_bf16* k, const lcc_bf16* v,
+                            int B, int T, int H, int D,
+                            const float* gamma_q, const float* gamma_k, const float* gamma_v,
+                            float eps, int d_rope, float rope_base, const int64_t* pos0,
+                            lcc_bf16* q_out, lcc_bf16* k_out, lcc_bf16* v_out, void* stream);
+
+/* ---------------------------------------------------------------------- *
+ * Decode-step update of one layer's caches ([VIDEO] "쉽게 이해하기": the
+ * window keeps the most recent 128 raw tokens, CSA pools every 4 tokens and
+ * HCA every 128; [HYBRID]: an entry is the softmax-weighted pool of m
+ * consecutive tokens).  For every sequence b, with t = pos[b] the position of
+ * the new token and r = t - raw_pos0[b] its raw row:
+ *   Kr[b, r, :] = k_new[b, :], Vr[b, r, :] = v_new[b, :], gate_r[b, r] = g_new[b];
+ *   if (t + 1) % m == 0 (the token completes block j = (t + 1)/m - 1):
+ *     Kc/Vc[b, j, :] = softmax-weighted pool of raw rows r-m+1 .. r, computed
+ *       exactly as lcc_csa_compress / lcc_hca_compress compute it;
+ *     kI[b, j] = kI_new[b] (and the NVFP4 scales), when kI_new is not NULL;
+ *     n_valid[b] = j + 1.
+ * Positions, raw offsets and counts live in device memory and every decision
+ * is taken on the device, so the call can sit in a captured CUDA graph; the
+ * caller advances pos between steps and passes the same pos as q_pos0 to the
+ * step's attention calls (the new token is the query).
+ * m in {1, 4, 128} (m = 1: every token is its own entry); D in {64, 128}.
+ * k_new, v_new: [B, D] bf16; g_new: [B] fp32; pos, raw_pos0: [B] int64.
+ * Kr, Vr: [B, Rcap, D] bf16 (batch stride r_bstride elements, rows D apart);
+ * gate_r: [B, Rcap] fp32 (batch stride g_bstride); Kc, Vc: [B, Ncap, D] bf16
+ * (batch stride c_bstride); n_valid: [B] int32, written.
+ * kI_new (optional): [B, DI] bf16 (LCC_KEY_BF16) or [B, DI/2] uint8 with
+ * kI_scale_new [B, DI/16] (LCC_KEY_NVFP4): the indexer key of the entry the
+ * token completes -- an input, like every indexer key (read only when a
+ * block completes); kI / kI_scale: the layer's key store [B, Ncap, ...].
+ * A position outside [raw_pos0, raw_pos0 + Rcap), a block whose first token
+ * is no longer in the raw buffer, or an entry j >= Ncap skips that sequence
+ * and sets the device error word (lcc_sync_status: LCC_ERR_DEVICE).
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_decode_append(int m, int B, int D,
+                             const lcc_bf16* k_new, const lcc_bf16* v_new, const float* g_new,
+                             const int64_t* pos,
+                             lcc_bf16* Kr, lcc_bf16* Vr, float* gate_r,
+                             int64_t r_bstride, int64_t g_bstride, int Rcap,
+                             const int64_t* raw_pos0,
+                             lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride, int Ncap,
+                             int32_t* n_valid,
+                             lcc_key_format fmt, int DI, const void* kI_new, const uint8_t* kI_scale_new,
+                             void* kI, uint8_t* kI_scale,
+                             void* stream);
 
 /* ---------------------------------------------------------------------- *
  * Lightning indexer + top-k.  [HYBRID]: a light indexer running in FP4
@@ -120,6 +195,25 @@ lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w,
                                     int32_t* idx, float* score,
                                     void* workspace, size_t workspace_bytes,
                                     void* stream);
+
+/* Re-index mode of CSA2 index sharing ([V41], the CSA2 passage: a full-mode
+ * layer keeps the notes -- the entries that matter -- and a re-index layer
+ * uses those notes as they are, adding its own marks for its own task).  For
+ * every query (b, i), only the candidate entries cand[b, i, :] (another
+ * layer's selection: ascending entry numbers, then -1 padding) are scored,
+ *   s = sum_h w[b,i,h] * max(0, qI[b,i,h,:] . kI[b,j,:]),
+ * and the k best (ties to the lower index) are written to idx[b, i, :] in
+ * ascending index order, padded with -1 when fewer than k candidates exist;
+ * score (optional) receives their scores (fp32, -inf for padding).
+ * Layouts and key formats as lcc_lightning_index_topk (the keys are the
+ * full-mode layer's); 1 <= k <= n_cand <= 1024.  A candidate >= Ncap sets
+ * the device error word and is skipped.  No workspace.
+ * The reuse mode needs no call: the layer passes the previous layer's idx to
+ * its attention (lcc_csa_layer_attn). */
+lcc_status lcc_lightning_reindex_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                                      lcc_key_format fmt, const void* kI, const uint8_t* kI_scale, int Ncap,
+                                      const int32_t* cand, int n_cand, int k,
+                                      int32_t* idx, float* score, void* stream);
 
 /* Indexer scores only: scores[b, i, j] = s for every visible entry j of
  * query (b, i) (entries past the visible count are left untouched).
@@ -285,6 +379,23 @@ const char* lcc_version(void);
 uint64_t lcc_launch_count(void);
 /* Synchronise `stream`, then report (and clear) the device error word. */
 lcc_status lcc_sync_status(void* stream);
+
+/* TEST HOOK (not part of the computation; no page describes it).  Every
+ * device-side wait of the tensor-core kernels is bounded; this lets a test
+ * make one run out without faulting or hanging anything.
+ *  wait_limit_ns: limit of every bounded wait on the current device; 0
+ *      restores the default of 2 s; values are clamped to [1 ms, 2 s], so a
+ *      kernel winding down still waits long enough for its own copies and
+ *      MMAs in flight.
+ *  drop_tile: >= 0 makes the decode indexer (lcc_lightning_index_scores and
+ *      the score pass of lcc_lightning_index_topk) skip loading the key tile
+ *      with that CTA-local number, so the waits for it run out: the call
+ *      then leaves its scores unspecified and lcc_sync_status() returns
+ *      LCC_ERR_TIMEOUT.  -1 restores normal operation.
+ * Synchronises the device first; call it only between steps, never while
+ * another thread is launching work.  Returns LCC_ERR_CUDA if the device
+ * cannot be reached. */
+lcc_status lcc_test_set_wait_fault(uint64_t wait_limit_ns, int drop_tile);
 
 #ifdef __cplusplus
 }

@@ -17,8 +17,8 @@ import os
 import torch
 
 __all__ = [
-    "LccError", "load", "csa_compress", "hca_compress", "lightning_index_topk", "lightning_index_scores",
-    "lightning_index_topk_noalloc",
+    "LccError", "load", "qkv_prologue", "csa_compress", "hca_compress", "compress", "decode_append", "lightning_index_topk", "lightning_index_scores",
+    "lightning_index_topk_noalloc", "lightning_reindex_topk",
     "index_topk_workspace", "csa_sparse_attn", "hca_dense_attn", "dense_attn_workspace",
     "swa_attn", "attn_merge", "csa_layer_attn", "hca_layer_attn", "layer_attn_workspace", "csa_layer",
     "csa_layer_workspace",
@@ -37,6 +37,11 @@ _P, _I, _L, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_flo
 _SIGS = {
     "lcc_csa_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
     "lcc_hca_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
+    "lcc_compress": [_I, _P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
+    "lcc_decode_append": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _L, _L, _I, _P, _P, _P, _L, _I, _P, _I, _I,
+                          _P, _P, _P, _P, _P],
+    "lcc_qkv_prologue": [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _I, _F, _P, _P, _P, _P, _P],
+    "lcc_lightning_reindex_topk": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _I, _P, _I, _I, _P, _P, _P],
     "lcc_index_topk_workspace": [_I, _I, _I, _I],
     "lcc_lightning_index_topk": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
     "lcc_lightning_index_topk_noalloc": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P],
@@ -58,6 +63,7 @@ _SIGS = {
     "lcc_version": [],
     "lcc_sync_status": [_P],
     "lcc_launch_count": [],
+    "lcc_test_set_wait_fault": [ctypes.c_uint64, _I],
 }
 _RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z, "lcc_csa_layer_workspace": _Z,
         "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p, "lcc_launch_count": ctypes.c_uint64}
@@ -141,9 +147,39 @@ def _positions(x, B, device, dtype=torch.int64):
 
 
 # ---------------------------------------------------------------------------
+# query / KV prologue
+# ---------------------------------------------------------------------------
+def qkv_prologue(q, k, v, gamma_q, gamma_k, gamma_v, pos0, d_rope=64, eps=1e-6, rope_base=10000.0,
+                 q_out=None, k_out=None, v_out=None, stream=None):
+    """RMSNorm of q [B, T, H, D], k and v [B, T, D] (bf16) with gains [D] fp32, then
+    rotary embedding of the last d_rope channels of q and k at positions pos0 + t.
+    v (with gamma_v) may be None.  Outputs default to new tensors; pass the inputs
+    to work in place.  Returns (q_out, k_out, v_out)."""
+    _need(q, torch.bfloat16, "q", 4)
+    _need(k, torch.bfloat16, "k", 3)
+    B, T, H, D = q.shape
+    for t, n in ((gamma_q, "gamma_q"), (gamma_k, "gamma_k")):
+        _need(t, torch.float32, n, 1)
+    if v is not None:
+        _need(v, torch.bfloat16, "v", 3)
+        _need(gamma_v, torch.float32, "gamma_v", 1)
+    if not (q.is_contiguous() and k.is_contiguous() and (v is None or v.is_contiguous())):
+        raise ValueError("q, k and v must be contiguous")
+    q_out = torch.empty_like(q) if q_out is None else q_out
+    k_out = torch.empty_like(k) if k_out is None else k_out
+    if v is not None and v_out is None:
+        v_out = torch.empty_like(v)
+    pos0 = _positions(pos0, B, q.device)
+    _call("lcc_qkv_prologue", _ptr(q), _ptr(k), _ptr(v), B, T, H, D, _ptr(gamma_q), _ptr(gamma_k), _ptr(gamma_v),
+          float(eps), int(d_rope), float(rope_base), _ptr(pos0), _ptr(q_out), _ptr(k_out), _ptr(v_out),
+          _stream(stream))
+    return q_out, k_out, v_out
+
+
+# ---------------------------------------------------------------------------
 # compression
 # ---------------------------------------------------------------------------
-def _compress(fname, m, K, V, gate, Kc, Vc, n_blocks, stream):
+def _compress(fname, m, K, V, gate, Kc, Vc, n_blocks, stream, pass_m=False):
     for t, n in ((K, "K"), (V, "V"), (Kc, "Kc"), (Vc, "Vc")):
         _need(t, torch.bfloat16, n, 3)
     _need(gate, torch.float32, "gate", 2)
@@ -157,8 +193,9 @@ def _compress(fname, m, K, V, gate, Kc, Vc, n_blocks, stream):
     n_blocks = R // m if n_blocks is None else int(n_blocks)
     if n_blocks > Kc.shape[1] or n_blocks * m > R:
         raise ValueError("n_blocks exceeds the input rows or the output entries")
-    _call(fname, _ptr(K), _ptr(V), _ptr(gate), B, n_blocks, D, kv_bs, gate.stride(0),
-          _ptr(Kc), _ptr(Vc), c_bs, _stream(stream))
+    args = (_ptr(K), _ptr(V), _ptr(gate), B, n_blocks, D, kv_bs, gate.stride(0), _ptr(Kc), _ptr(Vc), c_bs,
+            _stream(stream))
+    _call(fname, *(((int(m),) + args) if pass_m else args))
     return Kc, Vc
 
 
@@ -170,6 +207,57 @@ def csa_compress(K, V, gate, Kc, Vc, n_blocks=None, stream=None):
 def hca_compress(K, V, gate, Kc, Vc, n_blocks=None, stream=None):
     """Pool every 128 tokens of K/V [B, R, D] into entries of Kc/Vc [B, N, D]."""
     return _compress("lcc_hca_compress", 128, K, V, gate, Kc, Vc, n_blocks, stream)
+
+
+def compress(m, K, V, gate, Kc, Vc, n_blocks=None, stream=None):
+    """Pool every m in {1, 4, 128} tokens of K/V [B, R, D] into Kc/Vc [B, N, D] (m = 1: a copy)."""
+    return _compress("lcc_compress", m, K, V, gate, Kc, Vc, n_blocks, stream, pass_m=True)
+
+
+def decode_append(m, k_new, v_new, g_new, pos, Kr, Vr, gate_r, raw_pos0, Kc, Vc, n_valid,
+                  kI_new=None, kI=None, kI_scale_new=None, kI_scale=None, stream=None):
+    """One decode step of one layer's caches (lcc_decode_append).
+
+    The new tokens (k_new, v_new [B, D] bf16, g_new [B] fp32, at positions pos
+    [B] int64) go to raw row pos - raw_pos0 of Kr/Vr [B, Rcap, D] and gate_r
+    [B, Rcap]; a token that completes a block of m pools it into Kc/Vc
+    [B, Ncap, D], copies kI_new [B, DI] (bf16, or NVFP4 uint8 [B, DI/2] with
+    kI_scale_new [B, DI/16]) into kI/kI_scale and sets n_valid [B] (int32).
+    pos, raw_pos0 and n_valid must be device tensors for graph capture.
+    """
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _need(t, torch.bfloat16, n, 2)
+    _need(g_new, torch.float32, "g_new", 1)
+    for t, n in ((Kr, "Kr"), (Vr, "Vr"), (Kc, "Kc"), (Vc, "Vc")):
+        _need(t, torch.bfloat16, n, 3)
+    _need(gate_r, torch.float32, "gate_r", 2)
+    B, D = k_new.shape
+    if not (k_new.is_contiguous() and v_new.is_contiguous() and g_new.is_contiguous()):
+        raise ValueError("k_new, v_new and g_new must be contiguous")
+    r_bs, r_rs = _rows(Kr, "Kr")
+    c_bs, c_rs = _rows(Kc, "Kc")
+    if r_rs != D or Vr.stride() != Kr.stride() or c_rs != D or Vc.stride() != Kc.stride() or gate_r.stride(1) != 1:
+        raise ValueError("raw and compressed rows must be contiguous with identical K/V strides")
+    dev = k_new.device
+    pos = _positions(pos, B, dev)
+    raw_pos0 = _positions(raw_pos0, B, dev)
+    _need(n_valid, torch.int32, "n_valid", 1)
+    fmt, DI = KEY_BF16, 0
+    if kI_new is not None:
+        if kI is None:
+            raise ValueError("kI_new needs kI")
+        if kI_new.dtype == torch.uint8:
+            fmt, DI = KEY_NVFP4, kI_new.shape[1] * 2
+            if kI_scale_new is None or kI_scale is None:
+                raise ValueError("NVFP4 keys need kI_scale_new and kI_scale")
+        else:
+            _need(kI_new, torch.bfloat16, "kI_new", 2)
+            DI = kI_new.shape[1]
+        if not (kI_new.is_contiguous() and kI.is_contiguous()):
+            raise ValueError("kI_new and kI must be contiguous")
+    _call("lcc_decode_append", int(m), B, D, _ptr(k_new), _ptr(v_new), _ptr(g_new), _ptr(pos), _ptr(Kr), _ptr(Vr),
+          _ptr(gate_r), r_bs, gate_r.stride(0), Kr.shape[1], _ptr(raw_pos0), _ptr(Kc), _ptr(Vc), c_bs, Kc.shape[1],
+          _ptr(n_valid), fmt, DI, _ptr(kI_new), _ptr(kI_scale_new), _ptr(kI), _ptr(kI_scale), _stream(stream))
 
 
 # ---------------------------------------------------------------------------
@@ -238,6 +326,26 @@ def lightning_index_topk_noalloc(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None
         raise ValueError("q_pos0 and n_valid must be device tensors (nothing is allocated here)")
     _call("lcc_lightning_index_topk_noalloc", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
           _ptr(kI_scale), _ptr(n_valid), kI.shape[1], int(m), int(k), _ptr(idx), _ptr(score), _stream(stream))
+    return idx
+
+
+def lightning_reindex_topk(qI, w, kI, cand, k, kI_scale=None, idx=None, score=None, stream=None):
+    """CSA2 re-index mode: top-k of each query's candidate entries cand [B, Tq, n]
+    (another layer's selection) by this layer's indexer query qI / weights w and
+    the keys kI (bf16 [B, Ncap, DI], or NVFP4 uint8 with kI_scale).  Returns idx
+    [B, Tq, k] int32 in ascending index order (score [B, Tq, k] if given)."""
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    _need(cand, torch.int32, "cand", 3)
+    B, Tq, HI, DI = qI.shape
+    fmt = KEY_NVFP4 if kI.dtype == torch.uint8 else KEY_BF16
+    if not (qI.is_contiguous() and w.is_contiguous() and kI.is_contiguous() and cand.is_contiguous()):
+        raise ValueError("qI, w, kI and cand must be contiguous")
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=qI.device)
+    _need(idx, torch.int32, "idx", 3)
+    _call("lcc_lightning_reindex_topk", _ptr(qI), _ptr(w), B, Tq, HI, DI, fmt, _ptr(kI), _ptr(kI_scale),
+          kI.shape[1], _ptr(cand), cand.shape[2], int(k), _ptr(idx), _ptr(score), _stream(stream))
     return idx
 
 
@@ -447,6 +555,13 @@ def hca_layer_attn(q, Kc, Vc, n_valid, m, Kr, Vr, q_pos0, raw_pos0, W, scale=1.0
           Kc.shape[1], _ptr(n_valid), int(m), _ptr(Kr), _ptr(Vr), rr, Kr.shape[1], _ptr(raw_pos0), int(W),
           _ptr(out), _ptr(lse_out), _ptr(workspace), nbytes, _stream(stream))
     return out
+
+
+def test_set_wait_fault(wait_limit_ns=0, drop_tile=-1):
+    """Test hook: shorten every bounded device wait (0 = the default 2 s) and
+    make the decode indexer skip one key tile per CTA (-1 = none), so that a
+    test can make a wait run out.  See lcc_test_set_wait_fault in lcc.h."""
+    _call("lcc_test_set_wait_fault", int(wait_limit_ns), int(drop_tile))
 
 
 def sync_status(stream=None):

@@ -35,6 +35,8 @@ struct IndexTcArgs {
   uint32_t* gmax;   // optional [B * nq, g_stride]: key of the largest score of each 32-entry group
   int g_stride;
   int* counters;    // optional [2, B * nq]: zeroed here for the top-k kernel that follows
+  const uint8_t* kI_fp4;   // NVFP4 keys [B, Ncap, DI/2] (k_index_tc_fp4 only)
+  const uint8_t* kI_scale; // their e4m3 scales [B, Ncap, DI/16]
 };
 
 template <int HI, int DI, int NQ, int STAGES>
@@ -102,10 +104,12 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   }
   __syncthreads();
   const int row0 = b * a.Ncap + t_lo * C::TILE;
+  const int drop = warp == 0 && lane == 0 ? *static_cast<volatile int*>(&tc::g_test_drop_tile) : -1;
   if (warp == 0 && lane == 0) {
     // start streaming keys before the rest of the set-up
     tc::tma_prefetch_desc(&tmap_k);
     for (int t = 0; t < min(STAGES, ntiles); ++t) {
+      if (t == drop) continue;  // test hook: this tile's barrier never completes
       tc::mbar_arrive_expect_tx(full + t, C::A_BYTES);
       tc::tma_load_2d(sA + t * C::A_BYTES, &tmap_k, full + t, 0, row0 + t * C::TILE);
     }
@@ -152,13 +156,15 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
       for (int t = STAGES; t < ntiles; ++t) {
         const int s = t % STAGES;
         if (*s_abort || !tc::mbar_wait(empty + s, ((t / STAGES) & 1) ^ 1, 1)) { *s_abort = 1; break; }
+        issued = t + 1;
+        if (t == drop) continue;
         tc::mbar_arrive_expect_tx(full + s, C::A_BYTES);
         tc::tma_load_2d(sA + s * C::A_BYTES, &tmap_k, full + s, 0, row0 + t * C::TILE);
-        issued = t + 1;
       }
-      // copies still in flight must land before the CTA may exit
+      // copies still in flight must land before the CTA may exit (a dropped
+      // tile's wait runs out instead: nothing of it is in flight)
       for (int t = max(0, issued - STAGES); t < issued; ++t)
-        tc::mbar_wait(full + t % STAGES, (t / STAGES) & 1, 2);
+        if (t != drop) tc::mbar_wait(full + t % STAGES, (t / STAGES) & 1, 2);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -219,6 +225,293 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
               const uint32_t key = __reduce_max_sync(0xffffffffu, entry < vis ? f32_to_key(s) : 0u);
               const int g0 = entry - lane;
               if (lane == 0 && g0 < vis) a.gmax[r * a.g_stride + (g0 >> 5)] = key;
+            }
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(tempty + acc);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+
+// ---------------------------------------------------------------------------
+// NVFP4 keys on the tensor cores.  The keys stream as packed e2m1 pairs (32
+// bytes per entry) plus one e4m3 scale per 16 elements (4 bytes per entry):
+// 36 bytes instead of 128.  Roles (320 threads):
+//   warp 0      producer: bulk copies of 128-entry packed tiles (4 KB) into a
+//               ring of raw buffers;
+//   warp 1      TMEM allocation; one thread issues tcgen05.mma (kind::f16,
+//               fp16 operands) from a ring of converted buffers;
+//   warps 2..5  epilogue as k_index_tc; they also stage the indexer queries;
+//   warps 6..9  converters: one thread per entry of a tile expands its 64
+//               values to fp16 -- e2m1 -> fp16 (cvt) times the group's
+//               e4m3 scale (exact: the product has at most 6 significant
+//               bits and lies within fp16's normal range) -- into the
+//               128-byte-swizzled K-major layout of the MMA's A operand.
+// The indexer query is bf16, which fp16 cannot hold as it stands (8 exponent
+// bits against 5).  Each (query, head) row is multiplied by the power of two
+// that brings its largest element just under 2^15, which makes every element
+// within a factor 2^31 of that largest one exact in fp16, and the head weight
+// is multiplied by the inverse power: a power-of-two scale commutes with fp32
+// rounding, so ReLU(2^s q.k) * (2^-s w) equals ReLU(q.k) * w exactly.
+template <int DI>
+struct IndexTcFp4Cfg {
+  static constexpr int TILE = 128;
+  static constexpr int RAW_BYTES = TILE * DI / 2;       // packed tile
+  static constexpr int ROWB = DI * 2;                   // converted row (fp16)
+  static constexpr int A_BYTES = TILE * ROWB;
+};
+
+template <int HI, int DI, int NQ, int SR, int SC>
+struct IndexTcFp4Smem {
+  using F = IndexTcFp4Cfg<DI>;
+  using C = IndexTcCfg<HI, DI, NQ, 1>;
+  static constexpr int N = C::N;
+  static constexpr int OFF_A = 0;                                      // SC converted tiles
+  static constexpr int OFF_B = OFF_A + SC * F::A_BYTES;                // queries (fp16, scaled)
+  static constexpr int OFF_RAW = OFF_B + (C::B_BYTES + 1023) / 1024 * 1024;
+  static constexpr int OFF_W = OFF_RAW + SR * F::RAW_BYTES;
+  static constexpr int OFF_VIS = OFF_W + (NQ * HI * 4 + 15) / 16 * 16;
+  static constexpr int OFF_BAR = OFF_VIS + (NQ * 4 + 15) / 16 * 16;
+  static constexpr int NBAR = 2 * SR + 2 * SC + 4;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
+  static constexpr uint32_t IDESC = tc::idesc_f16(128, N, false);     // fp16 x fp16 -> fp32
+  static constexpr uint32_t SBO = 8 * F::ROWB;
+};
+
+template <int HI, int DI, int NQ, int SR, int SC>
+__global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
+  using F = IndexTcFp4Cfg<DI>;
+  using S = IndexTcFp4Smem<HI, DI, NQ, SR, SC>;
+  using C = IndexTcCfg<HI, DI, NQ, 1>;
+  static_assert(DI == 64, "NVFP4 keys: DI = 64 (one 128-byte swizzle row per converted entry)");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem + S::OFF_A;
+  uint8_t* sB = smem + S::OFF_B;
+  uint8_t* sRaw = smem + S::OFF_RAW;
+  float* sW = reinterpret_cast<float*>(smem + S::OFF_W);
+  int* sVis = reinterpret_cast<int*>(smem + S::OFF_VIS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::OFF_BAR);
+  uint64_t* rfull = bars;                    // [SR] packed tile landed
+  uint64_t* rempty = bars + SR;              // [SR] packed tile read by the converters
+  uint64_t* cfull = bars + 2 * SR;           // [SC] converted tile written
+  uint64_t* cempty = bars + 2 * SR + SC;     // [SC] converted tile consumed by the MMA
+  uint64_t* tfull = bars + 2 * SR + 2 * SC;  // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;              // [2] accumulator drained
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + S::NBAR);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
+
+  pdl_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.z;
+  const int qg0 = a.q0 + blockIdx.y * NQ;
+  const int qend = min(qg0 + NQ, a.q0 + a.nq);
+  const int64_t pos0 = __ldg(a.q_pos0 + b);
+  const int nval = __ldg(a.n_valid + b);
+  const int vis_max = visible_entries(pos0 + qend - 1, a.m, nval, a.Ncap);
+  const int ntiles_vis = (vis_max + F::TILE - 1) / F::TILE;
+  const int t_lo = blockIdx.x * a.tiles_per_split;
+  const int t_hi = min(t_lo + a.tiles_per_split, ntiles_vis);
+  if (t_lo >= t_hi) return;  // uniform across the CTA
+  const int ntiles = t_hi - t_lo;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SR; ++i) { tc::mbar_init(rfull + i, 1); tc::mbar_init(rempty + i, 128); }
+    for (int i = 0; i < SC; ++i) { tc::mbar_init(cfull + i, 128); tc::mbar_init(cempty + i, 1); }
+    for (int i = 0; i < 2; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  const int64_t row_base = static_cast<int64_t>(b) * a.Ncap;   // entry row of this batch's entry 0
+  // rows of tile t (CTA-local), the last one possibly partial
+  auto tile_rows = [&](int t) { return min(F::TILE, a.Ncap - (t_lo + t) * F::TILE); };
+  auto issue = [&](int t) {
+    const int s = t % SR;
+    const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * (DI / 2);
+    tc::mbar_arrive_expect_tx(rfull + s, bytes);
+    const uint8_t* src = a.kI_fp4 + (row_base + static_cast<int64_t>(t_lo + t) * F::TILE) * (DI / 2);
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(sRaw + s * F::RAW_BYTES)), "l"(src), "r"(bytes), "r"(smem_u32(rfull + s))
+        : "memory");
+  };
+  if (warp == 0 && lane == 0)
+    for (int t = 0; t < min(SR, ntiles); ++t) issue(t);
+  if (warp == 1) tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+  if (warp >= 2 && warp < 6) {
+    // B operand: row n = (query n / HI, head n % HI), fp16 after a power-of-two
+    // scale, K-major, swizzled like the converted tiles; head weight times the
+    // inverse scale
+    const int t = threadIdx.x - 64;
+    for (int n = t; n < C::N; n += 128) {
+      const int qq = qg0 + n / HI, hh = n % HI;
+      const bool live = n < C::NREAL && qq < qend;
+      uint4 v[DI / 8];
+      int emax = 0;
+#pragma unroll
+      for (int c = 0; c < DI / 8; ++c) {
+        v[c] = live ? __ldg(reinterpret_cast<const uint4*>(a.qI + ((static_cast<int64_t>(b) * a.Tq + qq) * HI + hh) *
+                                                                      DI) + c)
+                    : make_uint4(0, 0, 0, 0);
+        const uint32_t wd[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          emax = max(emax, static_cast<int>((wd[u] >> 7) & 0xFF));
+          emax = max(emax, static_cast<int>((wd[u] >> 23) & 0xFF));
+        }
+      }
+      // 2^sc brings the largest element to [2^14, 2^15)
+      const int sc = emax == 0 ? 0 : 141 - emax;
+      const float up = ldexpf(1.0f, sc);
+#pragma unroll
+      for (int c = 0; c < DI / 8; ++c) {
+        const uint32_t wd[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wd[u]));
+          __half2 h = __floats2half2_rn(f.x * up, f.y * up);
+          o[u] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        const int sw = c ^ (n & 7);
+        *reinterpret_cast<uint4*>(sB + (n >> 3) * S::SBO + (n & 7) * F::ROWB + sw * 16) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      if (n < NQ * HI)
+        sW[n] = live ? __ldg(a.w + (static_cast<int64_t>(b) * a.Tq + qq) * HI + hh) * ldexpf(1.0f, -sc) : 0.f;
+    }
+    for (int u = t; u < NQ; u += 128) {
+      const int qq = qg0 + u;
+      sVis[u] = qq < qend ? visible_entries(pos0 + qq, a.m, nval, a.Ncap) : 0;
+      if (a.counters && blockIdx.x == 0 && qq < qend) {
+        const int64_t r = static_cast<int64_t>(b) * a.nq + (qq - a.q0);
+        a.counters[r] = 0;
+        a.counters[static_cast<int64_t>(a.B) * a.nq + r] = 0;
+      }
+    }
+    tc::fence_proxy_async_smem();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  pdl_trigger();
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- producer
+    int issued = min(SR, ntiles);
+    if (lane == 0) {
+      for (int t = SR; t < ntiles; ++t) {
+        const int s = t % SR;
+        if (*s_abort || !tc::mbar_wait(rempty + s, ((t / SR) & 1) ^ 1, 11)) { *s_abort = 1; break; }
+        issue(t);
+        issued = t + 1;
+      }
+      for (int t = max(0, issued - SR); t < issued; ++t) tc::mbar_wait(rfull + t % SR, (t / SR) & 1, 12);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int c = t % SC, acc = t & 1;
+        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t >> 1) & 1) ^ 1, 13)) { *s_abort = 1; break; }
+        if (*s_abort || !tc::mbar_wait(cfull + c, (t / SC) & 1, 14)) { *s_abort = 1; break; }
+        tc::tc_fence_after();
+        const uint32_t d = tmem + acc * C::N;
+#pragma unroll
+        for (int k = 0; k < DI / 16; ++k) {
+          const uint64_t ad = tc::smem_desc(a_base + c * F::A_BYTES + k * 32, 16, S::SBO, tc::SW_128B);
+          const uint64_t bd = tc::smem_desc(b_base + k * 32, 16, S::SBO, tc::SW_128B);
+          tc::mma_f16_ss(d, ad, bd, S::IDESC, k > 0 ? 1u : 0u);
+        }
+        tc::mma_commit(cempty + c);
+        tc::mma_commit(tfull + acc);
+        issued = t + 1;
+      }
+      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 15);
+    }
+    __syncwarp();
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------- converters
+    const int r = threadIdx.x - 192;                // entry row within a tile
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % SR, c = t % SC;
+      const int64_t e = row_base + static_cast<int64_t>(t_lo + t) * F::TILE + r;
+      const bool live = r < tile_rows(t);
+      const uint32_t scales = live ? __ldg(reinterpret_cast<const uint32_t*>(a.kI_scale + e * (DI / 16))) : 0u;
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(rfull + s, (t / SR) & 1, 16))) { *s_abort = 1; break; }
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(cempty + c, ((t / SC) & 1) ^ 1, 17))) {
+        *s_abort = 1;
+        break;
+      }
+      uint4 p0 = make_uint4(0, 0, 0, 0), p1 = p0;
+      if (live) {
+        p0 = *reinterpret_cast<const uint4*>(sRaw + s * F::RAW_BYTES + r * (DI / 2));
+        p1 = *reinterpret_cast<const uint4*>(sRaw + s * F::RAW_BYTES + r * (DI / 2) + 16);
+      }
+      tc::mbar_arrive(rempty + s);
+      const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+      uint8_t* dst = sA + c * F::A_BYTES + (r >> 3) * S::SBO + (r & 7) * F::ROWB;
+#pragma unroll
+      for (int ch = 0; ch < DI / 8; ++ch) {       // 16-byte chunk = 8 elements = 2 packed words... 1 word
+        const uint32_t s2 = e4m3_to_f16x2_bcast(scales >> (8 * (ch >> 1)));
+        const uint32_t word = wd[ch];
+        uint4 o;
+        o.x = hmul2_u32(e2m1x2_to_f16x2(word), s2);
+        o.y = hmul2_u32(e2m1x2_to_f16x2(word >> 8), s2);
+        o.z = hmul2_u32(e2m1x2_to_f16x2(word >> 16), s2);
+        o.w = hmul2_u32(e2m1x2_to_f16x2(word >> 24), s2);
+        *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) * 16)) = o;
+      }
+      tc::fence_proxy_async_smem();   // generic writes -> visible to the tensor core
+      tc::mbar_arrive(cfull + c);
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int t = 0; t < ntiles; ++t) {
+      const int acc = t & 1;
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 18))) {
+        *s_abort = 1;
+        break;
+      }
+      tc::tc_fence_after();
+      const int entry = (t_lo + t) * F::TILE + quarter * 32 + lane;
+      constexpr int QPC = 8 / HI < 1 ? 1 : 8 / HI;
+      constexpr int NCH = (C::NREAL + 7) / 8;
+#pragma unroll 4
+      for (int ch = 0; ch < NCH; ++ch) {
+        float v[8];
+        tc::tmem_ld8(lane_addr + acc * C::N + ch * 8, v);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int qq = 0; qq < QPC; ++qq) {
+          const int qi = ch * QPC + qq;
+          const int q = qg0 + qi;
+          if (qi < NQ && q < qend) {
+            float sc = 0.f;
+#pragma unroll
+            for (int h = 0; h < HI; ++h) sc = fmaf(sW[qi * HI + h], fmaxf(v[qq * HI + h], 0.f), sc);
+            const int vis = sVis[qi];
+            const int64_t rr = static_cast<int64_t>(b) * a.nq + (q - a.q0);
+            if (entry < vis) a.scores[rr * a.Ncap + entry] = sc;
+            if (a.gmax) {
+              const uint32_t key = __reduce_max_sync(0xffffffffu, entry < vis ? f32_to_key(sc) : 0u);
+              const int g0 = entry - lane;
+              if (lane == 0 && g0 < vis) a.gmax[rr * a.g_stride + (g0 >> 5)] = key;
             }
           }
         }

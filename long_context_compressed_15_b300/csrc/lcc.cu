@@ -13,6 +13,11 @@
 #include "lcc.h"
 #include "common.cuh"
 #include "pool.cuh"
+#include "decode_step.cuh"
+#include "prologue.cuh"
+#include "reindex.cuh"
+#include <cmath>
+#include <type_traits>
 #include "merge.cuh"
 #include "attn.cuh"
 #include "attn_tc.cuh"
@@ -112,7 +117,8 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // ------------------------------------------------------------------ compress
 lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int nblk, int D,
                          int64_t kv_bs, int64_t g_bs, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bs, void* stream) {
-  const char* name = m == 4 ? "lcc_csa_compress" : "lcc_hca_compress";
+  const char* name = m == 4 ? "lcc_csa_compress" : m == 128 ? "lcc_hca_compress" : "lcc_compress";
+  if (m != 1 && m != 4 && m != 128) return fail(LCC_ERR_SHAPE, "%s: m=%d (supported: 1, 4, 128)", name, m);
   if (B < 0 || nblk < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d n_blocks=%d must be >= 0", name, B, nblk);
   if (B == 0 || nblk == 0) return LCC_OK;
   if (!K || !V || !gate || !Kc || !Vc) return fail(LCC_ERR_ARG, "%s: null pointer", name);
@@ -126,11 +132,17 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
   PoolArgs a{reinterpret_cast<const bf16*>(K), reinterpret_cast<const bf16*>(V), gate, B, nblk, kv_bs, g_bs,
              reinterpret_cast<bf16*>(Kc), reinterpret_cast<bf16*>(Vc), c_bs};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (m == 4) {
+  if (m <= 4) {
     const int bpw = 32 / (2 * (D / 8));
     dim3 grid((nblk + 8 * bpw - 1) / (8 * bpw), B);
-    if (D == 128) k_pool_small<4, 128><<<grid, 256, 0, s>>>(a);
-    else k_pool_small<4, 64><<<grid, 256, 0, s>>>(a);
+    if (grid.x > 0x7FFFFFFFu) return fail(LCC_ERR_SHAPE, "%s: too many blocks", name);
+    if (m == 4) {
+      if (D == 128) k_pool_small<4, 128><<<grid, 256, 0, s>>>(a);
+      else k_pool_small<4, 64><<<grid, 256, 0, s>>>(a);
+    } else {  // m = 1: every token is its own entry (softmax over one logit = 1)
+      if (D == 128) k_pool_small<1, 128><<<grid, 256, 0, s>>>(a);
+      else k_pool_small<1, 64><<<grid, 256, 0, s>>>(a);
+    }
   } else {
     dim3 grid(nblk, B);
     if (D == 128) k_pool_large<128, 128><<<grid, 256, 0, s>>>(a);
@@ -359,13 +371,34 @@ lcc_status lcc_sync_status(void* stream) {
   cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero));
   const unsigned int code = word >> 24, detail = word & 0xFFFFFFu;
   if (code == DEV_ERR_TIMEOUT) return fail(LCC_ERR_TIMEOUT, "device wait gave up (site %u)", detail);
+  if (code == DEV_ERR_RANGE)
+    return fail(LCC_ERR_DEVICE, "decode append: the new token of sequence %u falls outside its raw buffer, or the "
+                "block it completes outside the raw buffer or the caches", detail);
   return fail(LCC_ERR_DEVICE, "index list entry out of range at list position %u", detail);
+}
+
+lcc_status lcc_test_set_wait_fault(uint64_t wait_limit_ns, int drop_tile) {
+  unsigned long long lim = wait_limit_ns == 0 ? tc::kWaitLimitNs : static_cast<unsigned long long>(wait_limit_ns);
+  if (lim < 1000000ull) lim = 1000000ull;
+  if (lim > tc::kWaitLimitNs) lim = tc::kWaitLimitNs;
+  const int drop = drop_tile < 0 ? -1 : drop_tile;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_wait_limit_ns, &lim, sizeof(lim));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_test_drop_tile, &drop, sizeof(drop));
+  if (e != cudaSuccess) return fail(LCC_ERR_CUDA, "lcc_test_set_wait_fault: %s", cudaGetErrorString(e));
+  return LCC_OK;
 }
 
 lcc_status lcc_csa_compress(const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int n_blocks, int D,
                             int64_t kv_bstride, int64_t gate_bstride, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
                             void* stream) {
   return compress_impl(4, K, V, gate, B, n_blocks, D, kv_bstride, gate_bstride, Kc, Vc, c_bstride, stream);
+}
+
+lcc_status lcc_compress(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int n_blocks, int D,
+                        int64_t kv_bstride, int64_t gate_bstride, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
+                        void* stream) {
+  return compress_impl(m, K, V, gate, B, n_blocks, D, kv_bstride, gate_bstride, Kc, Vc, c_bstride, stream);
 }
 
 lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int n_blocks, int D,
@@ -375,6 +408,95 @@ lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* g
 }
 
 size_t lcc_index_topk_workspace(int B, int Tq, int Ncap, int k) { return index_ws(B, Tq, Ncap, k).total; }
+
+lcc_status lcc_qkv_prologue(const lcc_bf16* q, const lcc_bf16* k, const lcc_bf16* v, int B, int T, int H, int D,
+                            const float* gamma_q, const float* gamma_k, const float* gamma_v, float eps, int d_rope,
+                            float rope_base, const int64_t* pos0, lcc_bf16* q_out, lcc_bf16* k_out, lcc_bf16* v_out,
+                            void* stream) {
+  const char* name = "lcc_qkv_prologue";
+  if (B < 0 || T < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d T=%d must be >= 0", name, B, T);
+  if (B == 0 || T == 0) return LCC_OK;
+  if (!q || !k || !q_out || !k_out || !gamma_q || !gamma_k || !pos0) return fail(LCC_ERR_ARG, "%s: null pointer", name);
+  if ((v == nullptr) != (v_out == nullptr) || (v && !gamma_v))
+    return fail(LCC_ERR_ARG, "%s: v, v_out and gamma_v go together", name);
+  if (D != 64 && D != 128) return fail(LCC_ERR_SHAPE, "%s: D=%d (supported: 64, 128)", name, D);
+  if (H < 1 || H > 128) return fail(LCC_ERR_SHAPE, "%s: H=%d (supported: 1..128)", name, H);
+  if (d_rope < 0 || d_rope > D || (d_rope % 16))
+    return fail(LCC_ERR_SHAPE, "%s: d_rope=%d (a multiple of 16, at most D)", name, d_rope);
+  if (!(eps >= 0.f) || !(rope_base > 1.f) || !std::isfinite(rope_base))
+    return fail(LCC_ERR_ARG, "%s: eps must be >= 0 and rope_base > 1", name);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_out) || !aligned16(k_out) || (v && (!aligned16(v) ||
+      !aligned16(v_out))))
+    return fail(LCC_ERR_ALIGN, "%s: q, k, v and outputs must be 16-byte aligned", name);
+  const int64_t toks = static_cast<int64_t>(B) * T;
+  if (toks > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many tokens", name);
+  PrologueArgs a{};
+  a.q = reinterpret_cast<const bf16*>(q); a.k = reinterpret_cast<const bf16*>(k); a.v = reinterpret_cast<const bf16*>(v);
+  a.q_out = reinterpret_cast<bf16*>(q_out); a.k_out = reinterpret_cast<bf16*>(k_out);
+  a.v_out = reinterpret_cast<bf16*>(v_out);
+  a.gq = gamma_q; a.gk = gamma_k; a.gv = gamma_v; a.pos0 = pos0;
+  a.B = B; a.T = T; a.H = H; a.eps = eps; a.d_rope = d_rope; a.log2_base = std::log2(static_cast<double>(rope_base));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (D == 128) k_qkv_prologue<128><<<static_cast<unsigned>(toks), 256, 0, s>>>(a);
+  else k_qkv_prologue<64><<<static_cast<unsigned>(toks), 256, 0, s>>>(a);
+  return launch_check(name);
+}
+
+lcc_status lcc_decode_append(int m, int B, int D, const lcc_bf16* k_new, const lcc_bf16* v_new, const float* g_new,
+                             const int64_t* pos, lcc_bf16* Kr, lcc_bf16* Vr, float* gate_r, int64_t r_bstride,
+                             int64_t g_bstride, int Rcap, const int64_t* raw_pos0, lcc_bf16* Kc, lcc_bf16* Vc,
+                             int64_t c_bstride, int Ncap, int32_t* n_valid, lcc_key_format fmt, int DI,
+                             const void* kI_new, const uint8_t* kI_scale_new, void* kI, uint8_t* kI_scale,
+                             void* stream) {
+  const char* name = "lcc_decode_append";
+  if (B < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d", name, B);
+  if (B == 0) return LCC_OK;
+  if (m != 1 && m != 4 && m != 128) return fail(LCC_ERR_SHAPE, "%s: m=%d (supported: 1, 4, 128)", name, m);
+  if (D != 64 && D != 128) return fail(LCC_ERR_SHAPE, "%s: D=%d (supported: 64, 128)", name, D);
+  if (!k_new || !v_new || !g_new || !pos || !Kr || !Vr || !gate_r || !raw_pos0 || !Kc || !Vc || !n_valid)
+    return fail(LCC_ERR_ARG, "%s: null pointer", name);
+  if (Rcap < 1 || Ncap < 1) return fail(LCC_ERR_SHAPE, "%s: Rcap=%d Ncap=%d must be >= 1", name, Rcap, Ncap);
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(Kr) || !aligned16(Vr) || !aligned16(Kc) ||
+      !aligned16(Vc) || (r_bstride % 8) || (c_bstride % 8))
+    return fail(LCC_ERR_ALIGN, "%s: K/V buffers must be 16-byte aligned and batch strides multiples of 8", name);
+  if (B > 1 && (r_bstride < static_cast<int64_t>(Rcap) * D || c_bstride < static_cast<int64_t>(Ncap) * D ||
+                g_bstride < Rcap))
+    return fail(LCC_ERR_SHAPE, "%s: batch strides smaller than one batch's rows", name);
+  AppendArgs a{};
+  a.k_new = reinterpret_cast<const bf16*>(k_new); a.v_new = reinterpret_cast<const bf16*>(v_new); a.g_new = g_new;
+  a.pos = pos; a.raw_pos0 = raw_pos0;
+  a.Kr = reinterpret_cast<bf16*>(Kr); a.Vr = reinterpret_cast<bf16*>(Vr); a.gate_r = gate_r;
+  a.r_bs = r_bstride; a.g_bs = g_bstride; a.Rcap = Rcap;
+  a.Kc = reinterpret_cast<bf16*>(Kc); a.Vc = reinterpret_cast<bf16*>(Vc); a.c_bs = c_bstride; a.Ncap = Ncap;
+  a.n_valid = n_valid;
+  if (kI_new) {
+    if (!kI) return fail(LCC_ERR_ARG, "%s: kI_new given without kI", name);
+    if (fmt == LCC_KEY_BF16) {
+      if (DI != 32 && DI != 64) return fail(LCC_ERR_SHAPE, "%s: DI=%d (bf16 keys: 32, 64)", name, DI);
+      a.kI_bytes = DI * 2;
+    } else if (fmt == LCC_KEY_NVFP4) {
+      if (DI != 64) return fail(LCC_ERR_SHAPE, "%s: DI=%d (NVFP4 keys: 64)", name, DI);
+      if (!kI_scale_new || !kI_scale) return fail(LCC_ERR_ARG, "%s: NVFP4 keys need their scales", name);
+      a.kI_bytes = DI / 2;
+      a.kIs_new = kI_scale_new; a.kIs = kI_scale; a.kIs_bytes = DI / 16;
+    } else {
+      return fail(LCC_ERR_ARG, "%s: unknown key format %d", name, fmt);
+    }
+    a.kI_new = static_cast<const uint8_t*>(kI_new);
+    a.kI = static_cast<uint8_t*>(kI);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dim3 grid(static_cast<unsigned>(B));
+  if (m == 1) {
+    if (D == 128) k_decode_append<1, 128><<<grid, 256, 0, s>>>(a); else k_decode_append<1, 64><<<grid, 256, 0, s>>>(a);
+  } else if (m == 4) {
+    if (D == 128) k_decode_append<4, 128><<<grid, 256, 0, s>>>(a); else k_decode_append<4, 64><<<grid, 256, 0, s>>>(a);
+  } else {
+    if (D == 128) k_decode_append<128, 128><<<grid, 256, 0, s>>>(a);
+    else k_decode_append<128, 64><<<grid, 256, 0, s>>>(a);
+  }
+  return launch_check(name);
+}
 
 }  // extern "C"
 
@@ -493,6 +615,56 @@ lcc_status lcc_lightning_index_scores(const lcc_bf16* qI, const float* w, int B,
   IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, 0, Tq, scores,
                nullptr, 0, nullptr};
   return launch_scores(ia, HI, DI, fmt, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+namespace {
+template <int HI, int DI, bool FP4, int CAP>
+lcc_status launch_reindex(const ReindexArgs& a, cudaStream_t s) {
+  constexpr int NT = 128;
+  k_reindex_topk<HI, DI, FP4, NT, CAP><<<static_cast<unsigned>(static_cast<int64_t>(a.B) * a.Tq), NT, 0, s>>>(a);
+  return launch_check("k_reindex_topk");
+}
+template <int HI, int DI, bool FP4>
+lcc_status launch_reindex_cap(const ReindexArgs& a, cudaStream_t s) {
+  if (a.n_cand <= 256) return launch_reindex<HI, DI, FP4, 256>(a, s);
+  if (a.n_cand <= 512) return launch_reindex<HI, DI, FP4, 512>(a, s);
+  return launch_reindex<HI, DI, FP4, 1024>(a, s);
+}
+}  // namespace
+
+extern "C" {
+
+lcc_status lcc_lightning_reindex_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                                      lcc_key_format fmt, const void* kI, const uint8_t* kI_scale, int Ncap,
+                                      const int32_t* cand, int n_cand, int k, int32_t* idx, float* score,
+                                      void* stream) {
+  const char* name = "lcc_lightning_reindex_topk";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d Tq=%d must be >= 0", name, B, Tq);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  if (!qI || !w || !kI || !cand || !idx) return fail(LCC_ERR_ARG, "%s: null pointer", name);
+  if (fmt != LCC_KEY_BF16 && fmt != LCC_KEY_NVFP4) return fail(LCC_ERR_ARG, "%s: unknown key format %d", name, fmt);
+  if (fmt == LCC_KEY_NVFP4 && !kI_scale) return fail(LCC_ERR_ARG, "%s: NVFP4 keys need kI_scale", name);
+  if (HI != 4 && HI != 8) return fail(LCC_ERR_SHAPE, "%s: HI=%d (supported: 4, 8)", name, HI);
+  if (fmt == LCC_KEY_BF16 && DI != 32 && DI != 64) return fail(LCC_ERR_SHAPE, "%s: DI=%d (bf16: 32, 64)", name, DI);
+  if (fmt == LCC_KEY_NVFP4 && (DI != 64 || HI != 8))
+    return fail(LCC_ERR_SHAPE, "%s: HI=%d DI=%d (NVFP4 keys: HI=8, DI=64)", name, HI, DI);
+  if (Ncap < 1) return fail(LCC_ERR_SHAPE, "%s: Ncap=%d", name, Ncap);
+  if (n_cand < 1 || n_cand > 1024 || k < 1 || k > n_cand)
+    return fail(LCC_ERR_SHAPE, "%s: n_cand=%d k=%d (1 <= k <= n_cand <= 1024)", name, n_cand, k);
+  if (static_cast<int64_t>(B) * Tq > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many queries", name);
+  if (!aligned16(kI) || !aligned16(qI)) return fail(LCC_ERR_ALIGN, "%s: qI and kI must be 16-byte aligned", name);
+  ReindexArgs a{};
+  a.qI = reinterpret_cast<const bf16*>(qI); a.w = w; a.B = B; a.Tq = Tq;
+  a.kI = kI; a.kIs = kI_scale; a.Ncap = Ncap; a.cand = cand; a.n_cand = n_cand; a.k = k;
+  a.idx = idx; a.score = score;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fmt == LCC_KEY_NVFP4) return launch_reindex_cap<8, 64, true>(a, s);
+  if (HI == 8 && DI == 64) return launch_reindex_cap<8, 64, false>(a, s);
+  if (HI == 8 && DI == 32) return launch_reindex_cap<8, 32, false>(a, s);
+  if (HI == 4 && DI == 64) return launch_reindex_cap<4, 64, false>(a, s);
+  return launch_reindex_cap<4, 32, false>(a, s);
 }
 
 lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,

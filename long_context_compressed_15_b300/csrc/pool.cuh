@@ -32,6 +32,19 @@ __device__ __forceinline__ void fma8(float (&acc)[8], float a, uint4 v) {
   }
 }
 
+// 16-byte load: through the read-only path (RO) when nothing the kernel
+// writes can alias the source, else a plain coherent load.
+template <bool RO>
+__device__ __forceinline__ uint4 ld16(const bf16* p) {
+  if constexpr (RO) return __ldg(reinterpret_cast<const uint4*>(p));
+  else return *reinterpret_cast<const uint4*>(p);
+}
+template <bool RO>
+__device__ __forceinline__ float ldf(const float* p) {
+  if constexpr (RO) return __ldg(p);
+  else return *p;
+}
+
 __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
   uint4 o;
   o.x = pack_bf16(acc[0], acc[1]);
@@ -41,95 +54,119 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
   return o;
 }
 
-// Small blocks (m <= 16): each (half-)warp pools one block.  Lanes
-// [0, D/8) read K rows, lanes [D/8, D/4) read V rows, 16 bytes per lane.
-template <int M, int D>
-__global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
-  constexpr int LPR = D / 8;          // lanes per row (16-byte chunks)
-  constexpr int LPB = 2 * LPR;        // lanes per block (K and V)
-  constexpr int BPW = 32 / LPB;       // blocks per warp
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / LPB, isV = (lane / LPR) & 1, col = (lane % LPR) * 8;
-  const int b = blockIdx.y;
-  const int64_t blk = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * BPW + sub;
-  if (blk >= a.nblk) return;
-  const float* g = a.gate + b * a.g_bs + blk * M;
+// Pool one block of M <= 16 tokens with the lanes [sub*LPB, sub*LPB + LPB)
+// of a warp: lanes [0, D/8) of the group read K rows, lanes [D/8, D/4) V
+// rows, 16 bytes per lane.  g: the block's M gate logits; K/V: its first
+// token row; Kc/Vc: the entry.
+template <int M, int D, bool RO>
+__device__ __forceinline__ void pool_block_small(const float* g, const bf16* K, const bf16* V, bf16* Kc, bf16* Vc,
+                                                 int lane_in_group) {
+  constexpr int LPR = D / 8;
+  const int isV = lane_in_group / LPR, col = (lane_in_group % LPR) * 8;
   float gv[M];
   float mx = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < M; ++i) { gv[i] = __ldg(g + i); mx = fmaxf(mx, gv[i]); }
+  for (int i = 0; i < M; ++i) { gv[i] = ldf<RO>(g + i); mx = fmaxf(mx, gv[i]); }
   float sum = 0.f;
 #pragma unroll
   for (int i = 0; i < M; ++i) { gv[i] = expf(gv[i] - mx); sum += gv[i]; }
   const float inv = 1.0f / sum;
-  const bf16* src = (isV ? a.V : a.K) + b * a.kv_bs + blk * M * D + col;
+  const bf16* src = (isV ? V : K) + col;
   uint4 v[M];
 #pragma unroll
-  for (int i = 0; i < M; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src + i * D));
+  for (int i = 0; i < M; ++i) v[i] = ld16<RO>(src + i * D);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
   for (int i = 0; i < M; ++i) fma8(acc, gv[i] * inv, v[i]);
-  bf16* dst = (isV ? a.Vc : a.Kc) + b * a.c_bs + blk * D + col;
-  *reinterpret_cast<uint4*>(dst) = pack8(acc);
+  *reinterpret_cast<uint4*>((isV ? Vc : Kc) + col) = pack8(acc);
 }
 
-// Large blocks (m >= 32): one CTA of 256 threads per block.  Each warp
-// covers token slots with its K-half and V-half lanes; partial sums meet in
-// shared memory.
+// Small blocks (m <= 16): each (half-)warp pools one block.
 template <int M, int D>
-__global__ void __launch_bounds__(256) k_pool_large(PoolArgs a) {
+__global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
+  constexpr int LPB = 2 * (D / 8);    // lanes per block (K and V)
+  constexpr int BPW = 32 / LPB;       // blocks per warp
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / LPB;
+  const int b = blockIdx.y;
+  const int64_t blk = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * BPW + sub;
+  if (blk >= a.nblk) return;
+  pool_block_small<M, D, true>(a.gate + b * a.g_bs + blk * M, a.K + b * a.kv_bs + blk * M * D,
+                         a.V + b * a.kv_bs + blk * M * D, a.Kc + b * a.c_bs + blk * D, a.Vc + b * a.c_bs + blk * D,
+                         lane % LPB);
+}
+
+// Shared memory of pool_block_large.
+template <int M, int D>
+struct PoolLargeSmem {
+  static constexpr int SLOTS = 8 * (32 / (2 * (D / 8)));   // token slots per CTA
+  float g[M];
+  float stat[2];
+  float part[SLOTS][2 * D];
+};
+
+// Pool one block of M >= 32 tokens with a whole CTA of 256 threads.  Each
+// warp covers token slots with its K-half and V-half lanes; partial sums
+// meet in shared memory.  Every thread of the CTA must call it.
+template <int M, int D, bool RO>
+__device__ __forceinline__ void pool_block_large(const float* g, const bf16* K, const bf16* V, bf16* Kc, bf16* Vc,
+                                                 PoolLargeSmem<M, D>& sm) {
   constexpr int LPR = D / 8;
   constexpr int LPB = 2 * LPR;
   constexpr int SPW = 32 / LPB;       // token slots per warp
-  constexpr int SLOTS = 8 * SPW;      // token slots per CTA
+  constexpr int SLOTS = PoolLargeSmem<M, D>::SLOTS;
   static_assert(M % SLOTS == 0, "block size must be a multiple of the slot count");
-  __shared__ float s_g[M];
-  __shared__ float s_stat[2];
-  __shared__ float s_part[SLOTS][2 * D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int slot = warp * SPW + lane / LPB, isV = (lane / LPR) & 1, col = (lane % LPR) * 8;
-  const int b = blockIdx.y;
-  const int64_t blk = blockIdx.x;
-  const float* g = a.gate + b * a.g_bs + blk * M;
-  for (int i = threadIdx.x; i < M; i += 256) s_g[i] = __ldg(g + i);
+  for (int i = threadIdx.x; i < M; i += 256) sm.g[i] = ldf<RO>(g + i);
   __syncthreads();
   if (warp == 0) {
     float mx = -INFINITY;
-    for (int i = lane; i < M; i += 32) mx = fmaxf(mx, s_g[i]);
+    for (int i = lane; i < M; i += 32) mx = fmaxf(mx, sm.g[i]);
     mx = warp_max(mx);
     float sum = 0.f;
-    for (int i = lane; i < M; i += 32) sum += expf(s_g[i] - mx);
+    for (int i = lane; i < M; i += 32) sum += expf(sm.g[i] - mx);
     sum = warp_sum(sum);
-    if (lane == 0) { s_stat[0] = mx; s_stat[1] = 1.0f / sum; }
+    if (lane == 0) { sm.stat[0] = mx; sm.stat[1] = 1.0f / sum; }
   }
   __syncthreads();
-  const float mx = s_stat[0], inv = s_stat[1];
-  const bf16* src = (isV ? a.V : a.K) + b * a.kv_bs + blk * M * D + col;
+  const float mx = sm.stat[0], inv = sm.stat[1];
+  const bf16* src = (isV ? V : K) + col;
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   constexpr int PER = M / SLOTS;
   constexpr int UNR = PER < 8 ? PER : 8;
   for (int i0 = 0; i0 < PER; i0 += UNR) {
     uint4 v[UNR];
 #pragma unroll
-    for (int u = 0; u < UNR; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(src + ((i0 + u) * SLOTS + slot) * D));
+    for (int u = 0; u < UNR; ++u) v[u] = ld16<RO>(src + ((i0 + u) * SLOTS + slot) * D);
 #pragma unroll
     for (int u = 0; u < UNR; ++u) {
       const int tok = (i0 + u) * SLOTS + slot;
-      fma8(acc, expf(s_g[tok] - mx) * inv, v[u]);
+      fma8(acc, expf(sm.g[tok] - mx) * inv, v[u]);
     }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) s_part[slot][isV * D + col + e] = acc[e];
+  for (int e = 0; e < 8; ++e) sm.part[slot][isV * D + col + e] = acc[e];
   __syncthreads();
   for (int c = threadIdx.x; c < 2 * D / 8; c += 256) {
     float o[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     for (int s = 0; s < SLOTS; ++s)
 #pragma unroll
-      for (int e = 0; e < 8; ++e) o[e] += s_part[s][c * 8 + e];
+      for (int e = 0; e < 8; ++e) o[e] += sm.part[s][c * 8 + e];
     const int which = (c * 8) / D, cc = (c * 8) % D;
-    bf16* dst = (which ? a.Vc : a.Kc) + b * a.c_bs + blk * D + cc;
-    *reinterpret_cast<uint4*>(dst) = pack8(o);
+    *reinterpret_cast<uint4*>((which ? Vc : Kc) + cc) = pack8(o);
   }
+}
+
+// Large blocks (m >= 32): one CTA of 256 threads per block.
+template <int M, int D>
+__global__ void __launch_bounds__(256) k_pool_large(PoolArgs a) {
+  __shared__ PoolLargeSmem<M, D> sm;
+  const int b = blockIdx.y;
+  const int64_t blk = blockIdx.x;
+  pool_block_large<M, D, true>(a.gate + b * a.g_bs + blk * M, a.K + b * a.kv_bs + blk * M * D,
+                         a.V + b * a.kv_bs + blk * M * D, a.Kc + b * a.c_bs + blk * D, a.Vc + b * a.c_bs + blk * D,
+                         sm);
 }
 
 }  // namespace lcc

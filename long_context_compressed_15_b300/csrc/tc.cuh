@@ -11,9 +11,10 @@
 // 32-bit instruction descriptor holds the accumulator / operand types, the
 // operand majorness and N >> 3 (bits 17..22), M >> 4 (bits 24..28).
 //
-// Every wait is bounded: a wait that outlives kWaitLimitNs records
-// DEV_ERR_TIMEOUT in the device error word and reports failure so that the
-// caller can wind its pipeline down instead of spinning forever.
+// Every wait is bounded: a wait that outlives g_wait_limit_ns (2 s unless a
+// test shortens it) records DEV_ERR_TIMEOUT in the device error word and
+// reports failure so that the caller can wind its pipeline down instead of
+// spinning forever.
 #pragma once
 #include <cuda.h>
 #include "common.cuh"
@@ -22,6 +23,14 @@ namespace lcc {
 namespace tc {
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+// Limit every bounded wait uses.  Only the test hook changes it (to no less
+// than 1 ms, far above the microseconds an in-flight copy or MMA needs, so
+// that a wind-down still drains its own work).
+__device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+// Test hook: when >= 0, the decode indexer's producer skips the key tile with
+// this CTA-local number, leaving that tile's barrier one that nothing
+// completes, so the waits behind it run out.  -1 in normal operation.
+__device__ int g_test_drop_tile = -1;
 
 __device__ __forceinline__ unsigned long long globaltimer() {
   unsigned long long t;
@@ -62,9 +71,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned site) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
+  const unsigned long long limit = *static_cast<volatile unsigned long long*>(&g_wait_limit_ns);
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
+    if ((it & 15u) == 0 && globaltimer() - t0 > limit) {
       record_error(DEV_ERR_TIMEOUT, site);
       return false;
     }

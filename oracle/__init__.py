@@ -47,7 +47,18 @@ Readings where the pages are silent:
      W-1 raw tokens before it plus itself, and its blocks are pooled from raw
      row W-1 onward into entries ctx/m, ctx/m + 1, ...;
   R10 the 2048-token prefill pools its CSA and HCA entries from the same raw
-     K/V and gates.
+     K/V and gates;
+  R11 the query / KV prologue: RMSNorm (x / sqrt(mean(x^2) + eps) * gain)
+     over the head dimension of each query head and of the K and V rows,
+     then rotary embedding of the last d_rope channels of q and k (pairs
+     (c, c + d_rope/2), angle pos * base^(-2i/d_rope), base 10000); V is
+     not rotated;
+  R12 CSA2 index sharing: a full-mode layer keeps the n_notes best entries
+     by its own indexer score as the group's notes and attends to its own
+     top-k; a re-index layer scores only the notes, with its own indexer
+     query and weights against the same indexer keys, and attends to its
+     top-k among them; a reuse layer attends to the entries the layer before
+     it selected; each layer attends to its own compressed cache.
 
 Parity unpinned: the pages print no worked numeric example and no model
 dimensions, so the model-level figures (27% of V3.2's per-token FLOPs, ~10%
@@ -59,11 +70,13 @@ special cases in tests/test_oracle_pins.py.
 from .formats import (bf16_to_f64, f64_to_bf16_bits, round_bf16, e2m1_value,
                       e4m3_value, nvfp4_decode)
 from .method import (pool_weights, pool_exact, pool, visible_count, index_scores,
-                     topk_select, attend, window_positions, merge)
+                     topk_select, attend, window_positions, merge, rms_norm, rope_partial,
+                     qkv_prologue)
 from . import runs
 
 __all__ = [
     "bf16_to_f64", "f64_to_bf16_bits", "round_bf16", "e2m1_value", "e4m3_value",
     "nvfp4_decode", "pool_weights", "pool_exact", "pool", "visible_count",
-    "index_scores", "topk_select", "attend", "window_positions", "merge", "runs",
+    "index_scores", "topk_select", "attend", "window_positions", "merge", "rms_norm",
+    "rope_partial", "qkv_prologue", "runs",
 ]

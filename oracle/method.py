@@ -148,3 +148,51 @@ def merge(Os, lses):
     O = sum(wts[b][:, None] * np.asarray(Os[b], np.float64) for b in range(len(Os)))
     O = np.where(finite[:, None], O / np.where(tot > 0, tot, 1.0)[:, None], 0.0)
     return O, Lout
+
+
+# ---------------------------------------------------------------------------
+# query / KV prologue: RMS normalisation and partial rotary embedding
+# ---------------------------------------------------------------------------
+def rms_norm(x, gamma, eps):
+    """RMS normalisation of each row: x / sqrt(mean(x^2) + eps) * gamma.
+
+    [HYBRID]: both mechanisms apply query and KV normalisation.  Reading R11:
+    RMSNorm over the head dimension of every query head and of the shared K
+    and V rows, each tensor with its own per-channel gain.
+    x: [..., D]; gamma: [D].
+    """
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + float(eps)) * np.asarray(gamma, np.float64)
+
+
+def rope_partial(x, pos, d_rope, base=10000.0):
+    """Rotary position embedding on the last d_rope channels of each row.
+
+    [HYBRID]: both mechanisms use partial RoPE.  Reading R11: channels
+    D-d_rope .. D-1 form d_rope/2 pairs (c, c + d_rope/2) (the "rotate half"
+    pairing); pair i is rotated by the angle pos * base^(-2i/d_rope); the
+    first D-d_rope channels are left as they are.
+    x: [..., D] (rows of one position pos).
+    """
+    x = np.array(x, np.float64)
+    D = x.shape[-1]
+    h = d_rope // 2
+    i = np.arange(h, dtype=np.float64)
+    ang = float(pos) * np.power(float(base), -2.0 * i / d_rope)
+    c, s = np.cos(ang), np.sin(ang)
+    x1 = x[..., D - d_rope:D - h].copy()
+    x2 = x[..., D - h:].copy()
+    x[..., D - d_rope:D - h] = x1 * c - x2 * s
+    x[..., D - h:] = x2 * c + x1 * s
+    return x
+
+
+def qkv_prologue(q, k, v, pos, gq, gk, gv, eps, d_rope, base=10000.0):
+    """The prologue of the path for one position: q heads and k normalised then
+    rotated, v normalised only (RoPE encodes positions in scores, not values).
+    q: [H, D], k, v: [D] -> (q, k, v) in float64 (unrounded)."""
+    qn = rope_partial(rms_norm(q, gq, eps), pos, d_rope, base)
+    kn = rope_partial(rms_norm(k, gk, eps), pos, d_rope, base)
+    vn = rms_norm(v, gv, eps)
+    return qn, kn, vn

@@ -213,3 +213,94 @@ def pair_decode(inp, cfg, steps=None, batches=None, kI=None, kc_rows=None):
                                new_entries={j: (new_K[j], new_V[j]) for j in new_K},
                                new_entries_h={j: (new_Kh[j], new_Vh[j]) for j in new_Kh})
     return out
+
+
+def swa_replay(inp, cfg, R, batches=None):
+    """SWA bounded replay of a CSA/HCA layer pair ([V41], the SWA Bounded
+    Replay passage): after the local 128-token window state of a paused
+    session has been dropped, the compressed (global) caches are kept and
+    only the last R input tokens -- positions ctx-R .. ctx-1 -- are replayed
+    to rebuild the current state, instead of recomputing the whole prompt.
+
+    Reading: the replay is an R-token prefill chunk of each layer against its
+    kept caches; the rebuilt raw buffer holds only the replayed tokens
+    (raw_pos0 = ctx - R), so replayed query i sees a window of min(i+1, W)
+    tokens, and the last replayed query (position ctx-1) sees its full window
+    when R >= W.  Entries are visible by reading R2 against the kept caches.
+
+    inp: the layer-pair decode inputs (PairDecode recipe layout); the replayed
+    tokens' raw K/V are raw rows W-R .. W-1 of each layer's buffer and the
+    replayed queries are rq/rqI/rw [R, B, ...].  Returns {(i, b): dict(csa=
+    (O, lse), hca=(O, lse), idx, scores, kth)}.
+    """
+    batches = range(cfg.B) if batches is None else batches
+    out = {}
+    r0 = cfg.W - R                        # first replayed row of the raw buffers
+    pos0 = cfg.ctx - R
+    for b in batches:
+        kIb = nvfp4_decode(inp["kI_packed"][b], inp["kI_scale"][b])
+        Kr, Vr = f64(inp["Kr"][b])[r0:cfg.W], f64(inp["Vr"][b])[r0:cfg.W]
+        Kr_h, Vr_h = f64(inp["Kr_h"][b])[r0:cfg.W], f64(inp["Vr_h"][b])[r0:cfg.W]
+        Kc, Vc = f64(inp["Kc"][b]), f64(inp["Vc"][b])
+        Kc_h, Vc_h = f64(inp["Kc_h"][b]), f64(inp["Vc_h"][b])
+        for i in range(R):
+            t = pos0 + i
+            q, qI, w = f64(inp["rq"][i, b]), f64(inp["rqI"][i, b]), f64(inp["rw"][i, b])
+            c = csa_branch(q, t, qI, w, kIb, Kc, Vc, cfg.m_csa, cfg.k, n_valid=cfg.N_csa)
+            sw = swa_branch(q, t, Kr, Vr, pos0, cfg.W)
+            h = hca_branch(q, t, Kc_h, Vc_h, cfg.m_hca, n_valid=cfg.N_hca)
+            swh = swa_branch(q, t, Kr_h, Vr_h, pos0, cfg.W)
+            out[(i, b)] = dict(idx=c["idx"], scores=c["scores"], kth=c["kth"], window=sw["n_keys"],
+                               csa=merge([c["O"], sw["O"]], [c["lse"], sw["lse"]]),
+                               hca=merge([h["O"], swh["O"]], [h["lse"], swh["lse"]]))
+    return out
+
+
+def csa2_group(q_t, t, layers, kI, m, k, n_notes, n_valid=None):
+    """CSA2 index sharing across a group of CSA layers for one query ([V41], the
+    CSA2 passage: the first layer works in full mode -- reads the context,
+    highlights what matters and keeps the notes; a re-index layer takes those
+    notes as they are and adds its own marks for its own task; a reuse layer
+    copies the previous layer's result as it is).
+
+    Reading R12: a full layer scores every visible entry with its own indexer
+    query and weights against the indexer keys kI (the notes' keys), keeps the
+    n_notes best as the group's notes and attends to its own top-k (the k best
+    of the same scores); a re-index layer scores only the notes with its own
+    indexer query and weights against the same keys and attends to its top-k
+    among them; a reuse layer attends to the entries the layer before it
+    selected.  Each layer attends to its own compressed cache (entry j covers
+    the same tokens in every layer).  Ties go to the lower index everywhere.
+
+    layers: list of dicts with mode ("full" | "reindex" | "reuse"), q [H, D],
+    and, for full / reindex, qI [HI, DI], w [HI]; and Kc, Vc [N, D] (fp64).
+    q_t is unused (each layer brings its own q); kept for a uniform signature.
+    Returns per layer dict(idx, scores (of the entries it scored), kth, O, lse).
+    """
+    nv = visible_count(t, m, len(kI) if n_valid is None else n_valid)
+    notes = None
+    prev = None
+    out = []
+    for L in layers:
+        if L["mode"] == "full":
+            s = index_scores(L["qI"], L["w"], kI[:nv])
+            notes, _ = topk_select(s, n_notes)
+            idx, kth = topk_select(s, k)
+            scored = s
+        elif L["mode"] == "reindex":
+            cand = notes[notes >= 0]
+            s_c = index_scores(L["qI"], L["w"], kI[cand])
+            pick, kth = topk_select(s_c, k)           # positions within the candidate list
+            sel = np.sort(cand[pick[pick >= 0]])
+            idx = np.full(k, -1, dtype=np.int64)
+            idx[:sel.size] = sel
+            scored = dict(zip(cand.tolist(), s_c.tolist()))
+        elif L["mode"] == "reuse":
+            idx, kth, scored = prev["idx"], prev["kth"], prev["scores"]
+        else:
+            raise ValueError(L["mode"])
+        sel = idx[idx >= 0]
+        O, lse = attend(L["q"], L["Kc"][sel], L["Vc"][sel])
+        prev = dict(idx=idx, scores=scored, kth=kth, O=O, lse=lse, notes=notes)
+        out.append(prev)
+    return out

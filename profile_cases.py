@@ -1,6 +1,6 @@
 """Small, fixed cases of single library calls, sized for a profiler capture.
 
-    python -m long_context_compressed_15_b300.profile_cases <case> [--queries Q]
+    python profile_cases.py <case> [--queries Q]
 
 Each case builds its inputs with the seeded workload generators (``datagen``),
 runs the call twice and synchronises (capture the first launch: ncu flushes
@@ -26,14 +26,15 @@ import sys
 
 import torch
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import datagen  # noqa: E402
 from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, T_KI, T_QI, T_W  # noqa: E402
 
-from . import csa_layer_attn, hca_layer_attn, lightning_index_scores, lightning_index_topk, load  # noqa: E402
+from long_context_compressed_15_b300 import (csa_layer_attn, hca_layer_attn, lightning_index_scores,  # noqa: E402
+                                             lightning_index_topk, load)
 
 
 def index_topk_prefill(dev, nq):

@@ -9,7 +9,7 @@ import datagen
 import long_context_compressed_15_b300 as lcc
 import oracle
 from oracle import runs
-from parity import assert_close, assert_lse_close, bits, check_topk_rows, host
+from parity import assert_close, assert_lse_close, bits, check_topk_rows, host, topk_set_ok
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,6 +50,19 @@ def test_compress_parity(m, D, R):
             assert np.mean(gv == st) > 0.99
         # entries past the last complete block are untouched
         assert torch.isnan(Kc[b, n:].float()).all()
+
+
+def test_compress_m1_is_a_copy():
+    # m = 1 (the DSA comparator's cache): every token is its own entry
+    B, R, D = 2, 77, 128
+    K = datagen.normal_bf16(14, 1, (B, R, D)).to(DEV)
+    V = datagen.normal_bf16(14, 2, (B, R, D)).to(DEV)
+    g = datagen.normal_f32(14, 3, (B, R)).to(DEV)
+    Kc = torch.full((B, R, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.full_like(Kc, float("nan"))
+    lcc.compress(1, K, V, g, Kc, Vc)
+    torch.cuda.synchronize()
+    assert torch.equal(Kc, K) and torch.equal(Vc, V)
 
 
 def test_compress_one_block_at_offset():
@@ -432,3 +445,226 @@ def test_index_topk_prefill_fused_zero_score_ties():
         vis = min(Ncap, (q0 + i + 1) // m)
         want = np.arange(min(vis, k))
         assert np.array_equal(g[i, :len(want)], want) and np.all(g[i, len(want):] == -1), f"row {i}"
+
+
+# ---------------------------------------------------------------------------
+# CSA2 re-index mode (lcc_lightning_reindex_topk)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("HI,DI,fp4,n_notes,k", [(8, 64, False, 512, 128), (4, 32, False, 300, 64),
+                                                 (8, 64, True, 1024, 128), (8, 64, False, 200, 200)])
+def test_reindex_topk_parity(HI, DI, fp4, n_notes, k):
+    B, Tq, N = 3, 4, 5000
+    qI0 = datagen.normal_bf16(17, 1, (B, Tq, HI, DI)).to(DEV)
+    w0 = datagen.uniform_f32(17, 2, (B, Tq, HI)).to(DEV)
+    qI1 = datagen.normal_bf16(17, 3, (B, Tq, HI, DI)).to(DEV)
+    w1 = datagen.uniform_f32(17, 4, (B, Tq, HI)).to(DEV)
+    if fp4:
+        kp, ks = datagen.nvfp4_normal(17, 5, B * N, DI)
+        kI, kIs = kp.reshape(B, N, DI // 2).to(DEV), ks.reshape(B, N, DI // 16).to(DEV)
+        keys = [oracle.nvfp4_decode(host(kI[b]), host(kIs[b])) for b in range(B)]
+    else:
+        kI, kIs = datagen.normal_bf16(17, 5, (B, N, DI)).to(DEV), None
+        keys = [f64(kI[b]) for b in range(B)]
+    # the full layer's notes: its n_notes best entries (the last query sees only 1200 entries)
+    pos = torch.tensor([4 * N - Tq, 4 * N - Tq, 4 * 1200 - Tq], dtype=torch.int64, device=DEV)
+    notes = lcc.lightning_index_topk(qI0, w0, pos, kI, N, 4, n_notes, kI_scale=kIs)
+    sc = torch.empty((B, Tq, k), dtype=torch.float32, device=DEV)
+    idx = lcc.lightning_reindex_topk(qI1, w1, kI, notes, k, kI_scale=kIs, score=sc)
+    lcc.sync_status()
+    gi, gn, gs = host(idx), host(notes), host(sc)
+    near = 0
+    for b in range(B):
+        for i in range(Tq):
+            cand = gn[b, i][gn[b, i] >= 0]
+            s_c = oracle.index_scores(f64(qI1[b, i]), host(w1[b, i]).astype(np.float64), keys[b][cand])
+            pick, kth = oracle.topk_select(s_c, k)
+            want = np.full(k, -1, dtype=np.int64)
+            want[:np.sum(pick >= 0)] = np.sort(cand[pick[pick >= 0]])
+            full = np.full(int(cand.max()) + 1 if cand.size else 1, -np.inf)
+            full[cand] = s_c                                  # scores by entry number for the tie rule
+            ok, exact = topk_set_ok(gi[b, i], want, full, kth, k)
+            assert ok, f"b={b} i={i}: re-index set differs"
+            near += not exact
+            got = gi[b, i][gi[b, i] >= 0]
+            np.testing.assert_allclose(gs[b, i][:got.size], full[got], rtol=2e-5, atol=2e-5)
+            assert np.all(gs[b, i][got.size:] == -np.inf)
+    assert near <= 1
+
+
+def test_reindex_topk_ties_and_short_lists():
+    # all-zero scores: every candidate ties, the lowest entry numbers win; a list
+    # shorter than k is kept whole and padded
+    B, Tq, N, HI, DI, k = 1, 2, 900, 8, 64, 16
+    qI = torch.zeros((B, Tq, HI, DI), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones((B, Tq, HI), dtype=torch.float32, device=DEV)
+    kI = datagen.normal_bf16(18, 1, (B, N, DI)).to(DEV)
+    cand = torch.full((B, Tq, 40), -1, dtype=torch.int32, device=DEV)
+    cand[0, 0, :40] = torch.arange(100, 900, 20, dtype=torch.int32)
+    cand[0, 1, :7] = torch.tensor([3, 9, 10, 500, 501, 502, 899], dtype=torch.int32)
+    idx = lcc.lightning_reindex_topk(qI, w, kI, cand, k)
+    lcc.sync_status()
+    assert idx[0, 0].tolist() == list(range(100, 100 + 20 * k, 20))
+    assert idx[0, 1].tolist() == [3, 9, 10, 500, 501, 502, 899] + [-1] * (k - 7)
+
+
+# ---------------------------------------------------------------------------
+# query / KV prologue (RMSNorm + partial RoPE)
+# ---------------------------------------------------------------------------
+def _within_one_ulp(gpu_bf16, exact, what):
+    """One bf16 ulp of the fp64 value, plus the fp32 arithmetic's own error on the
+    row's scale (a rotated channel can cancel to near zero)."""
+    g = f64(gpu_bf16)
+    ulp = np.ldexp(1.0, np.frexp(np.abs(exact))[1] - 8)
+    fp32 = 2.0 ** -20 * np.max(np.abs(exact), axis=-1, keepdims=True)
+    bad = np.abs(g - exact) > ulp + fp32
+    assert not bad.any(), f"{what}: {bad.sum()} elements more than one bf16 ulp from the fp64 value"
+
+
+@pytest.mark.parametrize("H,D,d_rope,with_v", [(64, 128, 64, True), (8, 64, 32, True), (5, 128, 128, False),
+                                                (16, 128, 0, True)])
+def test_qkv_prologue_parity(H, D, d_rope, with_v):
+    B, T = 2, 37
+    q = datagen.normal_bf16(15, 1, (B, T, H, D), 3.0)
+    k = datagen.normal_bf16(15, 2, (B, T, D))
+    v = datagen.normal_bf16(15, 3, (B, T, D), 0.5)
+    gq, gk, gv = (1.0 + 0.1 * datagen.normal_f32(15, 4 + i, (D,)) for i in range(3))
+    pos0 = torch.tensor([0, 1048576 - 5], dtype=torch.int64)
+    qo, ko, vo = lcc.qkv_prologue(q.to(DEV), k.to(DEV), v.to(DEV) if with_v else None, gq.to(DEV), gk.to(DEV),
+                                  gv.to(DEV) if with_v else None, pos0.to(DEV), d_rope=d_rope)
+    torch.cuda.synchronize()
+    qh, kh, vh = f64(q), f64(k), f64(v)
+    for b in range(B):
+        for t in range(T):
+            p = int(pos0[b]) + t
+            eq, ek, ev = oracle.qkv_prologue(qh[b, t], kh[b, t], vh[b, t], p, f64(gq), f64(gk), f64(gv), 1e-6,
+                                             d_rope)
+            _within_one_ulp(qo[b, t], eq, f"q b={b} t={t}")
+            _within_one_ulp(ko[b, t], ek, f"k b={b} t={t}")
+            if with_v:
+                _within_one_ulp(vo[b, t], ev, f"v b={b} t={t}")
+    assert vo is None or with_v
+
+
+def test_qkv_prologue_in_place():
+    B, T, H, D = 1, 300, 64, 128
+    q = datagen.normal_bf16(16, 1, (B, T, H, D)).to(DEV)
+    k = datagen.normal_bf16(16, 2, (B, T, D)).to(DEV)
+    g = torch.ones(D, dtype=torch.float32, device=DEV)
+    want = lcc.qkv_prologue(q, k, None, g, g, None, 1000)
+    lcc.qkv_prologue(q, k, None, g, g, None, 1000, q_out=q, k_out=k)
+    torch.cuda.synchronize()
+    assert torch.equal(q, want[0]) and torch.equal(k, want[1])
+
+
+# ---------------------------------------------------------------------------
+# decode-step update of a layer's caches (lcc_decode_append)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("m,D", [(4, 128), (4, 64), (128, 128), (1, 128)])
+def test_decode_append_parity(m, D):
+    # three sequences at different positions, raw buffers that begin with the
+    # context rows only; enough steps that every sequence completes blocks
+    B, W, steps, DI = 3, 8 if m < 128 else 130, 2 * m + 5, 64
+    R = W + steps
+    ctx = [m * 50, m * 50 + 1, m * 50 + m - 1]                 # block boundary, just past it, just before it
+    Kfull = datagen.normal_bf16(13, 1, (B, R, D))
+    Vfull = datagen.normal_bf16(13, 2, (B, R, D))
+    gfull = datagen.normal_f32(13, 3, (B, R))
+    kI_tok = datagen.normal_bf16(13, 4, (steps, B, DI))        # indexer key offered with each new token
+    Kr = torch.zeros((B, R, D), dtype=torch.bfloat16, device=DEV)
+    Vr = torch.zeros_like(Kr)
+    gr = torch.zeros((B, R), dtype=torch.float32, device=DEV)
+    Kr[:, :W], Vr[:, :W], gr[:, :W] = Kfull[:, :W].to(DEV), Vfull[:, :W].to(DEV), gfull[:, :W].to(DEV)
+    Ncap = max(ctx) // m + steps // m + 2
+    Kc = torch.full((B, Ncap, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.full_like(Kc, float("nan"))
+    kI = torch.zeros((B, Ncap, DI), dtype=torch.bfloat16, device=DEV)
+    n_valid = torch.tensor([c // m for c in ctx], dtype=torch.int32, device=DEV)
+    raw0 = torch.tensor([c - W for c in ctx], dtype=torch.int64, device=DEV)
+    pos = raw0 + W
+    for s in range(steps):
+        lcc.decode_append(m, Kfull[:, W + s].contiguous().to(DEV), Vfull[:, W + s].contiguous().to(DEV),
+                          gfull[:, W + s].contiguous().to(DEV), pos, Kr, Vr, gr, raw0, Kc, Vc, n_valid,
+                          kI_new=kI_tok[s].to(DEV), kI=kI)
+        pos += 1
+    lcc.sync_status()
+    # raw buffers now hold every token, bit for bit
+    assert torch.equal(Kr.cpu(), Kfull) and torch.equal(Vr.cpu(), Vfull) and torch.equal(gr.cpu(), gfull)
+    for b in range(B):
+        first = ctx[b] // m                                      # the block under way at ctx completes first
+        last = (ctx[b] + steps) // m                             # one past the last completed block
+        assert int(n_valid[b]) == last
+        # each completed block: the oracle's pooled entry over its raw rows
+        for j in range(first, last):
+            r0 = j * m - int(raw0[b])
+            ex_k, ex_v = oracle.pool_exact(f64(Kfull[b, r0:r0 + m]), f64(Vfull[b, r0:r0 + m]),
+                                           f64(gfull[b, r0:r0 + m]), m)
+            for gpu, ex in ((Kc[b, j], ex_k[0]), (Vc[b, j], ex_v[0])):
+                ulp = np.ldexp(1.0, np.frexp(np.abs(ex))[1] - 8)
+                assert np.all(np.abs(f64(gpu) - ex) <= ulp)
+            s_done = (j + 1) * m - 1 - ctx[b]                    # the step whose token completed block j
+            assert torch.equal(kI[b, j].cpu(), kI_tok[s_done, b])
+        assert torch.isnan(Kc[b, last:].float()).all() and torch.isnan(Kc[b, :first].float()).all()
+    # the pooled entries equal what the compression call writes for the same rows
+    for b in range(B):
+        r0 = (ctx[b] // m) * m - int(raw0[b])
+        n = (ctx[b] + steps) // m - ctx[b] // m
+        Kc2 = torch.empty((1, n, D), dtype=torch.bfloat16, device=DEV)
+        Vc2 = torch.empty_like(Kc2)
+        if m in (4, 128):
+            fn = lcc.csa_compress if m == 4 else lcc.hca_compress
+            fn(Kr[b:b + 1, r0:r0 + n * m], Vr[b:b + 1, r0:r0 + n * m], gr[b:b + 1, r0:r0 + n * m], Kc2, Vc2)
+            torch.cuda.synchronize()
+            assert torch.equal(Kc2[0], Kc[b, ctx[b] // m:ctx[b] // m + n])
+            assert torch.equal(Vc2[0], Vc[b, ctx[b] // m:ctx[b] // m + n])
+        else:  # m = 1: an entry is its token
+            assert torch.equal(Kc[b, ctx[b]:ctx[b] + n].cpu(), Kfull[b, r0:r0 + n])
+
+
+def test_decode_append_out_of_range_is_reported():
+    B, R, D, m = 2, 16, 128, 4
+    Kr = torch.zeros((B, R, D), dtype=torch.bfloat16, device=DEV)
+    Vr = torch.zeros_like(Kr)
+    gr = torch.zeros((B, R), dtype=torch.float32, device=DEV)
+    Kc = torch.zeros((B, 8, D), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.zeros_like(Kc)
+    n_valid = torch.zeros(B, dtype=torch.int32, device=DEV)
+    kn = torch.ones((B, D), dtype=torch.bfloat16, device=DEV)
+    gn = torch.zeros(B, dtype=torch.float32, device=DEV)
+    raw0 = torch.zeros(B, dtype=torch.int64, device=DEV)
+    pos = torch.tensor([3, R], dtype=torch.int64, device=DEV)   # sequence 1 is past its raw buffer
+    lcc.decode_append(m, kn, kn, gn, pos, Kr, Vr, gr, raw0, Kc, Vc, n_valid)
+    with pytest.raises(lcc.LccError) as e:
+        lcc.sync_status()
+    assert e.value.status == 7 and "decode append" in str(e.value)
+    assert int(n_valid[0]) == 1 and int(n_valid[1]) == 0       # sequence 0 still completed its block
+    assert torch.equal(Kr[0, 3].cpu(), kn[0].cpu()) and float(Kr[1].float().abs().sum()) == 0.0
+
+
+# ---------------------------------------------------------------------------
+# bounded device waits: a wait that nothing completes runs out, the kernel
+# winds down (drains its own copies and MMAs, frees TMEM) and the host reads
+# LCC_ERR_TIMEOUT; the context stays usable and the next call is correct
+# ---------------------------------------------------------------------------
+def test_bounded_wait_runs_out_and_context_survives():
+    B, N, HI, DI = 32, 16384, 8, 64          # 14 key-range splits of 10 tiles per sequence
+    qI = datagen.normal_bf16(61, 5, (B, 1, HI, DI)).to(DEV)
+    w = datagen.uniform_f32(61, 6, (B, 1, HI)).to(DEV)
+    kI = datagen.normal_bf16(61, 7, (B, N, DI)).to(DEV)
+    pos = torch.full((B,), 4 * N - 1, dtype=torch.int64, device=DEV)
+    nval = torch.full((B,), N, dtype=torch.int32, device=DEV)
+    ref = lcc.lightning_index_scores(qI, w, pos, kI, nval, 4)
+    lcc.sync_status()
+    try:
+        # 20 ms waits; every CTA skips its second key tile
+        lcc.test_set_wait_fault(20_000_000, 1)
+        lcc.lightning_index_scores(qI, w, pos, kI, nval, 4)
+        with pytest.raises(lcc.LccError) as e:
+            lcc.sync_status()
+        assert e.value.status == 6 and "gave up" in str(e.value)
+    finally:
+        lcc.test_set_wait_fault(0, -1)
+    again = lcc.lightning_index_scores(qI, w, pos, kI, nval, 4)
+    lcc.sync_status()
+    assert torch.equal(again, ref)
+    sc = oracle.index_scores(runs.f64(host(qI[0, 0])), host(w[0, 0]).astype(np.float64), runs.f64(host(kI[0])))
+    np.testing.assert_allclose(again[0, 0].cpu().numpy(), sc, rtol=1e-4, atol=1e-4)

@@ -16,7 +16,8 @@ import datagen
 import long_context_compressed_15_b300 as lcc
 import oracle
 from datagen import workloads as wl
-from long_context_compressed_15_b300.layers import CsaLayerPlan, HcaLayerPlan
+from long_context_compressed_15_b300.layers import (Csa2GroupPlan, CsaLayerPlan, HcaLayerPlan, PairDecodePlan,
+                                                    SwaReplayPlan)
 from oracle import runs
 from parity import assert_close, assert_lse_close, check_topk_rows, decoupled, host, selected, topk_set_ok
 
@@ -140,6 +141,42 @@ def test_csa_decode_full():
 
 
 # ---------------------------------------------------------------------------
+def test_dsa_decode_full():
+    """The DSA comparator (m = 1: the indexer scores all 65536 raw tokens) at full size."""
+    cfg = wl.DsaDecode()
+    g = cfg.make(DEV)
+    plan = CsaLayerPlan(cfg.B, 1, cfg.H, cfg.D, cfg.N, cfg.k, cfg.W, m=cfg.m)
+    out = plan(g["q"], g["qI"], g["w"], cfg.q_pos, g["kI"], cfg.N, g["Kc"], g["Vc"], g["Kr"], g["Vr"],
+               cfg.raw_pos0)
+    lcc.sync_status()
+    gi = plan.idx.cpu().numpy()[:, 0]
+    gout = out.float().cpu().numpy()[:, 0]
+    del g, out
+    s = cfg.seed
+    kI = f64(datagen.normal_bf16(s, wl.T_KI, (cfg.B, cfg.N, cfg.DI)))
+    qI = f64(datagen.normal_bf16(s, wl.T_QI, (cfg.B, 1, cfg.HI, cfg.DI)))
+    w = f64(datagen.uniform_f32(s, wl.T_W, (cfg.B, 1, cfg.HI)))
+    q = f64(datagen.normal_bf16(s, wl.T_Q, (cfg.B, 1, cfg.H, cfg.D), cfg.q_scale))
+    near = 0
+    for b in range(cfg.B):
+        sc = oracle.index_scores(qI[b, 0], w[b, 0], kI[b])
+        oi, kth = oracle.topk_select(sc, cfg.k)
+        ok, exact = topk_set_ok(gi[b], oi, sc, kth, cfg.k)
+        assert ok, f"batch {b}: top-k set differs"
+        near += not exact
+        rows = b * cfg.N + selected(gi[b])
+        Kc = regen_rows(s, wl.T_KC, rows, cfg.D)
+        Vc = regen_rows(s, wl.T_VC, rows, cfg.D)
+        win = b * cfg.N + np.arange(cfg.N - cfg.W, cfg.N)
+        Kr, Vr = regen_rows(s, wl.T_KC, win, cfg.D), regen_rows(s, wl.T_VC, win, cfg.D)
+        cO, cL = oracle.attend(q[b, 0], Kc, Vc)
+        sw = runs.swa_branch(q[b, 0], cfg.q_pos, Kr, Vr, cfg.raw_pos0, cfg.W)
+        O, _ = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
+        assert_close(gout[b], O, f"DSA decode batch {b}")
+    assert near <= 1
+
+
+# ---------------------------------------------------------------------------
 def _prefill_rows(T, extra, seed):
     rng = np.random.default_rng(seed)
     fixed = [0, 1, 2, 3, 4, 5, 7, 8, 126, 127, 128, 129, 255, 4095, 4096, 4097, T - 2, T - 1]
@@ -230,28 +267,47 @@ def test_hca_prefill_sampled_rows():
 
 # ---------------------------------------------------------------------------
 def test_pair_decode_64_steps():
+    """64 decode steps of the layer pair through PairDecodePlan: each step's
+    token is appended by the library (raw buffers start with the W context
+    rows only; blocks are pooled and counts advanced on the device)."""
     cfg = wl.PairDecode()
     g = cfg.make(DEV)
-    B, D = cfg.B, cfg.D
-    csa = CsaLayerPlan(B, 1, cfg.H, D, cfg.Ncap_csa, cfg.k, cfg.W)
-    hca = HcaLayerPlan(B, 1, cfg.H, D, cfg.N_hca, cfg.W)
-    n_valid = torch.full((B,), cfg.N_csa, dtype=torch.int32, device=DEV)
+    B, D, W = cfg.B, cfg.D, cfg.W
+    plan = PairDecodePlan(B, cfg.H, D, cfg.Ncap_csa, cfg.N_hca, cfg.k, W, device=DEV)
+
+    def context_only(t):
+        z = torch.zeros_like(t)
+        z[:, :W] = t[:, :W]
+        return z
+    kI = torch.zeros_like(g["kI_packed"])
+    kIs = torch.zeros_like(g["kI_scale"])
+    kI[:, :cfg.N_csa], kIs[:, :cfg.N_csa] = g["kI_packed"][:, :cfg.N_csa], g["kI_scale"][:, :cfg.N_csa]
+    raw0 = torch.full((B,), cfg.raw_pos0, dtype=torch.int64, device=DEV)
+    csa_c = dict(Kr=context_only(g["Kr"]), Vr=context_only(g["Vr"]), gate=context_only(g["gate"]), raw_pos0=raw0,
+                 Kc=g["Kc"], Vc=g["Vc"], n_valid=torch.full((B,), cfg.N_csa, dtype=torch.int32, device=DEV),
+                 kI=kI, kI_scale=kIs)
+    hca_c = dict(Kr=context_only(g["Kr_h"]), Vr=context_only(g["Vr_h"]), gate=context_only(g["gate_h"]),
+                 raw_pos0=raw0, Kc=g["Kc_h"], Vc=g["Vc_h"],
+                 n_valid=torch.full((B,), cfg.N_hca, dtype=torch.int32, device=DEV))
     outs_c, outs_h, idxs = [], [], []
     for s in range(cfg.steps):
-        pos = cfg.ctx + s
-        if (pos + 1) % cfg.m_csa == 0:
-            j = (pos + 1) // cfg.m_csa - 1
-            r1 = cfg.W + s + 1
-            lcc.csa_compress(g["Kr"][:, r1 - 4:r1], g["Vr"][:, r1 - 4:r1], g["gate"][:, r1 - 4:r1],
-                             g["Kc"][:, j:j + 1], g["Vc"][:, j:j + 1], n_blocks=1)
-            n_valid += 1
+        pos = torch.full((B,), cfg.ctx + s, dtype=torch.int64, device=DEV)
+        j = min((cfg.ctx + s + 1) // cfg.m_csa - 1, cfg.Ncap_csa - 1)   # entry this token would complete
+        r = W + s
+        new_c = dict(k=g["Kr"][:, r].contiguous(), v=g["Vr"][:, r].contiguous(), g=g["gate"][:, r].contiguous(),
+                     kI=g["kI_packed"][:, j].contiguous(), kI_scale=g["kI_scale"][:, j].contiguous())
+        new_h = dict(k=g["Kr_h"][:, r].contiguous(), v=g["Vr_h"][:, r].contiguous(), g=g["gate_h"][:, r].contiguous())
         q = g["q"][s][:, None]
-        oc = csa(q, g["qI"][s][:, None], g["w"][s][:, None], pos, g["kI_packed"], n_valid, g["Kc"], g["Vc"],
-                 g["Kr"], g["Vr"], cfg.raw_pos0, kI_scale=g["kI_scale"])
-        oh = hca(q, pos, g["Kc_h"], g["Vc_h"], cfg.N_hca, g["Kr_h"], g["Vr_h"], cfg.raw_pos0)
+        oc, oh = plan(pos, q, g["qI"][s][:, None], g["w"][s][:, None], new_c, new_h, csa_c, hca_c)
         outs_c.append(oc[:, 0].float().cpu().numpy())
         outs_h.append(oh[:, 0].float().cpu().numpy())
-        idxs.append(csa.idx[:, 0].cpu().numpy())
+        idxs.append(plan.csa.idx[:, 0].cpu().numpy())
+    lcc.sync_status()
+    # the appended caches hold every token and every new indexer key, bit for bit
+    for name, c, full in (("Kr", csa_c, g["Kr"]), ("gate", csa_c, g["gate"]), ("Vr_h", hca_c, g["Vr_h"])):
+        assert torch.equal(c[name.split("_")[0]], full), name
+    assert torch.equal(kI, g["kI_packed"]) and torch.equal(kIs, g["kI_scale"])
+    assert torch.all(csa_c["n_valid"] == cfg.Ncap_csa) and torch.all(hca_c["n_valid"] == cfg.N_hca)
     lcc.sync_status()
     gnew = f64(g["Kc"][:, cfg.N_csa:])
     del g
@@ -275,7 +331,7 @@ def test_pair_decode_64_steps():
         ref = runs.pair_decode(hb, cfg, batches=[0], kI=kI, kc_rows=kc_rows)
         for j, (kn, vn) in ref[(cfg.steps - 1, 0)]["new_entries"].items():
             assert np.max(np.abs(gnew[b, j - cfg.N_csa] - kn)) <= 2 ** -7 * max(1.0, np.max(np.abs(kn)))
-        Krb, Vrb = f64(hk["Kr"][b]), f64(hk["Vr"][b])
+        Krb, Vrb = runs.f64(hk["Kr"][b]), runs.f64(hk["Vr"][b])
         for s in range(cfg.steps):
             r = ref[(s, 0)]
             ok, exact = topk_set_ok(idxs[s][b], r["idx"], r["scores"], r["kth"], cfg.k)
@@ -289,9 +345,115 @@ def test_pair_decode_64_steps():
                 ne = ref[(cfg.steps - 1, 0)]["new_entries"]
                 Kn = np.array([ne[j][0] for j in new]).reshape(-1, D)
                 Vn = np.array([ne[j][1] for j in new]).reshape(-1, D)
-                sw = runs.swa_branch(f64(hk["q"][s, b]), cfg.ctx + s, Krb[:cfg.W + s + 1], Vrb[:cfg.W + s + 1],
-                                     cfg.raw_pos0, cfg.W)
-                want = decoupled(f64(hk["q"][s, b]), np.concatenate([Ko, Kn]), np.concatenate([Vo, Vn]), sw)[1][0]
+                qs = runs.f64(hk["q"][s, b])
+                sw = runs.swa_branch(qs, cfg.ctx + s, Krb[:cfg.W + s + 1], Vrb[:cfg.W + s + 1], cfg.raw_pos0, cfg.W)
+                want = decoupled(qs, np.concatenate([Ko, Kn]), np.concatenate([Vo, Vn]), sw)[1][0]
             assert_close(outs_c[s][b], want, f"CSA layer step {s} batch {b}")
             assert_close(outs_h[s][b], r["hca"][0], f"HCA layer step {s} batch {b}")
+    assert near <= 2
+
+
+
+# ---------------------------------------------------------------------------
+def test_swa_replay_pair_at_1m_context():
+    """SWA bounded replay of the layer pair: the last 128 context tokens replayed
+    against the kept 1M-token caches (262144 CSA entries with NVFP4 keys, 8192
+    HCA entries); the rebuilt raw buffers hold only the replayed tokens."""
+    cfg = wl.PairDecode()
+    R = cfg.W
+    g = cfg.make(DEV)
+    rp = cfg.make_replay(R, DEV)
+    B, W = cfg.B, cfg.W
+    pos0 = torch.full((B,), cfg.ctx - R, dtype=torch.int64, device=DEV)
+    csa_c = dict(Kr=g["Kr"][:, W - R:W].contiguous(), Vr=g["Vr"][:, W - R:W].contiguous(), Kc=g["Kc"], Vc=g["Vc"],
+                 n_valid=torch.full((B,), cfg.N_csa, dtype=torch.int32, device=DEV), kI=g["kI_packed"],
+                 kI_scale=g["kI_scale"])
+    hca_c = dict(Kr=g["Kr_h"][:, W - R:W].contiguous(), Vr=g["Vr_h"][:, W - R:W].contiguous(), Kc=g["Kc_h"],
+                 Vc=g["Vc_h"], n_valid=torch.full((B,), cfg.N_hca, dtype=torch.int32, device=DEV))
+    plan = SwaReplayPlan(B, R, cfg.H, cfg.D, cfg.Ncap_csa, cfg.N_hca, cfg.k, W, device=DEV)
+    q = rp["rq"].transpose(0, 1).contiguous()
+    qI = rp["rqI"].transpose(0, 1).contiguous()
+    w = rp["rw"].transpose(0, 1).contiguous()
+    oc, oh = plan(pos0, q, qI, w, csa_c, hca_c)
+    lcc.sync_status()
+    gi = plan.csa.idx.cpu().numpy()
+    goc, goh = oc.float().cpu().numpy(), oh.float().cpu().numpy()
+    batches = [0, 3]
+    inp = {k: host(v) for k, v in g.items() if k in ("Kr", "Vr", "Kr_h", "Vr_h", "Kc_h", "Vc_h", "kI_packed",
+                                                       "kI_scale")}
+    inp["Kc"], inp["Vc"] = host(g["Kc"][:, :cfg.N_csa]), host(g["Vc"][:, :cfg.N_csa])
+    inp.update({k: host(v) for k, v in rp.items()})
+    del g, oc, oh
+    ref = runs.swa_replay(inp, cfg, R, batches=batches)
+    near = 0
+    for b in batches:
+        Kc_all, Vc_all = runs.f64(inp["Kc"][b]), runs.f64(inp["Vc"][b])
+        for i in range(R):
+            r = ref[(i, b)]
+            ok, exact = topk_set_ok(gi[b, i], r["idx"], r["scores"], r["kth"], cfg.k)
+            assert ok, f"replayed row {i} batch {b}: top-k set differs"
+            near += not exact
+            want = r["csa"][0]
+            if not exact:
+                sel = selected(gi[b, i])
+                qi = runs.f64(inp["rq"][i, b])
+                t = cfg.ctx - R + i
+                sw = runs.swa_branch(qi, t, runs.f64(inp["Kr"][b][W - R:W]), runs.f64(inp["Vr"][b][W - R:W]),
+                                     cfg.ctx - R, W)
+                want = decoupled(qi, Kc_all[sel], Vc_all[sel], sw)[1][0]
+            assert_close(goc[b, i], want, f"CSA replay row {i} batch {b}")
+            assert_close(goh[b, i], r["hca"][0], f"HCA replay row {i} batch {b}")
+    assert near <= 3
+
+
+
+# ---------------------------------------------------------------------------
+def test_csa2_group_decode():
+    """CSA2 index sharing over three CSA layers (full, re-index, reuse) on the CSA
+    decode batch: 32 sequences x 16384 entries, 512 notes, top-128, window 128."""
+    cfg = wl.CsaDecode()
+    B, N, n_notes = cfg.B, cfg.N, 512
+    modes = ("full", "reindex", "reuse")
+    layers = [cfg.make(DEV, rot=r) for r in range(3)]           # each layer: its own caches and queries
+    kI = layers[0]["kI"]                                         # the full layer's indexer keys
+    plan = Csa2GroupPlan(modes, B, 1, cfg.H, cfg.D, N, cfg.k, cfg.W, n_notes, device=DEV)
+    outs = plan([L["q"] for L in layers], [L["qI"] for L in layers], [L["w"] for L in layers], cfg.q_pos, kI, N,
+                layers, cfg.raw_pos0)
+    lcc.sync_status()
+    g_notes, g_idx = host(plan.notes)[:, 0], [host(i)[:, 0] for i in plan.idx]
+    g_out = [o.float().cpu().numpy()[:, 0] for o in outs]
+    hl = [{k: host(v) for k, v in L.items()} for L in layers]
+    del layers, outs
+    kI_h = runs.f64(hl[0]["kI"])
+    near = 0
+    for b in range(B):
+        t = cfg.q_pos
+        full = runs.csa_branch(runs.f64(hl[0]["q"][b, 0]), t, runs.f64(hl[0]["qI"][b, 0]), hl[0]["w"][b, 0], kI_h[b],
+                               runs.f64(hl[0]["Kc"][b]), runs.f64(hl[0]["Vc"][b]), cfg.m, n_notes)
+        ok, _ = topk_set_ok(g_notes[b], full["idx"], full["scores"], full["kth"], n_notes)
+        assert ok, f"batch {b}: notes differ"
+        # the oracle's group over the GPU's notes (decoupled from near-ties at rank 512)
+        Lq = [dict(mode=mo, q=runs.f64(hl[l]["q"][b, 0]), qI=runs.f64(hl[l]["qI"][b, 0]),
+                   w=hl[l]["w"][b, 0].astype(np.float64), Kc=runs.f64(hl[l]["Kc"][b]), Vc=runs.f64(hl[l]["Vc"][b]))
+              for l, mo in enumerate(modes)]
+        notes = selected(g_notes[b])
+        for l in range(3):
+            if l == 0:   # the full layer's own top-k over every visible entry
+                r = runs.csa2_group(None, t, [Lq[0]], kI_h[b], cfg.m, cfg.k, n_notes)[0]
+                ok, exact = topk_set_ok(g_idx[0][b], r["idx"], full["scores"], r["kth"], cfg.k)
+            else:        # re-index (layer 1) over the GPU's notes; reuse (layer 2) copies layer 1
+                s_all = np.full(N, -np.inf)
+                s_c = oracle.index_scores(Lq[min(l, 1)]["qI"], Lq[min(l, 1)]["w"], kI_h[b][notes])
+                s_all[notes] = s_c
+                pick, kth = oracle.topk_select(s_c, cfg.k)
+                want = np.sort(notes[pick[pick >= 0]])
+                ok, exact = topk_set_ok(g_idx[l][b], want, s_all, kth, cfg.k)
+            assert ok, f"batch {b} layer {l}: selection differs"
+            near += not exact
+            sel = selected(g_idx[l][b])
+            sw = runs.swa_branch(Lq[l]["q"], t, runs.f64(hl[l]["Kr"][b]), runs.f64(hl[l]["Vr"][b]), cfg.raw_pos0,
+                                 cfg.W)
+            want_O = decoupled(Lq[l]["q"], Lq[l]["Kc"][sel], Lq[l]["Vc"][sel], sw)[1][0]
+            assert_close(g_out[l][b], want_O, f"CSA2 layer {l} batch {b}")
+        assert np.array_equal(g_idx[2][b], g_idx[1][b])
     assert near <= 2

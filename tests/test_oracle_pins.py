@@ -285,6 +285,30 @@ def test_csa_with_large_k_equals_hca_m4():
         assert c["n_visible"] == h["n_visible"] == (t + 1) // 4
 
 
+def test_dsa_m1_with_large_k_equals_dense_causal():
+    # the DSA comparator ([THREAD] "주요 댓글": the indexer runs over the full KV,
+    # attention over the tokens it selects) is CSA with m = 1; when k covers
+    # every visible token it is textbook causal attention, and with a small k
+    # it attends exactly to the brute-force best-scoring tokens
+    T, H, D, HI, DI, k = 30, 2, 8, 2, 4, 5
+    K, V = _bf16_grid((T, D)), _bf16_grid((T, D))
+    Kc, Vc = oracle.pool(K, V, rng.standard_normal(T), 1)
+    kI = rng.standard_normal((T, DI))
+    q = rng.standard_normal((T, H, D)) * 0.4
+    ref = _causal_dense(q, K, V)
+    for t in range(T):
+        qI, w = rng.standard_normal((HI, DI)), rng.uniform(0, 1, HI)
+        c = runs.csa_branch(q[t], t, qI, w, kI, Kc, Vc, 1, k=T)
+        np.testing.assert_allclose(c["O"], ref[t], atol=1e-12)
+        assert c["n_visible"] == t + 1
+        small = runs.csa_branch(q[t], t, qI, w, kI, Kc, Vc, 1, k=k)
+        sc = [sum(w[h] * max(0.0, float(qI[h] @ kI[j])) for h in range(HI)) for j in range(t + 1)]
+        best = sorted(range(t + 1), key=lambda j: (-sc[j], j))[:k]
+        assert sorted(best) == [j for j in small["idx"] if j >= 0]
+        O, _ = oracle.attend(q[t], K[sorted(best)], V[sorted(best)])
+        np.testing.assert_allclose(small["O"], O, atol=1e-12)
+
+
 def test_merge_equals_softmax_over_concatenation():
     H, D = 4, 8
     q = rng.standard_normal((H, D))
@@ -426,3 +450,143 @@ def test_hca_prefill_matches_full_sequence_pooling():
         assert r["hca"]["n_visible"] == (t + 1) // cfg.m
         np.testing.assert_allclose(r["layer"][0], want[0], atol=1e-12)
         np.testing.assert_allclose(r["layer"][1], want[1], atol=1e-12)
+
+
+def test_swa_replay_bounds_the_window_and_restores_the_last_state():
+    # [V41], SWA Bounded Replay: only the last R tokens are replayed against the
+    # kept compressed caches.  Every expected value comes from whole-sequence
+    # pooling and the pinned branch functions with a raw buffer that holds the
+    # entire history.
+    from datagen.workloads import PairDecode
+    cfg = PairDecode(B=1, ctx=32, steps=1, D=8, H=2, HI=2, DI=16, k=3, W=8, m_csa=4, m_hca=8)
+    R = cfg.W
+    L = cfg.ctx
+    K, V, g = _bf16_grid((L, cfg.D)), _bf16_grid((L, cfg.D)), rng.standard_normal(L)
+    Kh, Vh, gh = _bf16_grid((L, cfg.D)), _bf16_grid((L, cfg.D)), rng.standard_normal(L)
+    Kc, Vc = oracle.pool(K, V, g, cfg.m_csa)
+    Khc, Vhc = oracle.pool(Kh, Vh, gh, cfg.m_hca)
+    # NVFP4 keys: codes and scales chosen at random, decoded by the pinned decoder
+    kp = rng.integers(0, 256, (1, cfg.N_csa, cfg.DI // 2), dtype=np.uint8)
+    ks = rng.integers(0x20, 0x48, (1, cfg.N_csa, cfg.DI // 16), dtype=np.uint8)
+    kI = oracle.nvfp4_decode(kp[0], ks[0])
+    rq = _bf16_grid((R, 1, cfg.H, cfg.D), 0.5)
+    rqI = _bf16_grid((R, 1, cfg.HI, cfg.DI))
+    rw = rng.uniform(0, 1, (R, 1, cfg.HI))
+    r0 = cfg.ctx - cfg.W
+    inp = dict(Kr=_bits(K[None, r0:]), Vr=_bits(V[None, r0:]), Kr_h=_bits(Kh[None, r0:]), Vr_h=_bits(Vh[None, r0:]),
+               Kc=_bits(Kc[None]), Vc=_bits(Vc[None]), Kc_h=_bits(Khc[None]), Vc_h=_bits(Vhc[None]),
+               kI_packed=kp, kI_scale=ks, rq=_bits(rq), rqI=_bits(rqI), rw=rw)
+    got = runs.swa_replay(inp, cfg, R)
+    for i in range(R):
+        t = cfg.ctx - R + i
+        r = got[(i, 0)]
+        assert r["window"] == i + 1                      # the rebuilt window only holds replayed tokens
+        c = runs.csa_branch(rq[i, 0], t, rqI[i, 0], rw[i, 0], kI, Kc, Vc, cfg.m_csa, cfg.k)
+        assert np.array_equal(r["idx"], c["idx"])
+        sw_full = runs.swa_branch(rq[i, 0], t, K, V, 0, cfg.W)
+        sw_rep = runs.swa_branch(rq[i, 0], t, K[cfg.ctx - R:], V[cfg.ctx - R:], cfg.ctx - R, cfg.W)
+        want = oracle.merge([c["O"], sw_rep["O"]], [c["lse"], sw_rep["lse"]])
+        np.testing.assert_allclose(r["csa"][0], want[0], atol=1e-12)
+        if i == R - 1:
+            # the last replayed position has its full window: its output equals
+            # the unbounded recomputation of the whole prompt's state
+            full_c = oracle.merge([c["O"], sw_full["O"]], [c["lse"], sw_full["lse"]])
+            h = runs.hca_branch(rq[i, 0], t, Khc, Vhc, cfg.m_hca)
+            swh = runs.swa_branch(rq[i, 0], t, Kh, Vh, 0, cfg.W)
+            full_h = oracle.merge([h["O"], swh["O"]], [h["lse"], swh["lse"]])
+            np.testing.assert_allclose(r["csa"][0], full_c[0], atol=1e-12)
+            np.testing.assert_allclose(r["hca"][0], full_h[0], atol=1e-12)
+        else:
+            assert sw_full["n_keys"] == cfg.W > r["window"]
+
+
+# ---------------------------------------------------------------------------
+# query / KV prologue ([HYBRID]: query and KV normalisation, partial RoPE)
+# ---------------------------------------------------------------------------
+def test_rms_norm_hand_values():
+    # row (3, 4): mean square 12.5; eps 0 -> (3, 4) / sqrt(12.5)
+    y = oracle.rms_norm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(y, [[3 / math.sqrt(12.5), 8 / math.sqrt(12.5)]], rtol=1e-15)
+    # unit gains: mean square of the output is ms / (ms + eps)
+    x = rng.standard_normal((5, 128))
+    y = oracle.rms_norm(x, np.ones(128), 1e-6)
+    ms = np.mean(x * x, 1)
+    np.testing.assert_allclose(np.mean(y * y, 1), ms / (ms + 1e-6), rtol=1e-12)
+    # scale invariance (up to eps)
+    np.testing.assert_allclose(oracle.rms_norm(7.0 * x, np.ones(128), 0.0), oracle.rms_norm(x, np.ones(128), 0.0),
+                               rtol=1e-13)
+
+
+def test_rope_matches_complex_rotation_and_leaves_the_rest():
+    D, d, pos = 128, 64, 12345
+    x = rng.standard_normal((3, D))
+    y = oracle.rope_partial(x, pos, d)
+    np.testing.assert_array_equal(y[:, :D - d], x[:, :D - d])
+    z = (x[:, D - d:D - d // 2] + 1j * x[:, D - d // 2:]) * np.exp(
+        1j * pos * 10000.0 ** (-np.arange(d // 2) * 2.0 / d))
+    np.testing.assert_allclose(y[:, D - d:D - d // 2], z.real, atol=1e-12)
+    np.testing.assert_allclose(y[:, D - d // 2:], z.imag, atol=1e-12)
+    np.testing.assert_array_equal(oracle.rope_partial(x, 0, d), x)          # position 0: identity
+
+
+def test_rope_scores_depend_on_relative_position_only():
+    D, d = 128, 64
+    q, k = rng.standard_normal(D), rng.standard_normal(D)
+    for p, s, c in ((10, 3, 1000), (70000, 1, 5), (1048575, 1048000, -1040000)):
+        a = oracle.rope_partial(q, p, d) @ oracle.rope_partial(k, s, d)
+        b = oracle.rope_partial(q, p + c, d) @ oracle.rope_partial(k, s + c, d)
+        assert abs(a - b) <= 1e-9 * (abs(a) + 1)
+    # rotating by p then by -p restores the row (the map is orthogonal)
+    np.testing.assert_allclose(oracle.rope_partial(oracle.rope_partial(q, 777, d), -777, d), q, atol=1e-12)
+
+
+def test_prologue_order_norm_then_rope_and_v_unrotated():
+    H, D, d = 3, 128, 64
+    q, k, v = rng.standard_normal((H, D)), rng.standard_normal(D), rng.standard_normal(D)
+    gq, gk, gv = 1 + 0.1 * rng.standard_normal((3, D))
+    qn, kn, vn = oracle.qkv_prologue(q, k, v, 99, gq, gk, gv, 1e-6, d)
+    np.testing.assert_allclose(qn, oracle.rope_partial(oracle.rms_norm(q, gq, 1e-6), 99, d), atol=0)
+    np.testing.assert_allclose(kn, oracle.rope_partial(oracle.rms_norm(k, gk, 1e-6), 99, d), atol=0)
+    np.testing.assert_allclose(vn, oracle.rms_norm(v, gv, 1e-6), atol=0)
+    # the rotation keeps each pair's length: |q| after norm equals |q| after norm and rope
+    np.testing.assert_allclose(np.linalg.norm(qn, axis=1),
+                               np.linalg.norm(oracle.rms_norm(q, gq, 1e-6), axis=1), rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# CSA2 index sharing ([V41], the CSA2 passage: full / re-index / reuse modes)
+# ---------------------------------------------------------------------------
+def test_csa2_modes_brute_force_and_special_cases():
+    N, D, H, HI, DI, k, n_notes, m = 40, 8, 2, 2, 4, 4, 10, 4
+    t = N * m - 1
+    kI = rng.standard_normal((N, DI))
+    caches = [(_bf16_grid((N, D)), _bf16_grid((N, D))) for _ in range(4)]
+    qIs = [rng.standard_normal((HI, DI)) for _ in range(3)]
+    ws = [rng.uniform(0, 1, HI) for _ in range(3)]
+    qs = [rng.standard_normal((H, D)) * 0.4 for _ in range(4)]
+    layers = [dict(mode="full", q=qs[0], qI=qIs[0], w=ws[0], Kc=caches[0][0], Vc=caches[0][1]),
+              dict(mode="reindex", q=qs[1], qI=qIs[1], w=ws[1], Kc=caches[1][0], Vc=caches[1][1]),
+              dict(mode="reuse", q=qs[2], Kc=caches[2][0], Vc=caches[2][1]),
+              dict(mode="reindex", q=qs[3], qI=qIs[0], w=ws[0], Kc=caches[3][0], Vc=caches[3][1])]
+    out = runs.csa2_group(None, t, layers, kI, m, k, n_notes)
+
+    def score(qI, w, j):
+        return sum(w[h] * max(0.0, sum(qI[h, c] * kI[j, c] for c in range(DI))) for h in range(HI))
+    s0 = [score(qIs[0], ws[0], j) for j in range(N)]
+    notes = sorted(sorted(range(N), key=lambda j: (-s0[j], j))[:n_notes])
+    assert [j for j in out[0]["notes"] if j >= 0] == notes
+    assert [j for j in out[0]["idx"] if j >= 0] == sorted(sorted(range(N), key=lambda j: (-s0[j], j))[:k])
+    s1 = {j: score(qIs[1], ws[1], j) for j in notes}
+    assert [j for j in out[1]["idx"] if j >= 0] == sorted(sorted(notes, key=lambda j: (-s1[j], j))[:k])
+    # reuse copies the previous layer's selection and attends to its own cache
+    assert np.array_equal(out[2]["idx"], out[1]["idx"])
+    sel = out[1]["idx"][out[1]["idx"] >= 0]
+    O, _ = oracle.attend(qs[2], caches[2][0][sel], caches[2][1][sel])
+    np.testing.assert_allclose(out[2]["O"], O, atol=1e-12)
+    # re-indexing the notes with the full layer's own query gives the full layer's top-k
+    assert np.array_equal(out[3]["idx"], out[0]["idx"])
+    # notes covering every visible entry: re-index = full mode with the layer's own query
+    wide = runs.csa2_group(None, t, layers[:2], kI, m, k, n_notes=N)
+    full1 = runs.csa_branch(qs[1], t, qIs[1], ws[1], kI, caches[1][0], caches[1][1], m, k)
+    assert np.array_equal(wide[1]["idx"], full1["idx"])
+    np.testing.assert_allclose(wide[1]["O"], full1["O"], atol=1e-12)
