@@ -345,20 +345,25 @@ class CsaDecodeBench:
         s = c.seed
         done, t_oracle = 0, 0.0
         b = first
+        cache = {}   # inputs of the batch rows this process cycles over, regenerated once
         while t_oracle < budget_s and (max_queries is None or done < max_queries):
             bb = b % c.B
-            kI = _host_rows(s, wl.T_KI, bb, c.N, c.DI)
-            qI = _host_rows(s, wl.T_QI, bb, c.HI, c.DI)
-            w = datagen.uniform_f32(s, wl.T_W, (c.B, c.HI)).numpy()[bb].astype(np.float64)
-            q = _host_rows(s, wl.T_Q, bb, c.H, c.D, c.q_scale)
-            Kr = _host_rows(s, wl.T_KR, bb, c.W, c.D)
-            Vr = _host_rows(s, wl.T_VR, bb, c.W, c.D)
+            if bb not in cache:
+                cache[bb] = dict(
+                    kI=_host_rows(s, wl.T_KI, bb, c.N, c.DI), qI=_host_rows(s, wl.T_QI, bb, c.HI, c.DI),
+                    w=datagen.uniform_f32(s, wl.T_W, (c.B, c.HI)).numpy()[bb].astype(np.float64),
+                    q=_host_rows(s, wl.T_Q, bb, c.H, c.D, c.q_scale), Kr=_host_rows(s, wl.T_KR, bb, c.W, c.D),
+                    Vr=_host_rows(s, wl.T_VR, bb, c.W, c.D))
+            kI, qI, w, q, Kr, Vr = (cache[bb][x] for x in ("kI", "qI", "w", "q", "Kr", "Vr"))
             t0 = time.perf_counter()
             sc = oracle.index_scores(qI, w, kI)
             idx, _ = oracle.topk_select(sc, c.k)
             t_oracle += time.perf_counter() - t0
-            Kc = _host_entry_rows(s, wl.T_KC, bb * c.N + idx, c.D)
-            Vc = _host_entry_rows(s, wl.T_VC, bb * c.N + idx, c.D)
+            key = (bb, tuple(idx.tolist()))
+            if key not in cache:
+                cache[key] = (_host_entry_rows(s, wl.T_KC, bb * c.N + idx, c.D),
+                              _host_entry_rows(s, wl.T_VC, bb * c.N + idx, c.D))
+            Kc, Vc = cache[key]
             t0 = time.perf_counter()
             cO, cL = oracle.attend(q, Kc, Vc)
             sw = runs.swa_branch(q, c.q_pos, Kr, Vr, c.raw_pos0, c.W)
@@ -366,7 +371,8 @@ class CsaDecodeBench:
             t_oracle += time.perf_counter() - t0
             done += 1
             b += stride
-        return done, t_oracle, "decode queries of the batch (inputs regenerated on the host, untimed)"
+        return done, t_oracle, ("decode queries of the batch (each process regenerates the inputs of its "
+                                "batch rows once on the host, untimed, then repeats their queries)")
 
 
 
@@ -455,7 +461,7 @@ class PairDecodeBench:
     """Interleaved CSA/HCA layer pair decode at 1M context, batch 4, NVFP4 indexer keys, 64 steps."""
     unit = "queries/s"
     name = "pair_decode"
-    dominant = "k_index_score<NVFP4>"
+    dominant = "k_index_tc_fp4"
     bound = "hbm"
     graph_steps = 64
 
@@ -759,9 +765,18 @@ def e2e_of(wb, ws, n_steps):
                     "output, synchronise"}
 
 
+T0 = time.perf_counter()
+
+
+def phase(msg):
+    """Progress of the run on stderr (wall seconds since start)."""
+    print(f"[bench {time.perf_counter() - T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+
+
 def measure_secondary(name, dev, stream, pk):
     """A short measurement of another workload (throughput + its dominant kernel's roofline)."""
     import long_context_compressed_15_b300 as lcc
+    phase(f"secondary {name}")
     wb = WORKLOADS[name]()
     wb.setup(dev)
     G = wb.graph_steps
@@ -796,6 +811,7 @@ def run_ours(args, ws, rank, local):
     dev = f"cuda:{local}"
     pk = peaks()
     wb = WORKLOADS[args.workload]()
+    phase(f"setup {args.workload}")
     wb.setup(dev)
     stream = torch.cuda.current_stream()
     G = wb.graph_steps
@@ -833,9 +849,11 @@ def run_ours(args, ws, rank, local):
     repeat = {"steps": n_rep, "seconds": round(t_rep, 4), "value": round(wb.units_per_step() * n_rep * ws / t_rep, 1),
               "ms_per_step": round(t_rep / n_rep * 1e3, 5), "clocks": ck_r}
 
+    phase("roofline")
     roofline = roofline_of(wb, stream, max(4, min(64, args.steps // G)), pk)
     if hasattr(wb, "step_bytes"):
         roofline["step_hbm_gbs"] = round(wb.step_bytes() * args.steps / t / 1e9, 1)
+    phase("e2e")
     e2e = e2e_of(wb, ws, max(3, min(200, args.steps)))
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": wb.unit, "n_gpus": ws, "steps": args.steps,
@@ -846,6 +864,7 @@ def run_ours(args, ws, rank, local):
     if hasattr(wb, "extra"):
         line["config"].update(wb.extra())
     if rank == 0 and not args.no_cpu_baseline and hasattr(wb, "oracle_sample"):
+        phase("cpu baseline")
         n, rate, what, nw, ncpu = oracle_on_host_cores(args.workload, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(rate, 3), "unit": wb.unit, "cores": nw, "host_cpu_count": ncpu,
                                 "kind": "oracle", "sample": f"about {args.cpu_budget:g} s of oracle work per "
@@ -861,6 +880,7 @@ def run_ours(args, ws, rank, local):
         w = line["workloads"]
         if args.workload == "csa_decode" and "dsa_decode" in w:
             w["dsa_decode"]["vs_csa_decode"] = dsa_comparison({"ms_per_step": line["ms_per_step"]}, w["dsa_decode"])
+    phase("done")
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -896,7 +916,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="csa_decode")
-    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work per process for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the short measurements of the other workloads")

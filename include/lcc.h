@@ -183,8 +183,12 @@ lcc_status lcc_decode_append(int m, int B, int D,
  * q_pos0, n_valid: device arrays [B] (int64, int32).
  * HI in {4, 8}; DI in {32, 64} (NVFP4: DI = 64); 1 <= k <= 1024; Ncap >= 1.
  * workspace: at least lcc_index_topk_workspace(B, Tq, Ncap, k) bytes.
- * With NVFP4 keys the indexer queries are rounded to fp16 for the tensor-
- * core product (exact for 2^-14 <= |qI| <= 65504).
+ * With NVFP4 keys the tensor cores multiply fp16 operands: the keys expand
+ * to fp16 exactly (e2m1 x e4m3), and each (query, head) row of qI is scaled
+ * by the power of two that puts its largest element just under 2^15, with
+ * the head weight scaled by the inverse; every element within a factor 2^31
+ * of its row's largest is then exact, so the scores equal those of the bf16
+ * queries (a power-of-two scale commutes with the fp32 rounding).
  * ---------------------------------------------------------------------- */
 size_t lcc_index_topk_workspace(int B, int Tq, int Ncap, int k);
 lcc_status lcc_lightning_index_topk(const lcc_bf16* qI, const float* w,

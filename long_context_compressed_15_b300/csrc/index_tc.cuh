@@ -246,8 +246,8 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
 // NVFP4 keys on the tensor cores.  The keys stream as packed e2m1 pairs (32
 // bytes per entry) plus one e4m3 scale per 16 elements (4 bytes per entry):
 // 36 bytes instead of 128.  Roles (320 threads):
-//   warp 0      producer: bulk copies of 128-entry packed tiles (4 KB) into a
-//               ring of raw buffers;
+//   warp 0      producer: bulk copies of 128-entry packed tiles (4 KB) and
+//               their scales (512 B) into a ring of raw buffers;
 //   warp 1      TMEM allocation; one thread issues tcgen05.mma (kind::f16,
 //               fp16 operands) from a ring of converted buffers;
 //   warps 2..5  epilogue as k_index_tc; they also stage the indexer queries;
@@ -265,7 +265,8 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
 template <int DI>
 struct IndexTcFp4Cfg {
   static constexpr int TILE = 128;
-  static constexpr int RAW_BYTES = TILE * DI / 2;       // packed tile
+  static constexpr int PACK_BYTES = TILE * DI / 2;      // packed values of a tile
+  static constexpr int RAW_BYTES = PACK_BYTES + TILE * DI / 16;   // + their scales
   static constexpr int ROWB = DI * 2;                   // converted row (fp16)
   static constexpr int A_BYTES = TILE * ROWB;
 };
@@ -288,7 +289,7 @@ struct IndexTcFp4Smem {
 };
 
 template <int HI, int DI, int NQ, int SR, int SC>
-__global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
+__global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   using F = IndexTcFp4Cfg<DI>;
   using S = IndexTcFp4Smem<HI, DI, NQ, SR, SC>;
   using C = IndexTcCfg<HI, DI, NQ, 1>;
@@ -335,15 +336,29 @@ __global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
   const int64_t row_base = static_cast<int64_t>(b) * a.Ncap;   // entry row of this batch's entry 0
   // rows of tile t (CTA-local), the last one possibly partial
   auto tile_rows = [&](int t) { return min(F::TILE, a.Ncap - (t_lo + t) * F::TILE); };
+  // bytes of tile t's scales that one bulk copy moves (a multiple of 16; the
+  // scales of the last 1..3 rows of a ragged final tile are read directly)
+  // (none when this batch's scale rows do not start on a 16-byte boundary)
+  const bool scale_bulk = ((reinterpret_cast<uintptr_t>(a.kI_scale) + row_base * (DI / 16)) & 15) == 0;
+  auto scale_bytes = [&](int t) {
+    return scale_bulk ? static_cast<uint32_t>(tile_rows(t)) * (DI / 16) & ~15u : 0u;
+  };
   auto issue = [&](int t) {
     const int s = t % SR;
-    const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * (DI / 2);
-    tc::mbar_arrive_expect_tx(rfull + s, bytes);
-    const uint8_t* src = a.kI_fp4 + (row_base + static_cast<int64_t>(t_lo + t) * F::TILE) * (DI / 2);
+    const uint32_t bytes = static_cast<uint32_t>(tile_rows(t)) * (DI / 2), sbytes = scale_bytes(t);
+    tc::mbar_arrive_expect_tx(rfull + s, bytes + sbytes);
+    const int64_t e0 = row_base + static_cast<int64_t>(t_lo + t) * F::TILE;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(smem_u32(sRaw + s * F::RAW_BYTES)), "l"(src), "r"(bytes), "r"(smem_u32(rfull + s))
+        ::"r"(smem_u32(sRaw + s * F::RAW_BYTES)), "l"(a.kI_fp4 + e0 * (DI / 2)), "r"(bytes),
+        "r"(smem_u32(rfull + s))
         : "memory");
+    if (sbytes)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+          ::"r"(smem_u32(sRaw + s * F::RAW_BYTES + F::PACK_BYTES)), "l"(a.kI_scale + e0 * (DI / 16)),
+          "r"(sbytes), "r"(smem_u32(rfull + s))
+          : "memory");
   };
   if (warp == 0 && lane == 0)
     for (int t = 0; t < min(SR, ntiles); ++t) issue(t);
@@ -370,8 +385,9 @@ __global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
           emax = max(emax, static_cast<int>((wd[u] >> 23) & 0xFF));
         }
       }
-      // 2^sc brings the largest element to [2^14, 2^15)
-      const int sc = emax == 0 ? 0 : 141 - emax;
+      // 2^sc brings the largest element to [2^14, 2^15) (rows of values below
+      // 2^-112 stay below that range: 2^sc must remain a finite float)
+      const int sc = emax == 0 ? 0 : min(141 - emax, 126);
       const float up = ldexpf(1.0f, sc);
 #pragma unroll
       for (int c = 0; c < DI / 8; ++c) {
@@ -450,8 +466,11 @@ __global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
       const int s = t % SR, c = t % SC;
       const int64_t e = row_base + static_cast<int64_t>(t_lo + t) * F::TILE + r;
       const bool live = r < tile_rows(t);
-      const uint32_t scales = live ? __ldg(reinterpret_cast<const uint32_t*>(a.kI_scale + e * (DI / 16))) : 0u;
+      const bool copied = static_cast<uint32_t>(r) * (DI / 16) < scale_bytes(t);
       if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(rfull + s, (t / SR) & 1, 16))) { *s_abort = 1; break; }
+      const uint32_t scales =
+          copied ? *reinterpret_cast<const uint32_t*>(sRaw + s * F::RAW_BYTES + F::PACK_BYTES + r * (DI / 16))
+                 : (live ? __ldg(reinterpret_cast<const uint32_t*>(a.kI_scale + e * (DI / 16))) : 0u);
       if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(cempty + c, ((t / SC) & 1) ^ 1, 17))) {
         *s_abort = 1;
         break;
@@ -465,7 +484,7 @@ __global__ void __launch_bounds__(320, 1) k_index_tc_fp4(IndexTcArgs a) {
       const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
       uint8_t* dst = sA + c * F::A_BYTES + (r >> 3) * S::SBO + (r & 7) * F::ROWB;
 #pragma unroll
-      for (int ch = 0; ch < DI / 8; ++ch) {       // 16-byte chunk = 8 elements = 2 packed words... 1 word
+      for (int ch = 0; ch < DI / 8; ++ch) {       // one packed word = 8 elements = one 16-byte fp16 chunk
         const uint32_t s2 = e4m3_to_f16x2_bcast(scales >> (8 * (ch >> 1)));
         const uint32_t word = wd[ch];
         uint4 o;

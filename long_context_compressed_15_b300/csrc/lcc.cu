@@ -27,6 +27,7 @@
 #include "index_topk_tc.cuh"
 #include "topk_thr.cuh"
 #include "topk_cluster.cuh"
+#include "topk_gsel.cuh"
 
 #include <cudaTypedefs.h>
 
@@ -179,6 +180,19 @@ constexpr int kClMaxG = 512;
 using ClSmem = TopkClSmem<kClNT, kClPer, kClCap, kClMaxG>;
 unsigned long long g_topk_cl_done = 0;
 
+// Group-selected top-k (one CTA per row, reads only the score groups that can
+// hold a winner): k up to 256 and rows whose group maxima fit shared memory.
+// Rows the cluster top-k takes (up to 16384 entries) go there instead: its
+// eight CTAs per row finish sooner than one CTA's serial selection rounds
+// (measured on the 32 x 16384 decode batch: 31.7 us against 35.3 us per
+// step); longer rows come here, where reading ~k groups instead of the whole
+// row wins (262144-entry rows: the layer-pair step 86 us -> 68 us).
+constexpr int kGselNT = 512;
+constexpr int kGselCap = 4096;
+unsigned long long g_topk_gsel_done = 0;
+size_t gsel_smem(int Ncap) { return static_cast<size_t>((Ncap + 31) / 32) * 8 + kGselCap * 12; }
+bool use_gsel(int Ncap, int k) { return k <= 256 && gsel_smem(Ncap) <= 200 * 1024; }
+
 int topk_cluster_ctas(int Ncap, int k, int gs) {
   if (Ncap > 8 * kClSeg || 2 * k > kClMaxG || static_cast<int64_t>(k) * gs > kClCap) return 0;
   return (Ncap + kClSeg - 1) / kClSeg;
@@ -293,6 +307,41 @@ lcc_status launch_index_tc(const IndexArgs& ia, cudaStream_t s) {
   return launch_index_tc_q<HI, DI, 128 / HI>(ia, tm, 1, s);
 }
 
+unsigned long long g_index_fp4_done[2] = {};
+
+// NVFP4 keys: tcgen05 indexer fed by bulk copies of the packed tiles and a
+// converter warpgroup (k_index_tc_fp4); key-range splits as k_index_tc.
+template <int NQ>
+lcc_status launch_index_fp4_q(const IndexArgs& ia, int bit, cudaStream_t s) {
+  constexpr int HI = 8, DI = 64, SR = 6, SC = 3;
+  using Sm = IndexTcFp4Smem<HI, DI, NQ, SR, SC>;
+  auto kern = k_index_tc_fp4<HI, DI, NQ, SR, SC>;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    lcc_status st = ensure_smem(kern, Sm::SMEM, g_index_fp4_done[bit]);
+    if (st != LCC_OK) return st;
+  }
+  IndexTcArgs a{ia.qI, ia.w, ia.B, ia.Tq, ia.q_pos0, ia.n_valid, ia.Ncap, ia.m, ia.q0, ia.nq, 0,
+                ia.scores, ia.gmax, ia.g_stride, ia.counters, static_cast<const uint8_t*>(ia.kI), ia.kIs};
+  const int ngroups = (ia.nq + NQ - 1) / NQ;
+  const int tiles = (ia.Ncap + 127) / 128;
+  const int64_t base = static_cast<int64_t>(ia.B) * ngroups;
+  const int target = 2 * num_sms();  // one wave at two CTAs per SM
+  int nsplit = base >= 2 * num_sms() ? 1 : static_cast<int>((target + base - 1) / base);
+  if (nsplit > tiles) nsplit = tiles;
+  if (nsplit < 1) nsplit = 1;
+  a.tiles_per_split = (tiles + nsplit - 1) / nsplit;
+  nsplit = (tiles + a.tiles_per_split - 1) / a.tiles_per_split;
+  if (ngroups > 65535) return fail(LCC_ERR_SHAPE, "k_index_tc_fp4: %d query groups", ngroups);
+  launch_k(kern, dim3(nsplit, ngroups, ia.B), dim3(320), Sm::SMEM, s, true, a);
+  return launch_check("k_index_tc_fp4");
+}
+
+lcc_status launch_index_fp4(const IndexArgs& ia, cudaStream_t s) {
+  if (ia.nq * 8 <= 16) return launch_index_fp4_q<2>(ia, 0, s);
+  return launch_index_fp4_q<16>(ia, 1, s);
+}
+
 unsigned long long g_index_topk_tc_done[2][2] = {};
 unsigned long long g_index_topk_pw_done[2] = {};
 constexpr int kFusedTopkMaxK = 256;
@@ -335,21 +384,6 @@ bool use_fused_topk(lcc_key_format fmt, int Tq, int HI, int k) {
   return fmt == LCC_KEY_BF16 && static_cast<int64_t>(Tq) * HI > 16 && k <= kFusedTopkMaxK &&
          (Tq + 128 / HI - 1) / (128 / HI) <= 65535;
 }
-
-template <int HI, int DI, bool FP4>
-lcc_status launch_index_score(const IndexArgs& a, cudaStream_t s) {
-  constexpr int QPT = 8 / HI;
-  if (a.nq <= QPT) {
-    dim3 grid((a.Ncap + 255) / 256, 1, a.B);
-    k_index_score<HI, DI, FP4, QPT><<<grid, 128, 0, s>>>(a);
-  } else {
-    constexpr int NQ = 8 * QPT;
-    dim3 grid((a.Ncap + 255) / 256, (a.nq + NQ - 1) / NQ, a.B);
-    k_index_score<HI, DI, FP4, NQ><<<grid, 128, 0, s>>>(a);
-  }
-  return launch_check("k_index_score");
-}
-
 
 }  // namespace
 
@@ -515,11 +549,13 @@ lcc_status check_index_args(const char* name, const lcc_bf16* qI, const float* w
   if (B > 65535) return fail(LCC_ERR_SHAPE, "%s: B=%d too large", name, B);
   if (!aligned16(qI) || !aligned16(kI) || !aligned16(w) || !aligned16(out))
     return fail(LCC_ERR_ALIGN, "%s: qI, w, kI and the output must be 16-byte aligned", name);
+  if (fmt == LCC_KEY_NVFP4 && (reinterpret_cast<uintptr_t>(kI_scale) & 3))
+    return fail(LCC_ERR_ALIGN, "%s: kI_scale must be 4-byte aligned", name);
   return LCC_OK;
 }
 
 lcc_status launch_scores(const IndexArgs& ia, int HI, int DI, lcc_key_format fmt, cudaStream_t s) {
-  if (fmt == LCC_KEY_NVFP4) return launch_index_score<8, 64, true>(ia, s);
+  if (fmt == LCC_KEY_NVFP4) return launch_index_fp4(ia, s);
   if (HI == 8 && DI == 64) return launch_index_tc<8, 64>(ia, s);
   if (HI == 8 && DI == 32) return launch_index_tc<8, 32>(ia, s);
   if (HI == 4 && DI == 64) return launch_index_tc<4, 64>(ia, s);
@@ -561,7 +597,7 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
     TopkThrArgs ta{};
     ta.scores = scores;
     ta.gmax = gmax;
-    ta.gs = fmt == LCC_KEY_NVFP4 ? 16 : 32;
+    ta.gs = 32;  // both tensor-core indexers write one maximum per 32 entries
     ta.g_stride = gmax_stride(Ncap);
     ta.Ncap = Ncap;
     ta.q_pos0 = q_pos0;
@@ -582,6 +618,17 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
     const int64_t rows = static_cast<int64_t>(B) * nq;
     if (rows > 0x7FFFFFFF / 8) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
     const int cl = topk_cluster_ctas(Ncap, k, ta.gs);
+    if (cl == 0 && use_gsel(Ncap, k)) {
+      auto kern = k_topk_gsel<kGselNT, kGselCap>;
+      const size_t smem = gsel_smem(Ncap);
+      {
+        std::lock_guard<std::mutex> lk(g_attr_mu);
+        if ((st = ensure_smem(kern, 200 * 1024, g_topk_gsel_done)) != LCC_OK) return st;
+      }
+      launch_k(kern, dim3(static_cast<unsigned>(rows)), dim3(kGselNT), smem, s, true, ta);
+      if ((st = launch_check("k_topk_gsel")) != LCC_OK) return st;
+      continue;
+    }
     if (cl > 0) {
       auto kern = k_topk_cluster<kClNT, kClPer, kClCap, kClMaxG>;
       {

@@ -1,0 +1,183 @@
+// Exact top-k of a row of indexer scores, one CTA per row, reading only the
+// score groups that can hold a winner.  Source: "DeepSeek-V4가 이차적 어텐션
+// 비용 없이 ...", section "두 가지 압축 전략: CSA 및 HCA" (the indexer keeps the
+// top-k compressed entries per query).
+//
+// Result (identical to k_topk_thr / k_topk_cluster): the min(k, visible)
+// entries with the largest scores, ties to the lower index, in ascending
+// index order, padded with -1.
+//
+// The indexer writes the key of each group's largest score (groups of gs
+// consecutive entries).  theta = the k-th largest group maximum is a lower
+// bound of the row's k-th largest score, so every winner lies in a group
+// whose maximum reaches theta -- at most k groups plus those tied at theta.
+//   1. the row's group maxima are loaded and theta is selected (256-bin
+//      histogram rounds);
+//   2. the groups whose maximum reaches theta are listed in index order
+//      (one block scan) and only their scores are read, one warp per group;
+//   3. the scores >= theta are compacted in index order (typically little
+//      more than k of them) and the exact k-th largest key T is selected
+//      among them;
+//   4. every candidate above T and the lowest-index candidates equal to T
+//      are written, in index order.
+// When the listed groups hold more than CAP entries (massive exact ties at
+// theta) the CTA falls back to a bisection over the whole row.
+#pragma once
+#include "topk_cluster.cuh"
+
+namespace lcc {
+
+template <int NT, int CAP>
+__global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
+  extern __shared__ __align__(16) uint32_t sm_gsel[];
+  __shared__ int s_warp[NT / 32];
+  __shared__ uint32_t s_hist[256];
+  __shared__ uint32_t s_bc[4];
+  const int G_cap = (a.Ncap + a.gs - 1) / a.gs;
+  uint32_t* s_g = sm_gsel;                 // [G_cap] group maxima
+  int* s_gl = reinterpret_cast<int*>(s_g + G_cap);   // [G_cap] listed groups, index order
+  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_gl + G_cap);  // [CAP] keys of the listed groups
+  uint32_t* s_ok = s_ck + CAP;             // [CAP] compacted candidate keys
+  int32_t* s_oi = reinterpret_cast<int32_t*>(s_ok + CAP);      // [CAP] their entries
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    s_bc[2] = 0xFFFFFFFFu;
+    s_bc[3] = 0u;
+  }
+  const int row = blockIdx.x;
+  const int b = row / a.nq, i = a.q0 + row % a.nq;
+  const int k = a.k;
+  const float* srow = a.scores + static_cast<int64_t>(row) * a.Ncap;
+  const int64_t qpos = __ldg(a.q_pos0 + b) + i;
+  const int nval = __ldg(a.n_valid + b);
+  const int vis = visible_entries(qpos, a.m, nval, a.Ncap);
+  int32_t* oi = a.out_i + (static_cast<int64_t>(b) * a.Tq + i) * k;
+  float* os = a.out_s ? a.out_s + (static_cast<int64_t>(b) * a.Tq + i) * k : nullptr;
+  pdl_trigger();
+  pdl_wait();  // scores and group maxima come from the indexer kernel
+
+  if (vis <= k) {  // every visible entry is selected
+    for (int p = tid; p < k; p += NT) {
+      oi[p] = p < vis ? p : -1;
+      if (os) os[p] = p < vis ? __ldcg(srow + p) : -INFINITY;
+    }
+    return;
+  }
+  const int gs = a.gs;
+  const int G = (vis + gs - 1) / gs;
+  const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
+  for (int g = tid; g < G; g += NT) s_g[g] = __ldcg(gm + g);
+  __syncthreads();
+  // 1. theta (0 when fewer than k groups: every group is listed)
+  const uint32_t theta = G >= k ? block_kth_hist<NT>(s_g, G, k, s_hist, s_bc) : 0u;
+  // 2. groups whose maximum reaches theta, in index order
+  int ng = 0;
+  {
+    constexpr int PERG = 4;  // consecutive groups per thread per pass
+    for (int g0 = 0; g0 < G; g0 += NT * PERG) {
+      const int gb = g0 + tid * PERG;
+      int f = 0;
+#pragma unroll
+      for (int u = 0; u < PERG; ++u) f += (gb + u < G && s_g[gb + u] >= theta) ? 1 : 0;
+      int tot;
+      int p = ng + block_scan_excl<NT>(f, s_warp, &tot);
+#pragma unroll
+      for (int u = 0; u < PERG; ++u)
+        if (gb + u < G && s_g[gb + u] >= theta) s_gl[p++] = gb + u;
+      ng += tot;
+    }
+  }
+  __syncthreads();
+  const int C = ng * gs;
+  if (C <= CAP && gs == 32) {
+    // 3a. the listed groups' scores (one warp per group, coalesced 128-byte rows)
+    for (int l = warp; l < ng; l += NT / 32) {
+      const int e = s_gl[l] * 32 + lane;
+      s_ck[l * 32 + lane] = e < vis ? f32_to_key(__ldcg(srow + e)) : 0u;
+    }
+    __syncthreads();
+    // 3b. compact the keys >= theta (and not empty) in index order
+    constexpr int PER = CAP / NT;
+    int n = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int c = tid * PER + u;
+      n += (c < C && s_ck[c] >= theta && s_ck[c] != 0u) ? 1 : 0;
+    }
+    int M;
+    int p = block_scan_excl<NT>(n, s_warp, &M);
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int c = tid * PER + u;
+      if (c < C && s_ck[c] >= theta && s_ck[c] != 0u) {
+        s_ok[p] = s_ck[c];
+        s_oi[p] = s_gl[c / 32] * 32 + (c & 31);
+        ++p;
+      }
+    }
+    __syncthreads();
+    // 3c. the exact k-th key among the candidates (M >= k: each of the k best
+    // groups has its maximum among them)
+    const uint32_t T = block_kth_hist<NT>(s_ok, M, k, s_hist, s_bc);
+    // 4. everything above T, then the lowest-index entries equal to T
+    int pk = 0;
+    for (int c = tid; c < M; c += NT) pk += (s_ok[c] > T ? 1 : 0) + (s_ok[c] == T ? 0x10000 : 0);
+    pk = block_sum<NT>(pk, s_warp);
+    const int need_eq = k - (pk & 0xFFFF), n_eq = pk >> 16;
+    int eq_seen = 0, out_pos = 0;
+    for (int cb = 0; cb < M; cb += NT) {
+      const int c = cb + tid;
+      const uint32_t key = c < M ? s_ok[c] : 0u;
+      bool sel;
+      if (n_eq == need_eq) {
+        sel = c < M && key >= T;
+      } else {
+        const bool eq = c < M && key == T;
+        int eq_tot;
+        const int eq_rank = eq_seen + block_scan_excl<NT>(eq ? 1 : 0, s_warp, &eq_tot);
+        eq_seen += eq_tot;
+        sel = c < M && (key > T || (eq && eq_rank < need_eq));
+      }
+      int sel_tot;
+      const int q = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
+      out_pos += sel_tot;
+      if (sel && q < k) {
+        oi[q] = s_oi[c];
+        if (os) os[q] = key_to_f32(key);
+      }
+    }
+    return;
+  }
+
+  // ---- massive ties: exact k-th key by bisection over the whole row ----
+  uint32_t T = 0u;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t c = T | (1u << bit);
+    int cnt = 0;
+    for (int e = tid; e < vis; e += NT) cnt += f32_to_key(__ldcg(srow + e)) >= c;
+    if (block_sum<NT>(cnt, s_warp) >= k) T = c;
+  }
+  int ngt = 0;
+  for (int e = tid; e < vis; e += NT) ngt += f32_to_key(__ldcg(srow + e)) > T;
+  const int need_eq = k - block_sum<NT>(ngt, s_warp);
+  int out_pos = 0, eq_seen = 0;
+  for (int eb = 0; eb < vis; eb += NT) {
+    const int e = eb + tid;
+    const uint32_t key = e < vis ? f32_to_key(__ldcg(srow + e)) : 0u;
+    const bool eq = e < vis && key == T;
+    int eq_tot;
+    const int eq_rank = eq_seen + block_scan_excl<NT>(eq ? 1 : 0, s_warp, &eq_tot);
+    eq_seen += eq_tot;
+    const bool sel = e < vis && (key > T || (eq && eq_rank < need_eq));
+    int sel_tot;
+    const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
+    out_pos += sel_tot;
+    if (sel && p < k) {
+      oi[p] = e;
+      if (os) os[p] = key_to_f32(key);
+    }
+  }
+}
+
+}  // namespace lcc

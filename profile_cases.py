@@ -17,6 +17,10 @@ capture (``ncu --set full``) of one launch finishes in seconds:
     csa-prefill-attn     the first Q queries (default 4096) of the CSA prefill
                          at the end of the 131072-token sequence: 128 selected
                          entries per query + the window, one softmax
+    pair-decode-index    the layer-pair decode's CSA indexer at 1M context
+                         (4 x 262160 entries, NVFP4 keys): scores only
+    csa-decode-topk      the CSA decode batch's indexer + top-k (32 x 16384
+                         entries, top-128)
 """
 from __future__ import annotations
 
@@ -31,7 +35,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 import datagen  # noqa: E402
-from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, T_KI, T_QI, T_W  # noqa: E402
+from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, PairDecode, T_KI, T_QI, T_W  # noqa: E402
 
 from long_context_compressed_15_b300 import (csa_layer_attn, hca_layer_attn, lightning_index_scores,  # noqa: E402
                                              lightning_index_topk, load)
@@ -83,8 +87,26 @@ def csa_prefill_attn(dev, nq):
     return lambda: csa_layer_attn(q, Kc, Vc, idx, Kr, Vr, t0, t0 - (c.W - 1), c.W, out=out)
 
 
+def pair_decode_index(dev, nq):
+    c = PairDecode()
+    g = c.make(dev)
+    pos = torch.full((c.B,), c.ctx, dtype=torch.int64, device=dev)
+    scores = torch.empty((c.B, 1, c.Ncap_csa), dtype=torch.float32, device=dev)
+    return lambda: lightning_index_scores(g["qI"][0][:, None], g["w"][0][:, None], pos, g["kI_packed"],
+                                          c.N_csa, c.m_csa, kI_scale=g["kI_scale"], scores=scores)
+
+
+def csa_decode_topk(dev, nq):
+    c = CsaDecode()
+    s = c.make(dev)
+    pos = torch.full((c.B,), c.q_pos, dtype=torch.int64, device=dev)
+    idx = torch.empty((c.B, 1, c.k), dtype=torch.int32, device=dev)
+    return lambda: lightning_index_topk(s["qI"], s["w"], pos, s["kI"], c.N, 4, c.k, idx=idx)
+
+
 CASES = {"index-topk-prefill": index_topk_prefill, "hca-prefill-attn": hca_prefill_attn,
-         "csa-decode-index": csa_decode_index, "csa-prefill-attn": csa_prefill_attn}
+         "csa-decode-index": csa_decode_index, "csa-prefill-attn": csa_prefill_attn,
+         "pair-decode-index": pair_decode_index, "csa-decode-topk": csa_decode_topk}
 
 
 def main(argv=None):

@@ -117,7 +117,7 @@ def _index_case(seed, B, Tq, HI, DI, Ncap, m, k, q_pos0, n_valid, nvfp4=False):
 
 @pytest.mark.parametrize("HI,DI", [(8, 64), (4, 32), (8, 32), (4, 64)])
 def test_index_topk_decode_two_stage(HI, DI):
-    # Ncap > one top-k segment: exercises the per-segment lists and their merge; ragged n_valid
+    # rows longer than 16384 entries (625 score groups of 32); ragged n_valid
     B, Ncap = 3, 20000
     near, g = _index_case(21, B, 1, HI, DI, Ncap, 4, 128, q_pos0=[4 * Ncap - 1] * B, n_valid=[Ncap, 8193, 100])
     assert np.all(g[2, 0, 100:] == -1) and np.all(g[2, 0, :100] == np.arange(100))
@@ -126,9 +126,9 @@ def test_index_topk_decode_two_stage(HI, DI):
 
 @pytest.mark.parametrize("HI,DI", [(8, 64), (4, 32)])
 def test_index_topk_decode_cluster(HI, DI):
-    # rows of up to 16384 entries go to the cluster top-k (one CTA per 2048 entries); the visible
-    # counts cover a full row, rows whose group maxima give no threshold (fewer than k groups: 4000,
-    # 2049 entries, the latter one entry into the second CTA), a row just above k and one below it
+    # the visible counts cover a full 16384-entry row, rows whose group maxima give no threshold
+    # (fewer than k groups of 32: 4000 and 2049 entries, the latter one entry into a new group),
+    # a row just above k and one below it
     B, Ncap = 5, 16384
     near, g = _index_case(26, B, 1, HI, DI, Ncap, 4, 128, q_pos0=[4 * Ncap - 1] * B,
                           n_valid=[Ncap, 4000, 2049, 129, 50])
@@ -163,6 +163,28 @@ def test_index_topk_nvfp4_keys():
     near, _ = _index_case(24, B, 2, 8, 64, Ncap, 4, 128, q_pos0=[4 * Ncap - 2] * B, n_valid=[Ncap, 5000],
                           nvfp4=True)
     assert near <= 1
+
+
+def test_index_nvfp4_scores_exact_for_any_query_scale():
+    # each (query, head) row of qI scaled by its own power of two in 2^-30 .. 2^30:
+    # rounding bf16 queries to fp16 would lose or overflow them; the per-row
+    # power-of-two scaling keeps the scores at fp32 accuracy
+    B, Tq, N, HI, DI = 2, 3, 3000, 8, 64
+    kp, ks = datagen.nvfp4_normal(19, 1, B * N, DI)
+    kI, kIs = kp.reshape(B, N, DI // 2).to(DEV), ks.reshape(B, N, DI // 16).to(DEV)
+    exps = (torch.arange(B * Tq * HI, dtype=torch.float32).reshape(B, Tq, HI, 1) * 17) % 61 - 30
+    qI = (datagen.normal_bf16(19, 2, (B, Tq, HI, DI)).float() * torch.exp2(exps)).to(torch.bfloat16).to(DEV)
+    w = (datagen.uniform_f32(19, 3, (B, Tq, HI)) * torch.exp2(-exps[..., 0])).to(DEV)
+    pos = torch.full((B,), 4 * N - Tq, dtype=torch.int64, device=DEV)
+    sc = lcc.lightning_index_scores(qI, w, pos, kI, N, 4, kI_scale=kIs)
+    torch.cuda.synchronize()
+    for b in range(B):
+        keys = oracle.nvfp4_decode(host(kI[b]), host(kIs[b]))
+        for i in range(Tq):
+            nv = oracle.visible_count(4 * N - Tq + i, 4, N)
+            want = oracle.index_scores(f64(qI[b, i]), host(w[b, i]).astype(np.float64), keys[:nv])
+            got = sc[b, i, :nv].cpu().numpy().astype(np.float64)
+            np.testing.assert_allclose(got, want, rtol=1e-5, atol=1e-5 * np.max(np.abs(want)))
 
 
 def test_index_topk_scores_output():
