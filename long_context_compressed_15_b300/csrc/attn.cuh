@@ -100,7 +100,18 @@ __device__ __forceinline__ void attn_row_bounds(const AttnArgs& a, int b, int qi
 // tile position j0+kk outside a row's [lo, hi) are masked.  Online softmax in
 // the log2 domain: m = running max of scale*log2(e)*q.k, l = running sum of
 // 2^(z - m), oacc = unnormalised output.
-template <int D, int KT = 64>
+// Element offset of 16-byte chunk cc of key row `key` in a K/V tile.  Plain
+// layout: rows of D elements, chunks XOR-swizzled by key & 7.  Split layout
+// (what TMA writes with 128-byte swizzling from tensor maps whose box is 64
+// columns wide): the tile is stored as D/64 halves of KT rows x 128 bytes,
+// chunk c of a half at position c ^ (key & 7) -- the same swizzle per half.
+template <int D, int KT, bool SPLIT>
+__device__ __forceinline__ int kv_off(int key, int cc) {
+  if constexpr (SPLIT) return (cc >> 3) * KT * 64 + key * 64 + (((cc & 7) ^ (key & 7)) * 8);
+  else return key * D + ((cc ^ (key & 7)) * 8);
+}
+
+template <int D, int KT = 64, bool SPLIT = false>
 __device__ __forceinline__ void attn_tile_step(const uint32_t (&qf)[D / 16][4], const bf16* tK, const bf16* tV,
                                                const int* keyv, int j0, int lA, int hA, int lB, int hB,
                                                float scale_log2, float& m0, float& m1, float& l0, float& l1,
@@ -118,7 +129,7 @@ __device__ __forceinline__ void attn_tile_step(const uint32_t (&qf)[D / 16][4], 
       const int key = 16 * p + (lane & 7) + ((lane >> 4) & 1) * 8;
       const int cc = 2 * ks + ((lane >> 3) & 1);
       uint32_t b0, b1, b2, b3;
-      ldsm_x4(smem_u32(tK + key * D + ((cc ^ (key & 7)) * 8)), b0, b1, b2, b3);
+      ldsm_x4(smem_u32(tK + kv_off<D, KT, SPLIT>(key, cc)), b0, b1, b2, b3);
       mma_bf16(s[2 * p], qf[ks], b0, b1);
       mma_bf16(s[2 * p + 1], qf[ks], b2, b3);
     }
@@ -177,7 +188,7 @@ __device__ __forceinline__ void attn_tile_step(const uint32_t (&qf)[D / 16][4], 
       const int key = 16 * ks + (lane & 7) + ((lane >> 3) & 1) * 8;
       const int cc = 2 * p + (lane >> 4);
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(smem_u32(tV + key * D + ((cc ^ (key & 7)) * 8)), b0, b1, b2, b3);
+      ldsm_x4_t(smem_u32(tV + kv_off<D, KT, SPLIT>(key, cc)), b0, b1, b2, b3);
       mma_bf16(oacc[2 * p], pa, b0, b1);
       mma_bf16(oacc[2 * p + 1], pa, b2, b3);
     }

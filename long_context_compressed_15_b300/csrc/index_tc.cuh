@@ -511,26 +511,33 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
       const int entry = (t_lo + t) * F::TILE + quarter * 32 + lane;
       constexpr int QPC = 8 / HI < 1 ? 1 : 8 / HI;
       constexpr int NCH = (C::NREAL + 7) / 8;
-#pragma unroll 4
-      for (int ch = 0; ch < NCH; ++ch) {
-        float v[8];
-        tc::tmem_ld8(lane_addr + acc * C::N + ch * 8, v);
+      static_assert(NCH % 2 == 0, "columns in pairs of 8-column chunks");
+#pragma unroll 2
+      for (int ch2 = 0; ch2 < NCH; ch2 += 2) {
+        // two 8-column chunks per TMEM round trip
+        float v16[16];
+        tc::tmem_ld16(lane_addr + acc * C::N + ch2 * 8, v16);
         tc::tmem_wait_ld();
 #pragma unroll
-        for (int qq = 0; qq < QPC; ++qq) {
-          const int qi = ch * QPC + qq;
-          const int q = qg0 + qi;
-          if (qi < NQ && q < qend) {
-            float sc = 0.f;
+        for (int half = 0; half < 2; ++half) {
+          const int ch = ch2 + half;
+          const float* v = v16 + half * 8;
 #pragma unroll
-            for (int h = 0; h < HI; ++h) sc = fmaf(sW[qi * HI + h], fmaxf(v[qq * HI + h], 0.f), sc);
-            const int vis = sVis[qi];
-            const int64_t rr = static_cast<int64_t>(b) * a.nq + (q - a.q0);
-            if (entry < vis) a.scores[rr * a.Ncap + entry] = sc;
-            if (a.gmax) {
-              const uint32_t key = __reduce_max_sync(0xffffffffu, entry < vis ? f32_to_key(sc) : 0u);
-              const int g0 = entry - lane;
-              if (lane == 0 && g0 < vis) a.gmax[rr * a.g_stride + (g0 >> 5)] = key;
+          for (int qq = 0; qq < QPC; ++qq) {
+            const int qi = ch * QPC + qq;
+            const int q = qg0 + qi;
+            if (qi < NQ && q < qend) {
+              float sc = 0.f;
+#pragma unroll
+              for (int h = 0; h < HI; ++h) sc = fmaf(sW[qi * HI + h], fmaxf(v[qq * HI + h], 0.f), sc);
+              const int vis = sVis[qi];
+              const int64_t rr = static_cast<int64_t>(b) * a.nq + (q - a.q0);
+              if (entry < vis) a.scores[rr * a.Ncap + entry] = sc;
+              if (a.gmax) {
+                const uint32_t key = __reduce_max_sync(0xffffffffu, entry < vis ? f32_to_key(sc) : 0u);
+                const int g0 = entry - lane;
+                if (lane == 0 && g0 < vis) a.gmax[rr * a.g_stride + (g0 >> 5)] = key;
+              }
             }
           }
         }

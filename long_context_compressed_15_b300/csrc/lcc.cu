@@ -22,6 +22,7 @@
 #include "attn.cuh"
 #include "attn_tc.cuh"
 #include "attn_gather_tc.cuh"
+#include "attn_decode_tma.cuh"
 #include "index.cuh"
 #include "index_tc.cuh"
 #include "index_topk_tc.cuh"
@@ -134,15 +135,18 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
              reinterpret_cast<bf16*>(Kc), reinterpret_cast<bf16*>(Vc), c_bs};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (m <= 4) {
+    constexpr int NB = 4;  // blocks per (half-)warp
     const int bpw = 32 / (2 * (D / 8));
-    dim3 grid((nblk + 8 * bpw - 1) / (8 * bpw), B);
-    if (grid.x > 0x7FFFFFFFu) return fail(LCC_ERR_SHAPE, "%s: too many blocks", name);
+    const int64_t per_cta = 8LL * bpw * NB;
+    const int64_t gx = (nblk + per_cta - 1) / per_cta;
+    if (gx > 0x7FFFFFFF) return fail(LCC_ERR_SHAPE, "%s: too many blocks", name);
+    dim3 grid(static_cast<unsigned>(gx), B);
     if (m == 4) {
-      if (D == 128) k_pool_small<4, 128><<<grid, 256, 0, s>>>(a);
-      else k_pool_small<4, 64><<<grid, 256, 0, s>>>(a);
+      if (D == 128) k_pool_small<4, 128, NB><<<grid, 256, 0, s>>>(a);
+      else k_pool_small<4, 64, NB><<<grid, 256, 0, s>>>(a);
     } else {  // m = 1: every token is its own entry (softmax over one logit = 1)
-      if (D == 128) k_pool_small<1, 128><<<grid, 256, 0, s>>>(a);
-      else k_pool_small<1, 64><<<grid, 256, 0, s>>>(a);
+      if (D == 128) k_pool_small<1, 128, NB><<<grid, 256, 0, s>>>(a);
+      else k_pool_small<1, 64, NB><<<grid, 256, 0, s>>>(a);
     }
   } else {
     dim3 grid(nblk, B);
@@ -968,6 +972,26 @@ lcc_status launch_wsplit(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pd
   return launch_check("k_attn_wsplit");
 }
 
+// CSA layer decode with the selected entries gathered by TMA (D = 128).
+unsigned long long g_wsplit_tma_done = 0;
+lcc_status launch_wsplit_tma(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pdl) {
+  using Sm = WsplitTmaSmem<kWsplitWarps, kWsplitTile>;
+  CUtensorMap tk, tv;
+  const uint64_t rows = static_cast<uint64_t>(a.B) * a.Ncap;
+  lcc_status st = make_tmap_2d(&tk, a.K, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_wsplit_tma K");
+  if (st != LCC_OK) return st;
+  if ((st = make_tmap_2d(&tv, a.V, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_wsplit_tma V")) !=
+      LCC_OK)
+    return st;
+  auto kern = k_attn_wsplit_tma<kWsplitWarps, kWsplitTile>;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(kern, Sm::total, g_wsplit_tma_done)) != LCC_OK) return st;
+  }
+  launch_k(kern, dim3(gx, a.B), dim3(kWsplitWarps * 32), Sm::total, s, pdl, tk, tv, a);
+  return launch_check("k_attn_wsplit_tma");
+}
+
 // One pass over (compressed source ++ window rows) -> bf16 layer output.
 template <int MODE>
 lcc_status layer_attn_impl(const char* name, AttnArgs a, int D, int64_t rowblocks, unsigned gx, int rows_per_cta,
@@ -978,6 +1002,9 @@ lcc_status layer_attn_impl(const char* name, AttnArgs a, int D, int64_t rowblock
     a.out_bf16 = reinterpret_cast<bf16*>(out);
     a.lse = lse_out;
     const unsigned gw = static_cast<unsigned>(static_cast<int64_t>(a.Tq) * ((a.H + 15) / 16));
+    // selected entries by TMA gather (row numbers of the tensor map fit 31 bits)
+    if (MODE == ATT_GATHER && D == 128 && static_cast<int64_t>(a.B) * a.Ncap < (int64_t(1) << 31))
+      return launch_wsplit_tma(a, gw, s, pdl);
     return D == 128 ? launch_wsplit<128, MODE>(a, gw, s, pdl) : launch_wsplit<64, MODE>(a, gw, s, pdl);
   }
   const int ns = splits_for(rowblocks, keys);

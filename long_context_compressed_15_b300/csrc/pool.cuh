@@ -81,19 +81,51 @@ __device__ __forceinline__ void pool_block_small(const float* g, const bf16* K, 
   *reinterpret_cast<uint4*>((isV ? Vc : Kc) + col) = pack8(acc);
 }
 
-// Small blocks (m <= 16): each (half-)warp pools one block.
-template <int M, int D>
+// Small blocks (m <= 16): each (half-)warp pools NB blocks, every block's
+// loads issued before any arithmetic, so that each lane keeps NB * M 16-byte
+// loads in flight; the arithmetic is pool_block_small's.
+template <int M, int D, int NB>
 __global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
   constexpr int LPB = 2 * (D / 8);    // lanes per block (K and V)
-  constexpr int BPW = 32 / LPB;       // blocks per warp
+  constexpr int BPW = 32 / LPB;       // blocks per warp and pass
+  constexpr int LPR = D / 8;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / LPB;
+  const int sub = lane / LPB, li = lane % LPB;
+  const int isV = li / LPR, col = (li % LPR) * 8;
   const int b = blockIdx.y;
-  const int64_t blk = (static_cast<int64_t>(blockIdx.x) * 8 + warp) * BPW + sub;
-  if (blk >= a.nblk) return;
-  pool_block_small<M, D, true>(a.gate + b * a.g_bs + blk * M, a.K + b * a.kv_bs + blk * M * D,
-                         a.V + b * a.kv_bs + blk * M * D, a.Kc + b * a.c_bs + blk * D, a.Vc + b * a.c_bs + blk * D,
-                         lane % LPB);
+  // the CTA's NB passes cover 8 * BPW * NB consecutive blocks
+  const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * 8 * BPW * NB + warp * BPW + sub;
+  uint4 v[NB][M];
+  float gv[NB][M];
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int64_t blk = blk0 + static_cast<int64_t>(n) * 8 * BPW;
+    if (blk < a.nblk) {
+      const bf16* src = (isV ? a.V : a.K) + b * a.kv_bs + blk * M * D + col;
+      const float* g = a.gate + b * a.g_bs + blk * M;
+#pragma unroll
+      for (int i = 0; i < M; ++i) {
+        v[n][i] = ld16<true>(src + i * D);
+        gv[n][i] = __ldg(g + i);
+      }
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < NB; ++n) {
+    const int64_t blk = blk0 + static_cast<int64_t>(n) * 8 * BPW;
+    if (blk >= a.nblk) break;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < M; ++i) mx = fmaxf(mx, gv[n][i]);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < M; ++i) { gv[n][i] = expf(gv[n][i] - mx); sum += gv[n][i]; }
+    const float inv = 1.0f / sum;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+#pragma unroll
+    for (int i = 0; i < M; ++i) fma8(acc, gv[n][i] * inv, v[n][i]);
+    *reinterpret_cast<uint4*>((isV ? a.Vc : a.Kc) + b * a.c_bs + blk * D + col) = pack8(acc);
+  }
 }
 
 // Shared memory of pool_block_large.

@@ -119,6 +119,30 @@ __device__ __forceinline__ uint32_t block_kth_hist(const uint32_t* vals, int n, 
   return lo;
 }
 
+// k-th largest of vals[0..n) (1 <= k <= n <= 32*PL) by one warp, without
+// block barriers: T is built bit by bit from the top as the largest key with
+// at least k values >= T (each lane counts its PL values, one warp
+// reduction per bit).  Returned to every lane of the calling warp.
+template <int PL>
+__device__ __forceinline__ uint32_t warp_kth_bits(const uint32_t* vals, int n, int k) {
+  const int lane = threadIdx.x & 31;
+  uint32_t v[PL];
+#pragma unroll
+  for (int j = 0; j < PL; ++j) {
+    const int i = j * 32 + lane;
+    v[j] = i < n ? vals[i] : 0u;
+  }
+  uint32_t T = 0u;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t c = T | (1u << bit);
+    int cnt = 0;
+#pragma unroll
+    for (int j = 0; j < PL; ++j) cnt += v[j] >= c ? 1 : 0;
+    if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cnt))) >= k) T = c;
+  }
+  return T;
+}
+
 template <int NT, int PER, int CAP, int MAXG>
 struct TopkClSmem {
   static constexpr size_t ck = 0;                   // candidate keys, in arrival order (CTA 0)
@@ -209,7 +233,17 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
       s_g[s] = mx;
     }
     __syncthreads();
-    theta = block_kth_hist<NT>(s_g, Gs, k, s_hist, s_bc);
+    if (Gs <= 256) {  // one warp, no block barriers (Gs <= 2k super-groups by construction)
+      if (tid < 32) {
+        const uint32_t th = warp_kth_bits<8>(s_g, Gs, k);
+        if (tid == 0) s_bc[0] = th;
+      }
+      __syncthreads();
+      theta = s_bc[0];
+      __syncthreads();
+    } else {
+      theta = block_kth_hist<NT>(s_g, Gs, k, s_hist, s_bc);
+    }
   }
 
   // this CTA's run of candidates, stored into CTA 0
@@ -263,7 +297,17 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
       }
     }
     __syncthreads();
-    const uint32_t T = block_kth_hist<NT>(s_ok, C, k, s_hist, s_bc);
+    uint32_t T;
+    if (C <= 512) {  // the usual case (a few hundred candidates): one warp, no block barriers
+      if (tid < 32) {
+        const uint32_t t = warp_kth_bits<16>(s_ok, C, k);
+        if (tid == 0) s_bc[0] = t;
+      }
+      __syncthreads();
+      T = s_bc[0];
+    } else {
+      T = block_kth_hist<NT>(s_ok, C, k, s_hist, s_bc);
+    }
     int pk = 0;
     for (int c = tid; c < C; c += NT) pk += (s_ok[c] > T ? 1 : 0) + (s_ok[c] == T ? 0x10000 : 0);
     pk = block_sum<NT>(pk, s_warp);

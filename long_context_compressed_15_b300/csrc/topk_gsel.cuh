@@ -119,7 +119,17 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
     __syncthreads();
     // 3c. the exact k-th key among the candidates (M >= k: each of the k best
     // groups has its maximum among them)
-    const uint32_t T = block_kth_hist<NT>(s_ok, M, k, s_hist, s_bc);
+    uint32_t T;
+    if (M <= 512) {  // the usual case: one warp, no block barriers
+      if (tid < 32) {
+        const uint32_t t = warp_kth_bits<16>(s_ok, M, k);
+        if (tid == 0) s_bc[0] = t;
+      }
+      __syncthreads();
+      T = s_bc[0];
+    } else {
+      T = block_kth_hist<NT>(s_ok, M, k, s_hist, s_bc);
+    }
     // 4. everything above T, then the lowest-index entries equal to T
     int pk = 0;
     for (int c = tid; c < M; c += NT) pk += (s_ok[c] > T ? 1 : 0) + (s_ok[c] == T ? 0x10000 : 0);

@@ -353,8 +353,9 @@ def test_merge_parity(nb, D):
 # ---------------------------------------------------------------------------
 # whole layers in one pass: compressed keys ++ window keys, one softmax
 # ---------------------------------------------------------------------------
-# the first three run the warp-split kernel (short key lists); the last is long enough for the
-# split-across-CTAs path with its combine kernel
+# the first three run the warp-split kernels (short key lists; with D = 128 the selected entries
+# arrive by TMA gather4, including empty lists and a ragged k = 70); the last is long enough for
+# the split-across-CTAs path with its combine kernel
 @pytest.mark.parametrize("B,Tq,H,D,k,W,Ncap", [(3, 1, 64, 128, 128, 128, 400), (2, 40, 8, 64, 16, 32, 400),
                                                (1, 7, 16, 128, 70, 100, 400), (2, 1, 64, 128, 1000, 128, 1500)])
 def test_csa_layer_attn_parity(B, Tq, H, D, k, W, Ncap):
