@@ -58,7 +58,7 @@ struct IndexTcCfg {
   static constexpr int OFF_W = OFF_B + (B_BYTES + 1023) / 1024 * 1024;
   static constexpr int OFF_VIS = OFF_W + (NQ * HI * 4 + 15) / 16 * 16;
   static constexpr int OFF_BAR = OFF_VIS + (NQ * 4 + 15) / 16 * 16;
-  static constexpr int NBAR = 2 * STAGES + 4;
+  static constexpr int NBAR = 2 * STAGES + 8;          // full, empty, up to 4 accumulators ready / drained
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;  // + alignment slack
   static constexpr uint32_t IDESC = tc::idesc_f16(128, N, true);
 };
@@ -75,9 +75,14 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;                 // [STAGES] key tile landed
   uint64_t* empty = bars + STAGES;       // [STAGES] key tile consumed by the MMA
-  uint64_t* tfull = bars + 2 * STAGES;   // [2] accumulator ready
-  uint64_t* tempty = bars + 2 * STAGES + 2;  // [2] accumulator drained
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  // accumulators in TMEM: four when they are narrow (the MMA may run three tiles
+  // ahead of the epilogue), two at N = 128 (three CTAs per SM share 512 columns)
+  constexpr int NACC = C::N <= 64 ? 4 : 2;
+  constexpr uint32_t TMEM_COLS = NACC * C::N <= 32 ? 32 : NACC * C::N <= 64 ? 64 : NACC * C::N <= 128 ? 128 : 256;
+  static_assert(NACC * C::N <= 256 && (2 * STAGES + 2 * NACC) * 8 + 8 <= C::NBAR * 8 + 16, "TMEM / barrier room");
+  uint64_t* tfull = bars + 2 * STAGES;   // [NACC] accumulator ready
+  uint64_t* tempty = tfull + NACC;       // [NACC] accumulator drained
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + NACC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
   // launched as a programmatic dependent of whatever ran before on the
@@ -98,7 +103,7 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { tc::mbar_init(full + i, 1); tc::mbar_init(empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
+    for (int i = 0; i < NACC; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
     *s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
       tc::tma_load_2d(sA + t * C::A_BYTES, &tmap_k, full + t, 0, row0 + t * C::TILE);
     }
   }
-  if (warp == 1) tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc(s_tmem, TMEM_COLS);
   if (warp >= 2) {
     // B operand: row n = (query n / HI, head n % HI), K-major, swizzled like the TMA tiles
     const int t = threadIdx.x - 64;
@@ -172,8 +177,8 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
-        const int s = t % STAGES, acc = t & 1;
-        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t >> 1) & 1) ^ 1, 3)) { *s_abort = 1; break; }
+        const int s = t % STAGES, acc = t % NACC;
+        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t / NACC) & 1) ^ 1, 3)) { *s_abort = 1; break; }
         if (*s_abort || !tc::mbar_wait(full + s, (t / STAGES) & 1, 4)) { *s_abort = 1; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem + acc * C::N;
@@ -187,7 +192,7 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
         tc::mma_commit(tfull + acc);
         issued = t + 1;
       }
-      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 5);
+      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) % NACC), ((issued - 1) / NACC) & 1, 5);
     }
     __syncwarp();
   } else {
@@ -195,9 +200,9 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
     const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int t = 0; t < ntiles; ++t) {
-      const int acc = t & 1;
+      const int acc = t % NACC;
       // the TMEM loads below are warp-collective: leave the loop as a whole warp
-      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 6))) {
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t / NACC) & 1, 6))) {
         *s_abort = 1;
         break;
       }
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    tc::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -282,7 +287,10 @@ struct IndexTcFp4Smem {
   static constexpr int OFF_W = OFF_RAW + SR * F::RAW_BYTES;
   static constexpr int OFF_VIS = OFF_W + (NQ * HI * 4 + 15) / 16 * 16;
   static constexpr int OFF_BAR = OFF_VIS + (NQ * 4 + 15) / 16 * 16;
-  static constexpr int NBAR = 2 * SR + 2 * SC + 4;
+  // accumulators: four narrow ones (N <= 64), else two (two CTAs per SM share 512 columns)
+  static constexpr int NACC = N <= 64 ? 4 : 2;
+  static constexpr uint32_t TMEM_COLS = NACC * N <= 32 ? 32 : NACC * N <= 64 ? 64 : NACC * N <= 128 ? 128 : 256;
+  static constexpr int NBAR = 2 * SR + 2 * SC + 2 * NACC;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 16 + 1024;
   static constexpr uint32_t IDESC = tc::idesc_f16(128, N, false);     // fp16 x fp16 -> fp32
   static constexpr uint32_t SBO = 8 * F::ROWB;
@@ -306,8 +314,9 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   uint64_t* rempty = bars + SR;              // [SR] packed tile read by the converters
   uint64_t* cfull = bars + 2 * SR;           // [SC] converted tile written
   uint64_t* cempty = bars + 2 * SR + SC;     // [SC] converted tile consumed by the MMA
-  uint64_t* tfull = bars + 2 * SR + 2 * SC;  // [2] accumulator ready
-  uint64_t* tempty = tfull + 2;              // [2] accumulator drained
+  constexpr int NACC = S::NACC;
+  uint64_t* tfull = bars + 2 * SR + 2 * SC;  // [NACC] accumulator ready
+  uint64_t* tempty = tfull + NACC;           // [NACC] accumulator drained
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + S::NBAR);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
@@ -328,7 +337,7 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < SR; ++i) { tc::mbar_init(rfull + i, 1); tc::mbar_init(rempty + i, 128); }
     for (int i = 0; i < SC; ++i) { tc::mbar_init(cfull + i, 128); tc::mbar_init(cempty + i, 1); }
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
+    for (int i = 0; i < NACC; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
     *s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -362,7 +371,7 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   };
   if (warp == 0 && lane == 0)
     for (int t = 0; t < min(SR, ntiles); ++t) issue(t);
-  if (warp == 1) tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc(s_tmem, S::TMEM_COLS);
   if (warp >= 2 && warp < 6) {
     // B operand: row n = (query n / HI, head n % HI), fp16 after a power-of-two
     // scale, K-major, swizzled like the converted tiles; head weight times the
@@ -441,8 +450,8 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
-        const int c = t % SC, acc = t & 1;
-        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t >> 1) & 1) ^ 1, 13)) { *s_abort = 1; break; }
+        const int c = t % SC, acc = t % NACC;
+        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t / NACC) & 1) ^ 1, 13)) { *s_abort = 1; break; }
         if (*s_abort || !tc::mbar_wait(cfull + c, (t / SC) & 1, 14)) { *s_abort = 1; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem + acc * C::N;
@@ -456,7 +465,7 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
         tc::mma_commit(tfull + acc);
         issued = t + 1;
       }
-      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 15);
+      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) % NACC), ((issued - 1) / NACC) & 1, 15);
     }
     __syncwarp();
   } else if (warp >= 6) {
@@ -502,8 +511,8 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
     const int quarter = warp & 3;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     for (int t = 0; t < ntiles; ++t) {
-      const int acc = t & 1;
-      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 18))) {
+      const int acc = t % NACC;
+      if (!__all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t / NACC) & 1, 18))) {
         *s_abort = 1;
         break;
       }
@@ -550,7 +559,7 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    tc::tmem_dealloc(tmem, S::TMEM_COLS);
   }
 }
 

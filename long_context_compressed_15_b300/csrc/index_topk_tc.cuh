@@ -534,9 +534,14 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
+  // NACC accumulators in TMEM (4 x 128 columns = all 512): the MMA can run three
+  // tiles ahead of the epilogue, whose per-tile latency is the bottleneck
+  constexpr int NACC = 4;
+  constexpr uint32_t TMEM_COLS = NACC * C::N;
+  static_assert(TMEM_COLS <= 512 && (2 * STAGES + 2 * NACC) * 8 + 8 <= C::NBAR * 8 + 64, "TMEM / barrier room");
   uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+  uint64_t* tempty = tfull + NACC;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + NACC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
   uint32_t* sKeys = reinterpret_cast<uint32_t*>(smem + X::OFF_KEYS);  // [NQ][4][CAPB]
   int32_t* sIds = reinterpret_cast<int32_t*>(smem + X::OFF_IDS);      // [NQ][4][CAPB]
@@ -558,7 +563,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) { tc::mbar_init(full + i, 1); tc::mbar_init(empty + i, 1); }
-    for (int i = 0; i < 2; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, NEPI); }
+    for (int i = 0; i < NACC; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, NEPI); }
     *s_abort = 0;
     tc::fence_barrier_init();
   }
@@ -571,7 +576,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       tc::tma_load_2d(sA + t * C::A_BYTES, &tmap_k, full + t, 0, row0 + t * C::TILE);
     }
   }
-  if (warp == 1) tc::tmem_alloc(s_tmem, C::TMEM_COLS);
+  if (warp == 1) tc::tmem_alloc(s_tmem, TMEM_COLS);
   if (warp >= 2) {
     const int t = threadIdx.x - 64;
     constexpr int CPR = DI / 8;
@@ -619,8 +624,8 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       const uint32_t a_base = smem_u32(sA), b_base = smem_u32(sB);
       int issued = 0;
       for (int t = 0; t < ntiles; ++t) {
-        const int s = t % STAGES, acc = t & 1;
-        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t >> 1) & 1) ^ 1, 23)) { *s_abort = 1; break; }
+        const int s = t % STAGES, acc = t % NACC;
+        if (*s_abort || !tc::mbar_wait(tempty + acc, ((t / NACC) & 1) ^ 1, 23)) { *s_abort = 1; break; }
         if (*s_abort || !tc::mbar_wait(full + s, (t / STAGES) & 1, 24)) { *s_abort = 1; break; }
         tc::tc_fence_after();
         const uint32_t d = tmem + acc * C::N;
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
         tc::mma_commit(tfull + acc);
         issued = t + 1;
       }
-      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) & 1), ((issued - 1) >> 1) & 1, 25);
+      if (issued > 0) tc::mbar_wait(tfull + ((issued - 1) % NACC), ((issued - 1) / NACC) & 1, 25);
     }
     __syncwarp();
   } else {
@@ -654,8 +659,8 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
     }
     auto buf = [&](int j) { return ((grpq * QG + j) * 4 + quarter) * CAPB; };
     for (int t = 0; t < ntiles; ++t) {
-      const int acc = t & 1;
-      const bool wok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t >> 1) & 1, 26));
+      const int acc = t % NACC;
+      const bool wok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t / NACC) & 1, 26));
       if (!wok) {
         *s_abort = 1;
         break;
@@ -771,7 +776,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, C::TMEM_COLS);
+    tc::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 

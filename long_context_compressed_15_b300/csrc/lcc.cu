@@ -317,7 +317,7 @@ unsigned long long g_index_fp4_done[2] = {};
 // converter warpgroup (k_index_tc_fp4); key-range splits as k_index_tc.
 template <int NQ>
 lcc_status launch_index_fp4_q(const IndexArgs& ia, int bit, cudaStream_t s) {
-  constexpr int HI = 8, DI = 64, SR = 6, SC = 3;
+  constexpr int HI = 8, DI = 64, SR = 6, SC = 4;
   using Sm = IndexTcFp4Smem<HI, DI, NQ, SR, SC>;
   auto kern = k_index_tc_fp4<HI, DI, NQ, SR, SC>;
   {

@@ -11,8 +11,8 @@
 // consecutive entries).  theta = the k-th largest group maximum is a lower
 // bound of the row's k-th largest score, so every winner lies in a group
 // whose maximum reaches theta -- at most k groups plus those tied at theta.
-//   1. the row's group maxima are loaded and theta is selected (256-bin
-//      histogram rounds);
+//   1. the row's group maxima are loaded and theta is selected (one warp
+//      counting bits for up to 512 groups, 256-bin histogram rounds beyond);
 //   2. the groups whose maximum reaches theta are listed in index order
 //      (one block scan) and only their scores are read, one warp per group;
 //   3. the scores >= theta are compacted in index order (typically little
@@ -69,8 +69,22 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
   const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
   for (int g = tid; g < G; g += NT) s_g[g] = __ldcg(gm + g);
   __syncthreads();
-  // 1. theta (0 when fewer than k groups: every group is listed)
-  const uint32_t theta = G >= k ? block_kth_hist<NT>(s_g, G, k, s_hist, s_bc) : 0u;
+  // 1. theta (0 when fewer than k groups: every group is listed); one warp
+  // counting bits when the groups fit its registers, histogram rounds otherwise
+  uint32_t theta = 0u;
+  if (G >= k) {
+    if (G <= 512) {
+      if (tid < 32) {
+        const uint32_t th = warp_kth_bits<16>(s_g, G, k);
+        if (tid == 0) s_bc[0] = th;
+      }
+      __syncthreads();
+      theta = s_bc[0];
+      __syncthreads();
+    } else {
+      theta = block_kth_hist<NT>(s_g, G, k, s_hist, s_bc);
+    }
+  }
   // 2. groups whose maximum reaches theta, in index order
   int ng = 0;
   {

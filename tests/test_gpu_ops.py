@@ -453,6 +453,35 @@ def test_index_topk_prefill_fused_parity(DI, k):
     assert near <= 2
 
 
+@pytest.mark.parametrize("Ncap,Tq,q0,k", [(20000, 200, 4 * 20000 - 200, 128), (2000, 800, 0, 128),
+                                           (30000, 48, 4 * 30000 - 48, 1), (6000, 100, 4 * 6000 - 100, 16)])
+def test_index_topk_prefill_passes_parity(Ncap, Tq, q0, k):
+    # the prefill top-k fused into the indexer (8 heads): long rows; a causal block from
+    # position 0 (empty rows, rows below k, short rows); k = 1; a short k
+    near, g = _index_case(28, 1, Tq, 8, 64, Ncap, 4, k, q_pos0=[q0], n_valid=[Ncap])
+    assert near <= 2
+
+
+def test_index_topk_prefill_passes_integer_score_ties():
+    # scores that are small integers (binary keys, one head): thousands of exact ties around the
+    # k-th score (candidate buffers fill with equal keys); the result must be bit-exact
+    B, Tq, HI, DI, Ncap, k = 1, 64, 8, 64, 12000, 100
+    qI = torch.ones((B, Tq, HI, DI), dtype=torch.bfloat16)
+    w = torch.zeros((B, Tq, HI), dtype=torch.float32)
+    w[..., 0] = 1.0
+    bits01 = (datagen.uniform_f32(29, 1, (B, Ncap, DI)) < 0.3).to(torch.bfloat16)
+    q0 = 4 * Ncap - Tq
+    idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), q0, bits01.to(DEV), Ncap, 4, k)
+    torch.cuda.synchronize()
+    g = idx.cpu().numpy()[0]
+    kI = f64(bits01[0])
+    for i in range(Tq):
+        vis = min(Ncap, (q0 + i + 1) // 4)
+        sc = oracle.index_scores(f64(qI[0, i]), host(w[0, i]).astype(np.float64), kI[:vis])
+        want, _ = oracle.topk_select(sc, k)
+        assert np.array_equal(g[i], want), f"row {i}"
+
+
 def test_index_topk_prefill_fused_zero_score_ties():
     # prefill-shaped calls keep a running top-k inside the indexer; with zero weights every score
     # ties, so each query must keep its lowest visible indices (candidate buffers compact often)
