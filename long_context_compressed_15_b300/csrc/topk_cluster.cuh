@@ -143,6 +143,42 @@ __device__ __forceinline__ uint32_t warp_kth_bits(const uint32_t* vals, int n, i
   return T;
 }
 
+// Rank of the value v at position pos among vals[0..n): how many values beat
+// it (a larger value, or an equal value at a lower position).  Called by whole
+// warps with pos = wb + lane, wb a multiple of 32 (the same in every lane);
+// vals 16-byte aligned in shared memory.  Positions below the warp's own
+// compare with >=, those above with >, the warp's own 32 one by one; the
+// vector loads are warp-wide broadcasts.
+__device__ __forceinline__ int rank_by_count(const uint32_t* vals, int n, uint32_t v, int wb, int pos) {
+  if (wb >= n) return 0;
+  const uint4* v4 = reinterpret_cast<const uint4*>(vals);
+  int r0 = 0, r1 = 0;
+  const int a4 = wb >> 2;
+#pragma unroll 4
+  for (int j = 0; j < a4; ++j) {
+    const uint4 u = v4[j];
+    r0 += (u.x >= v ? 1 : 0) + (u.y >= v ? 1 : 0);
+    r1 += (u.z >= v ? 1 : 0) + (u.w >= v ? 1 : 0);
+  }
+#pragma unroll
+  for (int t = 0; t < 32; ++t) {
+    const int j = wb + t;
+    if (j < n) {
+      const uint32_t u = vals[j];
+      r0 += (u > v || (u == v && j < pos)) ? 1 : 0;
+    }
+  }
+  const int b = wb + 32, n4 = n >> 2;
+#pragma unroll 4
+  for (int j = b >> 2; j < n4; ++j) {
+    const uint4 u = v4[j];
+    r0 += (u.x > v ? 1 : 0) + (u.y > v ? 1 : 0);
+    r1 += (u.z > v ? 1 : 0) + (u.w > v ? 1 : 0);
+  }
+  for (int j = max(b, n4 << 2); j < n; ++j) r0 += vals[j] > v ? 1 : 0;
+  return r0 + r1;
+}
+
 template <int NT, int PER, int CAP, int MAXG>
 struct TopkClSmem {
   static constexpr size_t ck = 0;                   // candidate keys, in arrival order (CTA 0)

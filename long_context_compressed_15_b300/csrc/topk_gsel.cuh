@@ -11,15 +11,16 @@
 // consecutive entries).  theta = the k-th largest group maximum is a lower
 // bound of the row's k-th largest score, so every winner lies in a group
 // whose maximum reaches theta -- at most k groups plus those tied at theta.
-//   1. the row's group maxima are loaded and theta is selected (one warp
-//      counting bits for up to 512 groups, 256-bin histogram rounds beyond);
+//   1. the row's group maxima are loaded and theta is selected (each value
+//      ranked by counting for up to NT groups, 256-bin histogram rounds beyond);
 //   2. the groups whose maximum reaches theta are listed in index order
 //      (one block scan) and only their scores are read, one warp per group;
 //   3. the scores >= theta are compacted in index order (typically little
-//      more than k of them) and the exact k-th largest key T is selected
-//      among them;
-//   4. every candidate above T and the lowest-index candidates equal to T
-//      are written, in index order.
+//      more than k of them); a candidate wins iff fewer than k others beat
+//      it (a larger key, or an equal key at a lower index);
+//   4. the winners are written in index order (for more than NT candidates:
+//      the exact k-th key T by histogram rounds, then every key above T and
+//      the lowest-index keys equal to T).
 // When the listed groups hold more than CAP entries (massive exact ties at
 // theta) the CTA falls back to a bisection over the whole row.
 #pragma once
@@ -33,7 +34,7 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
   __shared__ int s_warp[NT / 32];
   __shared__ uint32_t s_hist[256];
   __shared__ uint32_t s_bc[4];
-  const int G_cap = (a.Ncap + a.gs - 1) / a.gs;
+  const int G_cap = ((a.Ncap + a.gs - 1) / a.gs + 3) & ~3;  // keeps the arrays below 16-byte aligned
   uint32_t* s_g = sm_gsel;                 // [G_cap] group maxima
   int* s_gl = reinterpret_cast<int*>(s_g + G_cap);   // [G_cap] listed groups, index order
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_gl + G_cap);  // [CAP] keys of the listed groups
@@ -73,11 +74,11 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
   // counting bits when the groups fit its registers, histogram rounds otherwise
   uint32_t theta = 0u;
   if (G >= k) {
-    if (G <= 512) {
-      if (tid < 32) {
-        const uint32_t th = warp_kth_bits<16>(s_g, G, k);
-        if (tid == 0) s_bc[0] = th;
-      }
+    if (G <= NT) {
+      // each group maximum's rank by counting (ties by position): rank k-1 is theta
+      const uint32_t v = tid < G ? s_g[tid] : 0u;
+      const int r = rank_by_count(s_g, G, v, tid & ~31, tid);
+      if (tid < G && r == k - 1) s_bc[0] = v;
       __syncthreads();
       theta = s_bc[0];
       __syncthreads();
@@ -133,17 +134,20 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
     __syncthreads();
     // 3c. the exact k-th key among the candidates (M >= k: each of the k best
     // groups has its maximum among them)
-    uint32_t T;
-    if (M <= 512) {  // the usual case: one warp, no block barriers
-      if (tid < 32) {
-        const uint32_t t = warp_kth_bits<16>(s_ok, M, k);
-        if (tid == 0) s_bc[0] = t;
+    if (M <= NT) {
+      // the usual case: a candidate wins iff fewer than k others beat it (larger key,
+      // or an equal key at a lower index); winners written in index order by one scan
+      const uint32_t v = tid < M ? s_ok[tid] : 0u;
+      const bool win = tid < M && rank_by_count(s_ok, M, v, tid & ~31, tid) < k;
+      int tot;
+      const int q = block_scan_excl<NT>(win ? 1 : 0, s_warp, &tot);
+      if (win && q < k) {
+        oi[q] = s_oi[tid];
+        if (os) os[q] = key_to_f32(s_ok[tid]);
       }
-      __syncthreads();
-      T = s_bc[0];
-    } else {
-      T = block_kth_hist<NT>(s_ok, M, k, s_hist, s_bc);
+      return;
     }
+    const uint32_t T = block_kth_hist<NT>(s_ok, M, k, s_hist, s_bc);
     // 4. everything above T, then the lowest-index entries equal to T
     int pk = 0;
     for (int c = tid; c < M; c += NT) pk += (s_ok[c] > T ? 1 : 0) + (s_ok[c] == T ? 0x10000 : 0);
