@@ -194,7 +194,7 @@ unsigned long long g_topk_cl_done = 0;
 constexpr int kGselNT = 512;
 constexpr int kGselCap = 4096;
 unsigned long long g_topk_gsel_done = 0;
-size_t gsel_smem(int Ncap) { return static_cast<size_t>(((Ncap + 31) / 32 + 3) & ~3) * 8 + kGselCap * 12; }
+size_t gsel_smem(int Ncap) { return static_cast<size_t>(((Ncap + 31) / 32 + 3) & ~3) * 8 + kGselCap * 8; }
 bool use_gsel(int Ncap, int k) { return k <= 256 && gsel_smem(Ncap) <= 200 * 1024; }
 
 int topk_cluster_ctas(int Ncap, int k, int gs) {

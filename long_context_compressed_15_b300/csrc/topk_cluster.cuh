@@ -19,10 +19,11 @@
 //   3. CTA 0 lays the runs out in CTA (= index) order, selects the exact
 //      k-th largest key T and writes every candidate above T and the
 //      lowest-index candidates equal to T.
-// Selections use a 256-bin histogram over the current key interval, each
-// round narrowing the interval to the bin that holds the k-th value (at
-// most four rounds for 32-bit keys), so no step is quadratic in the number
-// of values.  Candidates that do not fit CAP (massive exact ties) fall back
+// Both selections (theta among the super-group maxima, T among the
+// candidates) sort up to NT values, one per thread, with a bitonic network
+// and take the k-th; larger sets take 256-bin histogram rounds, each
+// narrowing the key interval to the bin that holds the k-th value (at most
+// four rounds for 32-bit keys).  Candidates that do not fit CAP (massive exact ties) fall back
 // to a bisection over the row's scores in CTA 0.  Control flow through the
 // cluster barriers depends only on per-row values, so every CTA of the
 // cluster meets each barrier.
@@ -119,6 +120,41 @@ __device__ __forceinline__ uint32_t block_kth_hist(const uint32_t* vals, int n, 
   return lo;
 }
 
+// k-th largest (1 <= k <= NT) of the values held one per thread (v; padding
+// values must be 0), returned to every thread.  A bitonic sort network over
+// the CTA's threads into descending order: partners within a warp exchange
+// by shuffles, partners in other warps through shared memory (x: NT words).
+// Every stage is a few independent instructions per thread, so the whole
+// CTA shares the work instead of one warp walking a long dependent chain.
+template <int NT>
+__device__ __forceinline__ uint32_t block_kth_bitonic(uint32_t v, int k, uint32_t* x, uint32_t* s_bc) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int kk = 2; kk <= NT; kk <<= 1) {
+#pragma unroll
+    for (int j = kk >> 1; j > 0; j >>= 1) {
+      uint32_t u;
+      if (j < 32) {
+        u = __shfl_xor_sync(0xffffffffu, v, j);
+      } else {
+        x[tid] = v;
+        __syncthreads();
+        u = x[tid ^ j];
+        __syncthreads();
+      }
+      // blocks of kk threads alternate direction; the last merge is descending
+      const bool desc = (tid & kk) == 0;
+      const bool low = (tid & j) == 0;
+      v = (low == desc) ? max(v, u) : min(v, u);
+    }
+  }
+  if (tid == k - 1) s_bc[0] = v;
+  __syncthreads();
+  const uint32_t r = s_bc[0];
+  __syncthreads();
+  return r;
+}
+
 // k-th largest of vals[0..n) (1 <= k <= n <= 32*PL) by one warp, without
 // block barriers: T is built bit by bit from the top as the largest key with
 // at least k values >= T (each lane counts its PL values, one warp
@@ -196,6 +232,7 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
   using L = TopkClSmem<NT, PER, CAP, MAXG>;
   constexpr int SEG = NT * PER;
   static_assert(PER % 4 == 0, "4-wide loads");
+  static_assert(NT <= 256 && (NT & (NT - 1)) == 0, "the sorts exchange through s_hist, one word per thread");
   extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(smem + L::ck);
   int32_t* s_ci = reinterpret_cast<int32_t*>(smem + L::ci);
@@ -269,14 +306,8 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
       s_g[s] = mx;
     }
     __syncthreads();
-    if (Gs <= 256) {  // one warp, no block barriers (Gs <= 2k super-groups by construction)
-      if (tid < 32) {
-        const uint32_t th = warp_kth_bits<8>(s_g, Gs, k);
-        if (tid == 0) s_bc[0] = th;
-      }
-      __syncthreads();
-      theta = s_bc[0];
-      __syncthreads();
+    if (Gs <= NT) {
+      theta = block_kth_bitonic<NT>(tid < Gs ? s_g[tid] : 0u, k, s_hist, s_bc);
     } else {
       theta = block_kth_hist<NT>(s_g, Gs, k, s_hist, s_bc);
     }
@@ -334,7 +365,9 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
     }
     __syncthreads();
     uint32_t T;
-    if (C <= 512) {  // the usual case (a few hundred candidates): one warp, no block barriers
+    if (C <= NT) {  // the usual case (a few hundred candidates)
+      T = block_kth_bitonic<NT>(tid < C ? s_ok[tid] : 0u, k, s_hist, s_bc);
+    } else if (C <= 512) {  // one warp, no block barriers
       if (tid < 32) {
         const uint32_t t = warp_kth_bits<16>(s_ok, C, k);
         if (tid == 0) s_bc[0] = t;

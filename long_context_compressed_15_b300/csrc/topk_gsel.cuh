@@ -11,18 +11,23 @@
 // consecutive entries).  theta = the k-th largest group maximum is a lower
 // bound of the row's k-th largest score, so every winner lies in a group
 // whose maximum reaches theta -- at most k groups plus those tied at theta.
-//   1. the row's group maxima are loaded and theta is selected (each value
-//      ranked by counting for up to NT groups, 256-bin histogram rounds beyond);
+// The same holds for the k-th largest maximum over any partition of the
+// groups into at least k parts (a lower theta, a few more listed groups).
+//   1. the row's group maxima are loaded and theta is selected: a bitonic
+//      sort of the group maxima when there are at most NT groups, else of
+//      NT partition maxima (thread t: groups t, t+NT, ...);
 //   2. the groups whose maximum reaches theta are listed in index order
-//      (one block scan) and only their scores are read, one warp per group;
-//   3. the scores >= theta are compacted in index order (typically little
+//      (one block scan);
+//   3. only their scores are read, each thread PER consecutive entries of a
+//      group (a warp reads whole 128-byte rows), and the scores >= theta are
+//      compacted in index order straight from registers (typically little
 //      more than k of them); a candidate wins iff fewer than k others beat
 //      it (a larger key, or an equal key at a lower index);
 //   4. the winners are written in index order (for more than NT candidates:
 //      the exact k-th key T by histogram rounds, then every key above T and
 //      the lowest-index keys equal to T).
-// When the listed groups hold more than CAP entries (massive exact ties at
-// theta) the CTA falls back to a bisection over the whole row.
+// When more than CAP scores reach theta (massive exact ties) the CTA falls
+// back to a bisection over the whole row.
 #pragma once
 #include "topk_cluster.cuh"
 
@@ -30,6 +35,7 @@ namespace lcc {
 
 template <int NT, int CAP>
 __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
+  static_assert(CAP >= NT && (NT & (NT - 1)) == 0, "the sort needs a power of two and NT words of scratch");
   extern __shared__ __align__(16) uint32_t sm_gsel[];
   __shared__ int s_warp[NT / 32];
   __shared__ uint32_t s_hist[256];
@@ -37,11 +43,10 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
   const int G_cap = ((a.Ncap + a.gs - 1) / a.gs + 3) & ~3;  // keeps the arrays below 16-byte aligned
   uint32_t* s_g = sm_gsel;                 // [G_cap] group maxima
   int* s_gl = reinterpret_cast<int*>(s_g + G_cap);   // [G_cap] listed groups, index order
-  uint32_t* s_ck = reinterpret_cast<uint32_t*>(s_gl + G_cap);  // [CAP] keys of the listed groups
-  uint32_t* s_ok = s_ck + CAP;             // [CAP] compacted candidate keys
+  uint32_t* s_ok = reinterpret_cast<uint32_t*>(s_gl + G_cap);  // [CAP] candidate keys, index order
   int32_t* s_oi = reinterpret_cast<int32_t*>(s_ok + CAP);      // [CAP] their entries
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   if (tid == 0) {
     s_bc[2] = 0xFFFFFFFFu;
     s_bc[3] = 0u;
@@ -68,20 +73,33 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
   const int gs = a.gs;
   const int G = (vis + gs - 1) / gs;
   const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
-  for (int g = tid; g < G; g += NT) s_g[g] = __ldcg(gm + g);
+  for (int g0 = 0; g0 < G; g0 += 8 * NT) {  // eight loads in flight per thread
+    uint32_t gv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int g = g0 + u * NT + tid;
+      gv[u] = g < G ? __ldcg(gm + g) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int g = g0 + u * NT + tid;
+      if (g < G) s_g[g] = gv[u];
+    }
+  }
   __syncthreads();
-  // 1. theta (0 when fewer than k groups: every group is listed); one warp
-  // counting bits when the groups fit its registers, histogram rounds otherwise
+  // 1. theta (0 when fewer than k groups: every group is listed)
   uint32_t theta = 0u;
   if (G >= k) {
     if (G <= NT) {
-      // each group maximum's rank by counting (ties by position): rank k-1 is theta
-      const uint32_t v = tid < G ? s_g[tid] : 0u;
-      const int r = rank_by_count(s_g, G, v, tid & ~31, tid);
-      if (tid < G && r == k - 1) s_bc[0] = v;
-      __syncthreads();
-      theta = s_bc[0];
-      __syncthreads();
+      theta = block_kth_bitonic<NT>(tid < G ? s_g[tid] : 0u, k, s_ok, s_bc);
+    } else if (k <= NT) {
+      // theta' = k-th largest of NT partition maxima (thread t: the groups t,
+      // t+NT, ...).  k partitions reach theta', so k distinct scores do and
+      // theta' is still a lower bound of the row's k-th score; it lists a few
+      // more groups than the exact k-th group maximum would
+      uint32_t mx = 0u;
+      for (int g = tid; g < G; g += NT) mx = max(mx, s_g[g]);
+      theta = block_kth_bitonic<NT>(mx, k, s_ok, s_bc);
     } else {
       theta = block_kth_hist<NT>(s_g, G, k, s_hist, s_bc);
     }
@@ -104,36 +122,49 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
     }
   }
   __syncthreads();
-  const int C = ng * gs;
-  if (C <= CAP && gs == 32) {
-    // 3a. the listed groups' scores (one warp per group, coalesced 128-byte rows)
-    for (int l = warp; l < ng; l += NT / 32) {
-      const int e = s_gl[l] * 32 + lane;
-      s_ck[l * 32 + lane] = e < vis ? f32_to_key(__ldcg(srow + e)) : 0u;
-    }
-    __syncthreads();
-    // 3b. compact the keys >= theta (and not empty) in index order
-    constexpr int PER = CAP / NT;
-    int n = 0;
+  // 3. the listed groups' scores, NT*PER entries per pass: each thread takes
+  // PER consecutive entries of one group (two 16-byte loads), so a warp reads
+  // whole 128-byte rows; the scores >= theta are compacted in index order
+  // (one block scan per pass)
+  constexpr int PER = 8;
+  const int C = ng * 32;
+  const bool vec = (a.Ncap & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
+  int M = 0;
+  if (gs == 32) {
+    for (int c0 = 0; c0 < C && M <= CAP; c0 += NT * PER) {
+      const int c = c0 + tid * PER;
+      const int e = c < C ? s_gl[c >> 5] * 32 + (c & 31) : vis;
+      uint32_t kv[PER];
+      if (vec && e + PER <= vis) {
+        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(srow + e));
+        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(srow + e + 4));
+        kv[0] = f32_to_key(x0.x); kv[1] = f32_to_key(x0.y); kv[2] = f32_to_key(x0.z); kv[3] = f32_to_key(x0.w);
+        kv[4] = f32_to_key(x1.x); kv[5] = f32_to_key(x1.y); kv[6] = f32_to_key(x1.z); kv[7] = f32_to_key(x1.w);
+      } else {
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int c = tid * PER + u;
-      n += (c < C && s_ck[c] >= theta && s_ck[c] != 0u) ? 1 : 0;
-    }
-    int M;
-    int p = block_scan_excl<NT>(n, s_warp, &M);
-#pragma unroll
-    for (int u = 0; u < PER; ++u) {
-      const int c = tid * PER + u;
-      if (c < C && s_ck[c] >= theta && s_ck[c] != 0u) {
-        s_ok[p] = s_ck[c];
-        s_oi[p] = s_gl[c / 32] * 32 + (c & 31);
-        ++p;
+        for (int u = 0; u < PER; ++u) kv[u] = e + u < vis ? f32_to_key(__ldcg(srow + e + u)) : 0u;
       }
+      int n = 0;
+#pragma unroll
+      for (int u = 0; u < PER; ++u) n += (kv[u] >= theta && kv[u] != 0u) ? 1 : 0;
+      int tot;
+      int p = M + block_scan_excl<NT>(n, s_warp, &tot);
+#pragma unroll
+      for (int u = 0; u < PER; ++u) {
+        if (kv[u] >= theta && kv[u] != 0u) {
+          if (p < CAP) {
+            s_ok[p] = kv[u];
+            s_oi[p] = e + u;
+          }
+          ++p;
+        }
+      }
+      M += tot;
     }
-    __syncthreads();
-    // 3c. the exact k-th key among the candidates (M >= k: each of the k best
-    // groups has its maximum among them)
+  }
+  __syncthreads();
+  if (gs == 32 && M <= CAP) {
+    // M >= k: each of the k best groups (or partitions) has its maximum among them
     if (M <= NT) {
       // the usual case: a candidate wins iff fewer than k others beat it (larger key,
       // or an equal key at a lower index); winners written in index order by one scan

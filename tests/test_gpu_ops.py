@@ -482,6 +482,33 @@ def test_index_topk_prefill_passes_integer_score_ties():
         assert np.array_equal(g[i], want), f"row {i}"
 
 
+@pytest.mark.parametrize("Ncap", [16384, 20000, 300000])
+def test_index_topk_decode_integer_score_ties(Ncap):
+    # decode rows (one query per sequence) whose scores are small integers (binary keys, one
+    # head): hundreds of exact ties at the k-th score.  16384 entries take the cluster top-k,
+    # 20000 and 300000 the group-selected one (partition maxima for its threshold); the
+    # candidate lists exceed one per thread, so the histogram selections run too
+    B, HI, DI, k = 2, 8, 64, 128
+    qI = torch.ones((B, 1, HI, DI), dtype=torch.bfloat16)
+    w = torch.zeros((B, 1, HI), dtype=torch.float32)
+    w[..., 0] = 1.0
+    dens = torch.tensor([0.3, 0.5]).view(B, 1, 1)
+    bits01 = (datagen.uniform_f32(30, 1, (B, Ncap, DI)) < dens).to(torch.bfloat16)
+    pos = [4 * Ncap - 1, 4 * Ncap - 1]
+    nval = [Ncap, Ncap - 77]
+    idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), torch.tensor(pos, device=DEV), bits01.to(DEV),
+                                   torch.tensor(nval, dtype=torch.int32, device=DEV), 4, k)
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    g = idx.cpu().numpy()
+    for b in range(B):
+        vis = oracle.visible_count(pos[b], 4, nval[b])
+        sc = oracle.index_scores(f64(qI[b, 0]), host(w[b, 0]).astype(np.float64), f64(bits01[b, :vis]))
+        want, kth = oracle.topk_select(sc, k)
+        assert np.sum(sc == kth) > 1, "the case must tie at the k-th score"
+        assert np.array_equal(g[b, 0], want), f"batch {b}"
+
+
 def test_index_topk_prefill_fused_zero_score_ties():
     # prefill-shaped calls keep a running top-k inside the indexer; with zero weights every score
     # ties, so each query must keep its lowest visible indices (candidate buffers compact often)
