@@ -345,6 +345,11 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
  * knows the order of its kernels here, so the attention is launched as a
  * programmatic dependent of the top-k: it may start while the top-k runs,
  * reads the queries and window rows early and waits for the index lists.
+ * Decode-shaped calls (H a multiple of 16 up to 128, D = 128, Ncap <=
+ * (H/16) * 4096, k <= 128, a few query rows) go further: after the indexer,
+ * one thread-block cluster per query (one CTA per 16 heads) selects the
+ * top-k and attends, the index list passed between its CTAs on chip; the
+ * index lists and outputs are identical to the two calls'.
  * Arguments as the two calls; idx [B, Tq, k] int32 is written; workspace:
  * at least lcc_csa_layer_workspace(B, Tq, H, D, Ncap, k, W) bytes.
  * ---------------------------------------------------------------------- */

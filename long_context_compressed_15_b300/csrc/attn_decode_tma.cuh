@@ -34,21 +34,23 @@ struct WsplitTmaSmem {
   static constexpr size_t total = off_bars + NW * 8 + 1024;               // + alignment slack
 };
 
-template <int NW, int KT>
-__global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_constant__ CUtensorMap tmK,
-                                                             const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+// The attention of query qi of sequence b for heads h0 .. h0+15 by one CTA
+// of NW warps; smem is the CTA's 1024-aligned WsplitTmaSmem area.  The index
+// list comes from global memory (a.idx) or, with SIDX, from shared memory
+// (sidx[0..k)).  between() runs after the window rows and queries are
+// requested and before the index list is read: it waits for whatever
+// produces the list.
+template <int NW, int KT, bool SIDX, class Between>
+__device__ __forceinline__ void attn_wsplit_tma_body(const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                                     const AttnArgs& a, uint8_t* smem, int qi, int h0, int b,
+                                                     const int* sidx, Between& between) {
   constexpr int D = 128, CPR = D / 8, NKS = D / 16, NDT = D / 8;
   static_assert(KT % 4 == 0 && KT / 4 <= 32, "four rows per gather, one lane per gather");
   using S = WsplitTmaSmem<NW, KT>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   uint8_t* work = smem + S::off_work;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
-  const int hblocks = (a.H + 15) / 16;
-  const int qi = blockIdx.x / hblocks, h0 = (blockIdx.x % hblocks) * 16;
-  const int b = blockIdx.y;
   bf16* sK = reinterpret_cast<bf16*>(work + warp * S::tile_bytes);
   bf16* sV = sK + KT * D;
   int* sKey = reinterpret_cast<int*>(smem + S::off_keys) + warp * KT;
@@ -106,7 +108,7 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_consta
         const int j = j0 + 4 * lane + u;
         int e = -1;
         if (j < a.k) {
-          e = __ldg(a.idx + qrow * a.k + j);
+          e = SIDX ? sidx[j] : __ldg(a.idx + qrow * a.k + j);
           if (e >= a.Ncap || e < -1) {
             record_error(DEV_ERR_INDEX, static_cast<unsigned>(j));
             e = -1;
@@ -124,8 +126,8 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_consta
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int dst = h * KT * 128 + 4 * lane * 128;
-        gtc::tma_gather4(kb + dst, &tmK, bar, h * 64, rows[0], rows[1], rows[2], rows[3]);
-        gtc::tma_gather4(vb + dst, &tmV, bar, h * 64, rows[0], rows[1], rows[2], rows[3]);
+        gtc::tma_gather4(kb + dst, tmK, bar, h * 64, rows[0], rows[1], rows[2], rows[3]);
+        gtc::tma_gather4(vb + dst, tmV, bar, h * 64, rows[0], rows[1], rows[2], rows[3]);
       }
     }
     return j0;
@@ -138,9 +140,9 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_consta
   uint32_t qf[NKS][4];
   int j0 = 0;
   pdl_trigger();
-  // window rows are inputs of the call; index lists may come from the previous kernel
+  // window rows are inputs of the call; index lists come later
   if (warp < T1 + T2 && warp >= T1) j0 = load_window(warp);
-  pdl_wait();
+  between();
   if (warp < T1) j0 = load_gather(warp);
   cp_async_wait<0>();
   __syncthreads();  // queries visible to every warp
@@ -222,6 +224,18 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_consta
     for (int d = 0; d < DPT; d += 2) *reinterpret_cast<uint32_t*>(o + d) = pack_bf16(x[d] * inv, x[d + 1] * inv);
     if (a.lse && tid % TPR == 0) a.lse[orow] = L > 0.f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
   }
+}
+
+template <int NW, int KT>
+__global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_constant__ CUtensorMap tmK,
+                                                             const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int hblocks = (a.H + 15) / 16;
+  const int qi = blockIdx.x / hblocks, h0 = (blockIdx.x % hblocks) * 16;
+  auto wait_lists = []() { pdl_wait(); };  // index lists may come from the previous kernel
+  attn_wsplit_tma_body<NW, KT, false>(&tmK, &tmV, a, smem, qi, h0, static_cast<int>(blockIdx.y), nullptr,
+                                      wait_lists);
 }
 
 }  // namespace lcc

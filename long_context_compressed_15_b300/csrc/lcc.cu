@@ -23,6 +23,7 @@
 #include "attn_tc.cuh"
 #include "attn_gather_tc.cuh"
 #include "attn_decode_tma.cuh"
+#include "csa_decode_fused.cuh"
 #include "index.cuh"
 #include "index_tc.cuh"
 #include "index_topk_tc.cuh"
@@ -1181,13 +1182,49 @@ size_t lcc_layer_attn_workspace(int B, int Tq, int H, int D, int n_keys) {
 }  // extern "C"
 
 namespace {
-lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
-                               const int64_t* q_pos0, const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride,
-                               int Ncap, const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr,
-                               int64_t r_rstride, int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out,
-                               float* lse_out, void* workspace, size_t workspace_bytes, void* stream, bool pdl) {
-  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
-  if (B == 0 || Tq == 0) return LCC_OK;
+// ---- CSA decode: top-k and attention in one cluster per query ----
+constexpr int kCfPer = 16;  // scores per thread of the top-k (4096 per CTA)
+static_assert(kWsplitWarps * 32 == kClNT, "the fused kernel's top-k runs on the attention CTA's threads");
+using CfSmem = CsaFusedSmem<kWsplitWarps, kWsplitTile, kCfPer, kClCap, kClMaxG>;
+unsigned long long g_csa_fused_done = 0;
+
+// Decode-shaped calls whose top-k fits the cluster selection (one CTA per 16
+// heads, each loading 4096 scores) and whose attention is the warp-split
+// kernel with TMA-gathered rows.
+bool use_csa_fused(lcc_key_format fmt, int B, int Tq, int H, int D, int HI, float scale, int Ncap, int k, int Rcap,
+                   int W) {
+  if (D != 128 || H % 16 != 0 || H < 16 || H > 128) return false;
+  const int cl = H / 16;
+  const int64_t groups16 = static_cast<int64_t>(B) * Tq * cl;
+  return !use_fused_topk(fmt, Tq, HI, k) && Ncap <= cl * kClNT * kCfPer && 2 * k <= kClMaxG &&
+         static_cast<int64_t>(k) * 32 <= kClCap && !use_gather_tc(B, Tq, H, D, scale, Ncap, Rcap) &&
+         use_wsplit<ATT_GATHER>(groups16, static_cast<int64_t>(k) + W) &&
+         static_cast<int64_t>(B) * Ncap < (int64_t(1) << 31) && static_cast<int64_t>(Tq) * cl <= 0x7FFFFFFF &&
+         B <= 65535 && index_chunk(B, Tq, Ncap) >= Tq;
+}
+
+lcc_status launch_csa_fused(const AttnArgs& a, const TopkThrArgs& t, int cl, cudaStream_t s) {
+  CUtensorMap tk, tv;
+  const uint64_t rows = static_cast<uint64_t>(a.B) * a.Ncap;
+  lcc_status st = make_tmap_2d(&tk, a.K, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_csa_decode_fused K");
+  if (st != LCC_OK) return st;
+  if ((st = make_tmap_2d(&tv, a.V, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_csa_decode_fused V")) !=
+      LCC_OK)
+    return st;
+  auto kern = k_csa_decode_fused<kWsplitWarps, kWsplitTile, kCfPer, kClCap, kClMaxG>;
+  {
+    std::lock_guard<std::mutex> lk(g_attr_mu);
+    if ((st = ensure_smem(kern, CfSmem::total, g_csa_fused_done)) != LCC_OK) return st;
+  }
+  launch_kc(kern, dim3(static_cast<unsigned>(a.Tq * cl), static_cast<unsigned>(a.B)), dim3(kWsplitWarps * 32),
+            CfSmem::total, s, true, static_cast<unsigned>(cl), tk, tv, a, t);
+  return launch_check("k_csa_decode_fused");
+}
+
+lcc_status check_csa_attn(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, const int64_t* q_pos0,
+                          const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap, const int32_t* idx,
+                          int k, const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride, int Rcap,
+                          const int64_t* raw_pos0, int W, const lcc_bf16* out) {
   if (!out) return fail(LCC_ERR_ARG, "%s: null out", name);
   const float* dummy = reinterpret_cast<const float*>(out);
   lcc_status st = check_attn_common(name, q, B, Tq, H, D, Kc, Vc, kv_rstride, Ncap, dummy, dummy);
@@ -1197,6 +1234,13 @@ lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int T
   if (!idx || !q_pos0 || !raw_pos0) return fail(LCC_ERR_ARG, "%s: null idx / q_pos0 / raw_pos0", name);
   if (k < 1 || k > 4096) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..4096)", name, k);
   if (W < 1 || W > 4096) return fail(LCC_ERR_SHAPE, "%s: W=%d (supported: 1..4096)", name, W);
+  return LCC_OK;
+}
+
+AttnArgs csa_attn_args(const lcc_bf16* q, int B, int Tq, int H, float scale, const int64_t* q_pos0,
+                       const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride, int Ncap, const int32_t* idx, int k,
+                       const lcc_bf16* Kr, const lcc_bf16* Vr, int64_t r_rstride, int Rcap, const int64_t* raw_pos0,
+                       int W) {
   AttnArgs a{};
   a.q = reinterpret_cast<const bf16*>(q);
   a.B = B; a.Tq = Tq; a.H = H;
@@ -1208,6 +1252,21 @@ lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int T
   a.K2 = reinterpret_cast<const bf16*>(Kr); a.V2 = reinterpret_cast<const bf16*>(Vr);
   a.kv2_bs = static_cast<int64_t>(Rcap) * r_rstride; a.kv2_rs = r_rstride; a.Ncap2 = Rcap;
   a.raw_pos0 = raw_pos0; a.W = W;
+  return a;
+}
+
+lcc_status csa_layer_attn_impl(const char* name, const lcc_bf16* q, int B, int Tq, int H, int D, float scale,
+                               const int64_t* q_pos0, const lcc_bf16* Kc, const lcc_bf16* Vc, int64_t kv_rstride,
+                               int Ncap, const int32_t* idx, int k, const lcc_bf16* Kr, const lcc_bf16* Vr,
+                               int64_t r_rstride, int Rcap, const int64_t* raw_pos0, int W, lcc_bf16* out,
+                               float* lse_out, void* workspace, size_t workspace_bytes, void* stream, bool pdl) {
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: negative size", name);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  lcc_status st = check_csa_attn(name, q, B, Tq, H, D, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k, Kr, Vr, r_rstride,
+                                 Rcap, raw_pos0, W, out);
+  if (st != LCC_OK) return st;
+  const AttnArgs a = csa_attn_args(q, B, Tq, H, scale, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k, Kr, Vr, r_rstride,
+                                   Rcap, raw_pos0, W);
   if (use_gather_tc(B, Tq, H, D, scale, Ncap, Rcap)) {
     AttnGatherArgs g{};
     g.B = B; g.Tq = Tq; g.H = H; g.scale_log2 = a.scale_log2; g.q_pos0 = q_pos0;
@@ -1257,6 +1316,44 @@ lcc_status lcc_csa_layer(const lcc_bf16* q, const lcc_bf16* qI, const float* w, 
   if (!workspace || workspace_bytes < need)
     return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, need);
   const size_t ws_index = round_up(index_ws(B, Tq, Ncap, k).total, 256);
+  if (use_csa_fused(fmt, B, Tq, H, D, HI, scale, Ncap, k, Rcap, W)) {
+    // indexer scores, then one cluster per query selects and attends
+    lcc_status st = check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, idx);
+    if (st != LCC_OK) return st;
+    if (!aligned16(workspace)) return fail(LCC_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
+    if ((st = check_csa_attn(name, q, B, Tq, H, D, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k, Kr, Vr, r_rstride, Rcap,
+                             raw_pos0, W, out)) != LCC_OK)
+      return st;
+    const IndexWs ws = index_ws_rows(static_cast<int64_t>(B) * Tq, Ncap);
+    char* base = static_cast<char*>(workspace);
+    float* scores = reinterpret_cast<float*>(base);
+    uint32_t* gmax = reinterpret_cast<uint32_t*>(base + ws.scores);
+    int* counters = reinterpret_cast<int*>(base + ws.scores + ws.gmax);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    IndexArgs ia{reinterpret_cast<const bf16*>(qI), w, B, Tq, q_pos0, kI, kI_scale, n_valid, Ncap, m, 0, Tq,
+                 scores, gmax, gmax_stride(Ncap), counters};
+    if ((st = launch_scores(ia, HI, DI, fmt, s)) != LCC_OK) return st;
+    TopkThrArgs ta{};
+    ta.scores = scores;
+    ta.gmax = gmax;
+    ta.gs = 32;  // the tensor-core indexers write one maximum per 32 entries
+    ta.g_stride = gmax_stride(Ncap);
+    ta.Ncap = Ncap;
+    ta.q_pos0 = q_pos0;
+    ta.n_valid = n_valid;
+    ta.m = m;
+    ta.Tq = Tq;
+    ta.q0 = 0;
+    ta.nq = Tq;
+    ta.k = k;
+    ta.out_i = idx;
+    ta.out_s = nullptr;
+    AttnArgs a = csa_attn_args(q, B, Tq, H, scale, q_pos0, Kc, Vc, kv_rstride, Ncap, idx, k, Kr, Vr, r_rstride, Rcap,
+                               raw_pos0, W);
+    a.out_bf16 = reinterpret_cast<bf16*>(out);
+    a.lse = lse_out;
+    return launch_csa_fused(a, ta, H / 16, s);
+  }
   lcc_status st = lcc_lightning_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx,
                                            nullptr, workspace, ws_index, stream);
   if (st != LCC_OK) return st;

@@ -225,15 +225,27 @@ struct TopkClSmem {
   static constexpr size_t total = g + MAXG * 4;
 };
 
-// MAXG: most super-groups (2k); the host routes rows to this kernel only when
-// 2k <= MAXG, k * (entries per group) <= CAP and the row fits 8*NT*PER entries.
-template <int NT, int PER, int CAP, int MAXG>
-__global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
+// Where a row's result goes: entry e (and, when wanted, its score) at place p.
+struct TopkOut {
+  int32_t* oi;
+  float* os;
+  __device__ __forceinline__ void put(int p, int e) const { oi[p] = e; }
+  __device__ __forceinline__ bool scores() const { return os != nullptr; }
+  __device__ __forceinline__ void put_score(int p, float v) const { os[p] = v; }
+};
+
+// The top-k of one row by the CTAs of a thread-block cluster (every CTA calls
+// this with the same row, after the scores and group maxima are visible).
+// CTA 0 writes the result through `out`; every CTA returns after the same
+// number of cluster barriers.  MAXG: most super-groups (2k); callers route
+// rows here only when 2k <= MAXG, k * (entries per group) <= CAP and the row
+// fits (CTAs of the cluster) * NT * PER entries.
+template <int NT, int PER, int CAP, int MAXG, class Out>
+__device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* smem, int row, const Out out) {
   using L = TopkClSmem<NT, PER, CAP, MAXG>;
   constexpr int SEG = NT * PER;
   static_assert(PER % 4 == 0, "4-wide loads");
   static_assert(NT <= 256 && (NT & (NT - 1)) == 0, "the sorts exchange through s_hist, one word per thread");
-  extern __shared__ __align__(128) uint8_t smem[];
   uint32_t* s_ck = reinterpret_cast<uint32_t*>(smem + L::ck);
   int32_t* s_ci = reinterpret_cast<int32_t*>(smem + L::ci);
   uint32_t* s_ok = reinterpret_cast<uint32_t*>(smem + L::ok);
@@ -253,25 +265,20 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
     s_bc[3] = 0u;
   }
   clu::arrive();  // every CTA of the cluster has started before any remote access (wait below)
-  const int row = static_cast<int>(blockIdx.x / CL);
   const int b = row / a.nq, i = a.q0 + row % a.nq;
   const int k = a.k;
   const float* srow = a.scores + static_cast<int64_t>(row) * a.Ncap;
   const int64_t qpos = __ldg(a.q_pos0 + b) + i;
   const int nval = __ldg(a.n_valid + b);
   const int vis = visible_entries(qpos, a.m, nval, a.Ncap);
-  int32_t* oi = a.out_i + (static_cast<int64_t>(b) * a.Tq + i) * k;
-  float* os = a.out_s ? a.out_s + (static_cast<int64_t>(b) * a.Tq + i) * k : nullptr;
-  pdl_trigger();
-  pdl_wait();  // scores and group maxima come from the indexer kernel
 
   if (vis <= k) {  // every visible entry is selected
+    clu::wait();  // every CTA has started: `out` may write into their shared memory
     if (rk == 0)
       for (int p = tid; p < k; p += NT) {
-        oi[p] = p < vis ? p : -1;
-        if (os) os[p] = p < vis ? __ldcg(srow + p) : -INFINITY;
+        out.put(p, p < vis ? p : -1);
+        if (out.scores()) out.put_score(p, p < vis ? __ldcg(srow + p) : -INFINITY);
       }
-    clu::wait();
     return;
   }
 
@@ -399,8 +406,8 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
       const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
       out_pos += sel_tot;
       if (sel && p < k) {
-        oi[p] = s_oi[c];
-        if (os) os[p] = key_to_f32(key);
+        out.put(p, s_oi[c]);
+        if (out.scores()) out.put_score(p, key_to_f32(key));
       }
     }
     return;
@@ -430,10 +437,22 @@ __global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
     const int p = out_pos + block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
     out_pos += sel_tot;
     if (sel && p < k) {
-      oi[p] = e;
-      if (os) os[p] = key_to_f32(key);
+      out.put(p, e);
+      if (out.scores()) out.put_score(p, key_to_f32(key));
     }
   }
+}
+
+// One thread-block cluster per row; the rows of the call are blockIdx.x / (cluster size).
+template <int NT, int PER, int CAP, int MAXG>
+__global__ void __launch_bounds__(NT) k_topk_cluster(TopkThrArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int row = static_cast<int>(blockIdx.x / clu::size());
+  const int b = row / a.nq, i = a.q0 + row % a.nq;
+  const int64_t o = (static_cast<int64_t>(b) * a.Tq + i) * a.k;
+  pdl_trigger();
+  pdl_wait();  // scores and group maxima come from the indexer kernel
+  topk_cluster_row<NT, PER, CAP, MAXG>(a, smem, row, TopkOut{a.out_i + o, a.out_s ? a.out_s + o : nullptr});
 }
 
 }  // namespace lcc

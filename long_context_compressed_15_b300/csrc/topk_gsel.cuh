@@ -17,7 +17,7 @@
 //      sort of the group maxima when there are at most NT groups, else of
 //      NT partition maxima (thread t: groups t, t+NT, ...);
 //   2. the groups whose maximum reaches theta are listed in index order
-//      (one block scan);
+//      (warp ballots and one scan over the warps' counts);
 //   3. only their scores are read, each thread PER consecutive entries of a
 //      group (a warp reads whole 128-byte rows), and the scores >= theta are
 //      compacted in index order straight from registers (typically little
@@ -104,29 +104,50 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
       theta = block_kth_hist<NT>(s_g, G, k, s_hist, s_bc);
     }
   }
-  // 2. groups whose maximum reaches theta, in index order
+  // 2. groups whose maximum reaches theta, in index order: each warp takes
+  // 512 consecutive groups of a chunk (ballots over 32 at a time), one scan
+  // over the warps' counts places the warps' lists
   int ng = 0;
   {
-    constexpr int PERG = 4;  // consecutive groups per thread per pass
-    for (int g0 = 0; g0 < G; g0 += NT * PERG) {
-      const int gb = g0 + tid * PERG;
-      int f = 0;
+    constexpr int NWARP = NT / 32, GPW = 512;
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int g0 = 0; g0 < G; g0 += NWARP * GPW) {
+      const int gw = g0 + warp * GPW;
+      int cnt = 0;
+#pragma unroll 4
+      for (int u = 0; u < GPW / 32; ++u) {
+        const int g = gw + u * 32 + lane;
+        cnt += __popc(__ballot_sync(0xffffffffu, g < G && s_g[g] >= theta));
+      }
+      if (lane == 0) s_warp[warp] = cnt;
+      __syncthreads();
+      int base = ng, tot = 0;
 #pragma unroll
-      for (int u = 0; u < PERG; ++u) f += (gb + u < G && s_g[gb + u] >= theta) ? 1 : 0;
-      int tot;
-      int p = ng + block_scan_excl<NT>(f, s_warp, &tot);
-#pragma unroll
-      for (int u = 0; u < PERG; ++u)
-        if (gb + u < G && s_g[gb + u] >= theta) s_gl[p++] = gb + u;
+      for (int w = 0; w < NWARP; ++w) {
+        const int c = s_warp[w];
+        base += w < warp ? c : 0;
+        tot += c;
+      }
+      if (cnt > 0) {
+#pragma unroll 4
+        for (int u = 0; u < GPW / 32; ++u) {
+          const int g = gw + u * 32 + lane;
+          const bool f = g < G && s_g[g] >= theta;
+          const unsigned bal = __ballot_sync(0xffffffffu, f);
+          if (f) s_gl[base + __popc(bal & ((1u << lane) - 1u))] = g;
+          base += __popc(bal);
+        }
+      }
       ng += tot;
+      __syncthreads();  // s_warp is reused
     }
   }
   __syncthreads();
   // 3. the listed groups' scores, NT*PER entries per pass: each thread takes
-  // PER consecutive entries of one group (two 16-byte loads), so a warp reads
+  // PER consecutive entries of one group (four 16-byte loads), so a warp reads
   // whole 128-byte rows; the scores >= theta are compacted in index order
   // (one block scan per pass)
-  constexpr int PER = 8;
+  constexpr int PER = 16;
   const int C = ng * 32;
   const bool vec = (a.Ncap & 3) == 0 && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0;
   int M = 0;
@@ -136,10 +157,11 @@ __global__ void __launch_bounds__(NT) k_topk_gsel(TopkThrArgs a) {
       const int e = c < C ? s_gl[c >> 5] * 32 + (c & 31) : vis;
       uint32_t kv[PER];
       if (vec && e + PER <= vis) {
-        const float4 x0 = __ldcg(reinterpret_cast<const float4*>(srow + e));
-        const float4 x1 = __ldcg(reinterpret_cast<const float4*>(srow + e + 4));
-        kv[0] = f32_to_key(x0.x); kv[1] = f32_to_key(x0.y); kv[2] = f32_to_key(x0.z); kv[3] = f32_to_key(x0.w);
-        kv[4] = f32_to_key(x1.x); kv[5] = f32_to_key(x1.y); kv[6] = f32_to_key(x1.z); kv[7] = f32_to_key(x1.w);
+#pragma unroll
+        for (int u = 0; u < PER; u += 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(srow + e + u));
+          kv[u] = f32_to_key(x.x); kv[u + 1] = f32_to_key(x.y); kv[u + 2] = f32_to_key(x.z); kv[u + 3] = f32_to_key(x.w);
+        }
       } else {
 #pragma unroll
         for (int u = 0; u < PER; ++u) kv[u] = e + u < vis ? f32_to_key(__ldcg(srow + e + u)) : 0u;

@@ -21,6 +21,9 @@ capture (``ncu --set full``) of one launch finishes in seconds:
                          (4 x 262160 entries, NVFP4 keys): scores only
     csa-decode-topk      the CSA decode batch's indexer + top-k (32 x 16384
                          entries, top-128)
+    csa-decode-layer     the CSA decode batch through the layer call:
+                         indexer, then top-k + attention in one cluster per
+                         query
 """
 from __future__ import annotations
 
@@ -37,6 +40,7 @@ if ROOT not in sys.path:
 import datagen  # noqa: E402
 from datagen.workloads import CsaDecode, CsaPrefill, HcaPrefill, PairDecode, T_KI, T_QI, T_W  # noqa: E402
 
+from long_context_compressed_15_b300.layers import CsaLayerPlan  # noqa: E402
 from long_context_compressed_15_b300 import (csa_layer_attn, hca_layer_attn, lightning_index_scores,  # noqa: E402
                                              lightning_index_topk, load)
 
@@ -104,9 +108,18 @@ def csa_decode_topk(dev, nq):
     return lambda: lightning_index_topk(s["qI"], s["w"], pos, s["kI"], c.N, 4, c.k, idx=idx)
 
 
+def csa_decode_layer(dev, nq):
+    c = CsaDecode()
+    s = c.make(dev)
+    plan = CsaLayerPlan(c.B, 1, c.H, c.D, c.N, c.k, c.W, device=dev)
+    return lambda: plan(s["q"], s["qI"], s["w"], c.q_pos, s["kI"], c.N, s["Kc"], s["Vc"], s["Kr"], s["Vr"],
+                        c.raw_pos0)
+
+
 CASES = {"index-topk-prefill": index_topk_prefill, "hca-prefill-attn": hca_prefill_attn,
          "csa-decode-index": csa_decode_index, "csa-prefill-attn": csa_prefill_attn,
-         "pair-decode-index": pair_decode_index, "csa-decode-topk": csa_decode_topk}
+         "pair-decode-index": pair_decode_index, "csa-decode-topk": csa_decode_topk,
+         "csa-decode-layer": csa_decode_layer}
 
 
 def main(argv=None):

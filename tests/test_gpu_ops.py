@@ -747,3 +747,68 @@ def test_bounded_wait_runs_out_and_context_survives():
     assert torch.equal(again, ref)
     sc = oracle.index_scores(runs.f64(host(qI[0, 0])), host(w[0, 0]).astype(np.float64), runs.f64(host(kI[0])))
     np.testing.assert_allclose(again[0, 0].cpu().numpy(), sc, rtol=1e-4, atol=1e-4)
+
+
+# ---------------------------------------------------------------------------
+# CSA layer, decode-shaped: top-k and attention in one cluster per query
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("H,B,Tq,Ncap,k,nval,nvfp4", [
+    (64, 3, 2, 16384, 128, [16384, 300, 50], False),   # 4 CTAs per query; rows above, near and below k
+    (16, 2, 1, 4000, 64, [4000, 1000], False),         # one CTA per query
+    (128, 2, 1, 10000, 128, [10000, 129], True),       # 8 CTAs per query, NVFP4 indexer keys
+])
+def test_csa_layer_decode_one_cluster_per_query(H, B, Tq, Ncap, k, nval, nvfp4):
+    # the whole layer call against the two-call composition (index + top-k, then the layer
+    # attention over that list): the same index lists and bit-identical outputs; and both
+    # against the oracle on every row
+    D, W, HI, DI, m = 128, 128, 8, 64, 4
+    seed = 40 + H
+    q = datagen.normal_bf16(seed, 1, (B, Tq, H, D), 1.0 / np.sqrt(D))
+    qI = datagen.normal_bf16(seed, 2, (B, Tq, HI, DI))
+    w = datagen.uniform_f32(seed, 3, (B, Tq, HI))
+    Kc = datagen.normal_bf16(seed, 4, (B, Ncap, D))
+    Vc = datagen.normal_bf16(seed, 5, (B, Ncap, D))
+    Rcap = W + Tq
+    Kr = datagen.normal_bf16(seed, 6, (B, Rcap, D))
+    Vr = datagen.normal_bf16(seed, 7, (B, Rcap, D))
+    if nvfp4:
+        kp, ks = datagen.nvfp4_normal(seed, 8, B * Ncap, DI)
+        kI, kIs = kp.reshape(B, Ncap, DI // 2), ks.reshape(B, Ncap, DI // 16)
+        kI_host = oracle.nvfp4_decode(kI.numpy(), kIs.numpy())
+        kIs_d = kIs.to(DEV)
+    else:
+        kI = datagen.normal_bf16(seed, 8, (B, Ncap, DI))
+        kI_host, kIs_d = f64(kI), None
+    pos = [4 * n + 3 - Tq + 1 for n in nval]        # the last query sees every valid entry
+    raw0 = [p - W + 1 for p in pos]                 # window rows of the first query present
+    dv = {n: t.to(DEV) for n, t in dict(q=q, qI=qI, w=w, Kc=Kc, Vc=Vc, Kr=Kr, Vr=Vr, kI=kI).items()}
+    pos_d = torch.tensor(pos, device=DEV)
+    raw_d = torch.tensor(raw0, device=DEV)
+    nval_d = torch.tensor(nval, dtype=torch.int32, device=DEV)
+    idx1 = torch.full((B, Tq, k), -7, dtype=torch.int32, device=DEV)
+    out1 = lcc.csa_layer(dv["q"], dv["qI"], dv["w"], pos_d, dv["kI"], nval_d, m, k, dv["Kc"], dv["Vc"], dv["Kr"],
+                         dv["Vr"], raw_d, W, kI_scale=kIs_d, idx=idx1)
+    idx2 = lcc.lightning_index_topk(dv["qI"], dv["w"], pos_d, dv["kI"], nval_d, m, k, kI_scale=kIs_d)
+    out2 = lcc.csa_layer_attn(dv["q"], dv["Kc"], dv["Vc"], idx2, dv["Kr"], dv["Vr"], pos_d, raw_d, W)
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    assert torch.equal(idx1, idx2)
+    assert torch.equal(out1, out2)
+    g, go = idx1.cpu().numpy(), out1.float().cpu().numpy()
+    qh, Kch, Vch, Krh, Vrh = f64(q), f64(Kc), f64(Vc), f64(Kr), f64(Vr)
+    near = 0
+    for b in range(B):
+        for i in range(Tq):
+            t = pos[b] + i
+            nv = oracle.visible_count(t, m, nval[b])
+            sc = oracle.index_scores(f64(qI[b, i]), f64(w[b, i]), kI_host[b, :nv])
+            oi, kth = oracle.topk_select(sc, k)
+            ok, exact = topk_set_ok(g[b, i], oi, sc, kth, k)
+            assert ok, f"batch {b} query {i}: top-k set differs"
+            near += not exact
+            sel = g[b, i][g[b, i] >= 0]
+            cO, cL = oracle.attend(qh[b, i], Kch[b, sel], Vch[b, sel])
+            sw = runs.swa_branch(qh[b, i], t, Krh[b], Vrh[b], raw0[b], W)
+            O, _ = oracle.merge([cO, sw["O"]], [cL, sw["lse"]])
+            assert_close(go[b, i], O, f"batch {b} query {i}")
+    assert near <= 1
