@@ -230,7 +230,7 @@ template <int NW, int KT>
 __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_constant__ CUtensorMap tmK,
                                                              const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   const int hblocks = (a.H + 15) / 16;
   const int qi = blockIdx.x / hblocks, h0 = (blockIdx.x % hblocks) * 16;
   auto wait_lists = []() { pdl_wait(); };  // index lists may come from the previous kernel

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(192, 1)
   using C = AttnTcCfg<D>;
   constexpr float TAU = 8.0f;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars;
   uint64_t* k_full = bars + 1;                  // [STAGES]

@@ -28,6 +28,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The first 1024-byte boundary at or after `raw` (the start of a dynamic
+// shared-memory array).  Offsetting the pointer itself, rather than rounding
+// its integer value, keeps it visibly a shared-memory pointer, so accesses
+// through it compile to shared-memory instructions instead of generic ones.
+__device__ __forceinline__ uint8_t* align_smem_1024(uint8_t* raw) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
 // ---- cp.async (16-byte, zero-fill when src_bytes == 0) ----
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));

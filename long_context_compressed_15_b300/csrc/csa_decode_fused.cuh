@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(NW * 32) k_csa_decode_fused(const __grid_const
                                                               TopkThrArgs t) {
   using S = CsaFusedSmem<NW, KT, PER, CAP, MAXG>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   int* sidx = reinterpret_cast<int*>(smem + S::off_idx);
   const uint32_t rk = clu::rank(), CL = clu::size();
   const int qi = static_cast<int>(blockIdx.x / CL), b = static_cast<int>(blockIdx.y);

@@ -67,7 +67,7 @@ template <int HI, int DI, int NQ, int STAGES>
 __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUtensorMap tmap_k, IndexTcArgs a) {
   using C = IndexTcCfg<HI, DI, NQ, STAGES>;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
   using C = IndexTcCfg<HI, DI, NQ, 1>;
   static_assert(DI == 64, "NVFP4 keys: DI = 64 (one 128-byte swizzle row per converted entry)");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* sA = smem + S::OFF_A;
   uint8_t* sB = smem + S::OFF_B;
   uint8_t* sRaw = smem + S::OFF_RAW;

@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(320, 1) k_index_topk_tc(const __grid_constant_
   constexpr int COLS = QH * HI;          // accumulator columns per half (64)
   static_assert(C::NREAL == C::N && COLS % 32 == 0, "whole 32-column loads");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
   constexpr int CAPB = X::CAPB;
   static_assert(C::NREAL == C::N && COLS % 32 == 0 && NQ % G == 0, "whole 32-column loads");
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = align_smem_1024(smem_raw);
   uint8_t* sA = smem + C::OFF_A;
   uint8_t* sB = smem + C::OFF_B;
   float* sW = reinterpret_cast<float*>(smem + C::OFF_W);
