@@ -93,6 +93,28 @@ __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte_in_low8) {
       : "=r"(out) : "r"(byte_in_low8));
   return out;
 }
+// The four e2m1 pairs of a 32-bit word -> four f16x2 (exact), byte j -> h[j]
+// (low nibble -> low half), without shifting the word.
+__device__ __forceinline__ void e2m1x8_to_f16x2x4(uint32_t word, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n"
+      " mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+      " cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+      " cvt.rn.f16x2.e2m1x2 %3, b3;\n}\n"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3]) : "r"(word));
+}
+// Four e4m3 bytes -> four f16x2, each with both halves equal to one byte's
+// value (exact): two paired conversions, then each half duplicated.
+__device__ __forceinline__ void e4m3x4_to_f16x2_bcast(uint32_t four, uint32_t (&s)[4]) {
+  uint32_t lo, hi;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(lo) : "h"(static_cast<uint16_t>(four & 0xFFFFu)));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(hi) : "h"(static_cast<uint16_t>(four >> 16)));
+  s[0] = __byte_perm(lo, 0u, 0x1010);
+  s[1] = __byte_perm(lo, 0u, 0x3232);
+  s[2] = __byte_perm(hi, 0u, 0x1010);
+  s[3] = __byte_perm(hi, 0u, 0x3232);
+}
 // One e4m3 byte -> f16x2 with both halves equal to its value (exact).
 __device__ __forceinline__ uint32_t e4m3_to_f16x2_bcast(uint32_t byte) {
   uint32_t out;

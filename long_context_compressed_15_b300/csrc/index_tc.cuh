@@ -492,15 +492,18 @@ __global__ void __launch_bounds__(320, 2) k_index_tc_fp4(IndexTcArgs a) {
       tc::mbar_arrive(rempty + s);
       const uint32_t wd[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
       uint8_t* dst = sA + c * F::A_BYTES + (r >> 3) * S::SBO + (r & 7) * F::ROWB;
+      uint32_t sb[4];  // scale of elements 16g .. 16g+15, both halves
+      e4m3x4_to_f16x2_bcast(scales, sb);
 #pragma unroll
       for (int ch = 0; ch < DI / 8; ++ch) {       // one packed word = 8 elements = one 16-byte fp16 chunk
-        const uint32_t s2 = e4m3_to_f16x2_bcast(scales >> (8 * (ch >> 1)));
-        const uint32_t word = wd[ch];
+        uint32_t h[4];
+        e2m1x8_to_f16x2x4(wd[ch], h);
+        const uint32_t s2 = sb[ch >> 1];
         uint4 o;
-        o.x = hmul2_u32(e2m1x2_to_f16x2(word), s2);
-        o.y = hmul2_u32(e2m1x2_to_f16x2(word >> 8), s2);
-        o.z = hmul2_u32(e2m1x2_to_f16x2(word >> 16), s2);
-        o.w = hmul2_u32(e2m1x2_to_f16x2(word >> 24), s2);
+        o.x = hmul2_u32(h[0], s2);
+        o.y = hmul2_u32(h[1], s2);
+        o.z = hmul2_u32(h[2], s2);
+        o.w = hmul2_u32(h[3], s2);
         *reinterpret_cast<uint4*>(dst + ((ch ^ (r & 7)) * 16)) = o;
       }
       tc::fence_proxy_async_smem();   // generic writes -> visible to the tensor core
