@@ -64,7 +64,7 @@ struct IndexTcCfg {
 };
 
 template <int HI, int DI, int NQ, int STAGES>
-__global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUtensorMap tmap_k, IndexTcArgs a) {
+__global__ void __maxnreg__(48) k_index_tc(const __grid_constant__ CUtensorMap tmap_k, IndexTcArgs a) {
   using C = IndexTcCfg<HI, DI, NQ, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_smem_1024(smem_raw);
@@ -85,10 +85,21 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(tempty + NACC);
   volatile int* s_abort = reinterpret_cast<volatile int*>(s_tmem + 1);
 
-  // launched as a programmatic dependent of whatever ran before on the
-  // stream: nothing is read before that grid has completed
-  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // set-up that reads nothing a previous kernel may write (barriers, TMEM
+  // columns, the tensor map's descriptor) runs before the launch wait, so it
+  // overlaps the previous kernel when this CTA is launched early
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) { tc::mbar_init(full + i, 1); tc::mbar_init(empty + i, 1); }
+    for (int i = 0; i < NACC; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
+    *s_abort = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) tc::tma_prefetch_desc(&tmap_k);
+  if (warp == 1) tc::tmem_alloc(s_tmem, TMEM_COLS);
+  // launched as a programmatic dependent of whatever ran before on the
+  // stream: nothing else is read before that grid has completed
+  pdl_wait();
   const int b = blockIdx.z;
   const int qg0 = a.q0 + blockIdx.y * NQ;                   // first query of this CTA
   const int qend = min(qg0 + NQ, a.q0 + a.nq);              // one past the last
@@ -98,28 +109,28 @@ __global__ void __launch_bounds__(192, 1) k_index_tc(const __grid_constant__ CUt
   const int ntiles_vis = (vis_max + C::TILE - 1) / C::TILE;
   const int t_lo = blockIdx.x * a.tiles_per_split;
   const int t_hi = min(t_lo + a.tiles_per_split, ntiles_vis);
-  if (t_lo >= t_hi) return;  // uniform across the CTA
+  if (t_lo >= t_hi) {  // uniform across the CTA: give the TMEM columns back
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+      tc::tc_fence_after();
+      tc::tmem_dealloc(*s_tmem, TMEM_COLS);
+    }
+    return;
+  }
   const int ntiles = t_hi - t_lo;
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i) { tc::mbar_init(full + i, 1); tc::mbar_init(empty + i, 1); }
-    for (int i = 0; i < NACC; ++i) { tc::mbar_init(tfull + i, 1); tc::mbar_init(tempty + i, 128); }
-    *s_abort = 0;
-    tc::fence_barrier_init();
-  }
-  __syncthreads();
+  __syncthreads();  // barriers initialised
   const int row0 = b * a.Ncap + t_lo * C::TILE;
   const int drop = warp == 0 && lane == 0 ? *static_cast<volatile int*>(&tc::g_test_drop_tile) : -1;
   if (warp == 0 && lane == 0) {
     // start streaming keys before the rest of the set-up
-    tc::tma_prefetch_desc(&tmap_k);
     for (int t = 0; t < min(STAGES, ntiles); ++t) {
       if (t == drop) continue;  // test hook: this tile's barrier never completes
       tc::mbar_arrive_expect_tx(full + t, C::A_BYTES);
       tc::tma_load_2d(sA + t * C::A_BYTES, &tmap_k, full + t, 0, row0 + t * C::TILE);
     }
   }
-  if (warp == 1) tc::tmem_alloc(s_tmem, TMEM_COLS);
   if (warp >= 2) {
     // B operand: row n = (query n / HI, head n % HI), K-major, swizzled like the TMA tiles
     const int t = threadIdx.x - 64;
