@@ -12,18 +12,17 @@
 //   1. every CTA loads its SEG = NT*PER scores, builds all super-group
 //      maxima from the group maxima and finds theta itself (the same
 //      deterministic selection in every CTA: no exchange);
-//   2. every CTA compacts its entries >= theta (a run in index order),
-//      reserves room for the run in CTA 0 with one atomic on CTA 0's shared
-//      counter and stores it there through distributed shared memory, with
-//      the run's place and length; one cluster barrier;
-//   3. CTA 0 lays the runs out in CTA (= index) order, selects the exact
-//      k-th largest key T and writes every candidate above T and the
-//      lowest-index candidates equal to T.
+//   2. every CTA compacts its entries >= theta (a run in index order) and
+//      stores it, with its length, into its own CAP/CL-slot region of CTA 0
+//      through distributed shared memory; one cluster barrier;
+//   3. CTA 0 takes the runs in CTA (= index) order, one candidate per
+//      thread, selects the exact k-th largest key T and writes every
+//      candidate above T and the lowest-index candidates equal to T.
 // Both selections (theta among the super-group maxima, T among the
 // candidates) sort up to NT values, one per thread, with a bitonic network
 // and take the k-th; larger sets take 256-bin histogram rounds, each
 // narrowing the key interval to the bin that holds the k-th value (at most
-// four rounds for 32-bit keys).  Candidates that do not fit CAP (massive exact ties) fall back
+// four rounds for 32-bit keys).  A run that does not fit its region (massive exact ties) falls back
 // to a bisection over the row's scores in CTA 0.  Control flow through the
 // cluster barriers depends only on per-row values, so every CTA of the
 // cluster meets each barrier.
@@ -254,13 +253,11 @@ __device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* s
   __shared__ int s_warp[NT / 32];
   __shared__ uint32_t s_hist[256];
   __shared__ uint32_t s_bc[4];
-  __shared__ uint32_t s_cnt, s_base;
-  __shared__ uint32_t s_rb[8], s_rc[8];  // CTA 0: place and length of each CTA's run
+  __shared__ uint32_t s_rc[8];  // CTA 0: length of each CTA's run
 
   const int tid = threadIdx.x;
   const uint32_t rk = clu::rank(), CL = clu::size();
   if (tid == 0) {  // before the arrive, so that no remote access can precede these
-    s_cnt = 0u;
     s_bc[2] = 0xFFFFFFFFu;
     s_bc[3] = 0u;
   }
@@ -320,7 +317,9 @@ __device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* s
     }
   }
 
-  // this CTA's run of candidates, stored into CTA 0
+  // this CTA's run of candidates, stored into its own region of CTA 0 (CAP / CL
+  // slots per CTA: the runs lie in CTA order = index order, with no atomics)
+  const int RUN = CAP / static_cast<int>(CL);
   uint32_t keys[PER];
   int n = 0;
 #pragma unroll
@@ -331,23 +330,16 @@ __device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* s
   int tot;
   int pos = block_scan_excl<NT>(n, s_warp, &tot);
   clu::wait();
-  if (tid == 0) {
-    const uint32_t base = clu::atom_add(clu::map(&s_cnt, 0), static_cast<uint32_t>(tot));
-    s_base = base;
-    clu::st(clu::map(s_rb + rk, 0), base);
-    clu::st(clu::map(s_rc + rk, 0), static_cast<uint32_t>(tot));
-  }
-  __syncthreads();
+  if (tid == 0) clu::st(clu::map(s_rc + rk, 0), static_cast<uint32_t>(tot));
   {
-    const int base = static_cast<int>(s_base);
     const uint32_t rck = clu::map(s_ck, 0), rci = clu::map(s_ci, 0);
+    const int base = static_cast<int>(rk) * RUN;
 #pragma unroll
     for (int u = 0; u < PER; ++u) {
       if (keys[u] >= theta && keys[u] != 0u) {
-        const int slot = base + pos;
-        if (slot < CAP) {
-          clu::st(rck + 4u * slot, keys[u]);
-          clu::st(rci + 4u * slot, static_cast<uint32_t>(e0 + u));
+        if (pos < RUN) {
+          clu::st(rck + 4u * (base + pos), keys[u]);
+          clu::st(rci + 4u * (base + pos), static_cast<uint32_t>(e0 + u));
         }
         ++pos;
       }
@@ -356,25 +348,59 @@ __device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* s
   clu::sync();  // CTA 0 holds every run; no remote access after this point
   if (rk != 0) return;
 
-  const int C = static_cast<int>(s_cnt);
-  if (C >= k && C <= CAP) {
-    // runs in CTA order = index order
-    for (int c = tid; c < C; c += NT) {
-      int off = 0;
-      for (uint32_t r = 0; r < CL; ++r) {
-        const int rb = static_cast<int>(s_rb[r]), rc = static_cast<int>(s_rc[r]);
-        if (c >= rb && c < rb + rc) {
-          s_ok[off + c - rb] = s_ck[c];
-          s_oi[off + c - rb] = s_ci[c];
-        }
-        off += rc;
+  int C = 0;
+  bool fits = true;
+  for (uint32_t r = 0; r < CL; ++r) {
+    const int rc = static_cast<int>(s_rc[r]);
+    C += rc;
+    fits = fits && rc <= RUN;
+  }
+  if (fits && C >= k && C <= NT) {
+    // the usual case (a few hundred candidates): candidate t of the concatenated
+    // runs in thread t, the exact k-th key T by a bitonic sort, then every key
+    // above T and the lowest-index keys equal to T, in index order
+    uint32_t v = 0u;
+    int ent = -1;
+    if (tid < C) {
+      int r = 0, pre = 0;
+      while (tid >= pre + static_cast<int>(s_rc[r])) pre += static_cast<int>(s_rc[r++]);
+      v = s_ck[r * RUN + tid - pre];
+      ent = s_ci[r * RUN + tid - pre];
+    }
+    const uint32_t T = block_kth_bitonic<NT>(v, k, s_hist, s_bc);
+    const int pk = block_sum<NT>((v > T ? 1 : 0) + (v == T ? 0x10000 : 0), s_warp);
+    const int need_eq = k - (pk & 0xFFFF), n_eq = pk >> 16;
+    bool sel;
+    if (n_eq == need_eq) {
+      sel = tid < C && v >= T;
+    } else {
+      const bool eq = tid < C && v == T;
+      int eq_tot;
+      const int eq_rank = block_scan_excl<NT>(eq ? 1 : 0, s_warp, &eq_tot);
+      sel = tid < C && (v > T || (eq && eq_rank < need_eq));
+    }
+    int sel_tot;
+    const int p = block_scan_excl<NT>(sel ? 1 : 0, s_warp, &sel_tot);
+    if (sel && p < k) {
+      out.put(p, ent);
+      if (out.scores()) out.put_score(p, key_to_f32(v));
+    }
+    return;
+  }
+  if (fits && C >= k) {
+    // more candidates than threads: lay the runs out contiguously first
+    int off = 0;
+    for (uint32_t r = 0; r < CL; ++r) {
+      const int rc = static_cast<int>(s_rc[r]);
+      for (int c = tid; c < rc; c += NT) {
+        s_ok[off + c] = s_ck[r * RUN + c];
+        s_oi[off + c] = s_ci[r * RUN + c];
       }
+      off += rc;
     }
     __syncthreads();
     uint32_t T;
-    if (C <= NT) {  // the usual case (a few hundred candidates)
-      T = block_kth_bitonic<NT>(tid < C ? s_ok[tid] : 0u, k, s_hist, s_bc);
-    } else if (C <= 512) {  // one warp, no block barriers
+    if (C <= 512) {  // one warp, no block barriers
       if (tid < 32) {
         const uint32_t t = warp_kth_bits<16>(s_ok, C, k);
         if (tid == 0) s_bc[0] = t;
