@@ -303,11 +303,19 @@ __device__ __forceinline__ void topk_cluster_row(const TopkThrArgs a, uint8_t* s
   uint32_t theta = 0u;  // fewer than k super-groups: every visible entry is a candidate
   if (Gs >= k) {
     const uint32_t* gm = a.gmax + static_cast<int64_t>(row) * a.g_stride;
-    for (int s = tid; s < Gs; s += NT) {
-      uint32_t mx = 0u;
-      const int g1 = min(G, (s + 1) * f);
-      for (int g = s * f; g < g1; ++g) mx = max(mx, __ldcg(gm + g));
-      s_g[s] = mx;
+    if (f == 2 && (reinterpret_cast<uintptr_t>(gm) & 7) == 0 && 2 * Gs <= a.g_stride) {
+      // the usual pairing: both groups of a super-group in one 8-byte load
+      for (int s = tid; s < Gs; s += NT) {
+        const uint2 pr = __ldcg(reinterpret_cast<const uint2*>(gm) + s);
+        s_g[s] = 2 * s + 1 < G ? max(pr.x, pr.y) : pr.x;
+      }
+    } else {
+      for (int s = tid; s < Gs; s += NT) {
+        uint32_t mx = 0u;
+        const int g1 = min(G, (s + 1) * f);
+        for (int g = s * f; g < g1; ++g) mx = max(mx, __ldcg(gm + g));
+        s_g[s] = mx;
+      }
     }
     __syncthreads();
     if (Gs <= NT) {
