@@ -97,6 +97,21 @@ lcc_status lcc_compress(int m, const lcc_bf16* K, const lcc_bf16* V, const float
                         int64_t kv_bstride, int64_t gate_bstride,
                         lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
                         void* stream);
+/* Pooling at positions held on the device, for graph-captured prefill
+ * chunks.  Rows 0 .. n_tokens-1 of sequence b's K/V/gate buffers are the
+ * tokens at positions tok0[b] .. tok0[b]+n_tokens-1; tok0 (device, [B]) must
+ * be a non-negative multiple of m.  The n_tokens/m complete blocks are pooled
+ * as in lcc_compress into entries tok0[b]/m, tok0[b]/m + 1, ... of Kc/Vc
+ * (those at or beyond Ncap are dropped), and n_valid[b] (device, [B]; may be
+ * NULL) is raised to min(Ncap, tok0[b]/m + n_tokens/m) if it was below.  A
+ * sequence whose tok0 is negative or not a multiple of m is skipped and
+ * reported as LCC_ERR_DEVICE by the next lcc_sync_status.  c_bstride must
+ * cover Ncap entries when B > 1. */
+lcc_status lcc_compress_at(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate,
+                           int B, int n_tokens, int D,
+                           int64_t kv_bstride, int64_t gate_bstride, const int64_t* tok0,
+                           lcc_bf16* Kc, lcc_bf16* Vc, int Ncap, int64_t c_bstride,
+                           int32_t* n_valid, void* stream);
 
 /* ---------------------------------------------------------------------- *
  * Query / KV prologue ([HYBRID]: both mechanisms use MQA with shared KV

@@ -38,6 +38,7 @@ _SIGS = {
     "lcc_csa_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
     "lcc_hca_compress": [_P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
     "lcc_compress": [_I, _P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _L, _P],
+    "lcc_compress_at": [_I, _P, _P, _P, _I, _I, _I, _L, _L, _P, _P, _P, _I, _L, _P, _P],
     "lcc_decode_append": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _L, _L, _I, _P, _P, _P, _L, _I, _P, _I, _I,
                           _P, _P, _P, _P, _P],
     "lcc_qkv_prologue": [_P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _F, _I, _F, _P, _P, _P, _P, _P],
@@ -212,6 +213,30 @@ def hca_compress(K, V, gate, Kc, Vc, n_blocks=None, stream=None):
 def compress(m, K, V, gate, Kc, Vc, n_blocks=None, stream=None):
     """Pool every m in {1, 4, 128} tokens of K/V [B, R, D] into Kc/Vc [B, N, D] (m = 1: a copy)."""
     return _compress("lcc_compress", m, K, V, gate, Kc, Vc, n_blocks, stream, pass_m=True)
+
+
+def compress_at(m, K, V, gate, tok0, Kc, Vc, n_valid=None, n_tokens=None, stream=None):
+    """Pool the complete blocks of K/V [B, R, D] (rows = tokens tok0[b] ..) into entries tok0[b]/m .. of
+    Kc/Vc [B, Ncap, D], raising n_valid [B] (int32, optional) on the device (lcc_compress_at)."""
+    for t, n in ((K, "K"), (V, "V"), (Kc, "Kc"), (Vc, "Vc")):
+        _need(t, torch.bfloat16, n, 3)
+    _need(gate, torch.float32, "gate", 2)
+    B, R, D = K.shape
+    kv_bs, kv_rs = _rows(K, "K")
+    if kv_rs != D or V.stride() != K.stride() or gate.stride(1) != 1:
+        raise ValueError("K/V rows must be contiguous with identical strides; gate contiguous per batch")
+    c_bs, c_rs = _rows(Kc, "Kc")
+    if c_rs != D or Vc.stride() != Kc.stride():
+        raise ValueError("Kc/Vc rows must be contiguous with identical strides")
+    n_tokens = R if n_tokens is None else int(n_tokens)
+    if n_tokens > R:
+        raise ValueError("n_tokens exceeds the input rows")
+    tok0 = _positions(tok0, B, K.device)
+    if n_valid is not None:
+        _need(n_valid, torch.int32, "n_valid", 1)
+    _call("lcc_compress_at", int(m), _ptr(K), _ptr(V), _ptr(gate), B, n_tokens, D, kv_bs, gate.stride(0),
+          _ptr(tok0), _ptr(Kc), _ptr(Vc), Kc.shape[1], c_bs, _ptr(n_valid), _stream(stream))
+    return Kc, Vc
 
 
 def decode_append(m, k_new, v_new, g_new, pos, Kr, Vr, gate_r, raw_pos0, Kc, Vc, n_valid,

@@ -18,6 +18,7 @@ enum DevErr : unsigned int {
   DEV_ERR_INDEX = 1,    // an index list entry was outside [-1, Ncap)
   DEV_ERR_TIMEOUT = 2,  // a bounded wait gave up
   DEV_ERR_RANGE = 3,    // a decode append fell outside its raw buffer or caches (detail: sequence)
+  DEV_ERR_POS = 4,      // a pooling position was negative or not a multiple of m (detail: sequence)
 };
 
 __device__ __forceinline__ void record_error(unsigned int code, unsigned int detail) {

@@ -119,8 +119,10 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // ------------------------------------------------------------------ compress
 lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int nblk, int D,
-                         int64_t kv_bs, int64_t g_bs, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bs, void* stream) {
-  const char* name = m == 4 ? "lcc_csa_compress" : m == 128 ? "lcc_hca_compress" : "lcc_compress";
+                         int64_t kv_bs, int64_t g_bs, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bs, void* stream,
+                         const int64_t* tok0 = nullptr, int32_t* n_valid = nullptr, int Ncap = 0,
+                         const char* name = nullptr) {
+  if (!name) name = m == 4 ? "lcc_csa_compress" : m == 128 ? "lcc_hca_compress" : "lcc_compress";
   if (m != 1 && m != 4 && m != 128) return fail(LCC_ERR_SHAPE, "%s: m=%d (supported: 1, 4, 128)", name, m);
   if (B < 0 || nblk < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d n_blocks=%d must be >= 0", name, B, nblk);
   if (B == 0 || nblk == 0) return LCC_OK;
@@ -132,8 +134,11 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
                 g_bs < static_cast<int64_t>(nblk) * m))
     return fail(LCC_ERR_SHAPE, "%s: batch strides smaller than one batch's rows", name);
   if (B > 65535) return fail(LCC_ERR_SHAPE, "%s: B=%d too large", name, B);
+  if (tok0 && Ncap < 1) return fail(LCC_ERR_SHAPE, "%s: Ncap=%d must be >= 1", name, Ncap);
+  if (tok0 && B > 1 && c_bs < static_cast<int64_t>(Ncap) * D)
+    return fail(LCC_ERR_SHAPE, "%s: entry batch stride smaller than Ncap entries", name);
   PoolArgs a{reinterpret_cast<const bf16*>(K), reinterpret_cast<const bf16*>(V), gate, B, nblk, kv_bs, g_bs,
-             reinterpret_cast<bf16*>(Kc), reinterpret_cast<bf16*>(Vc), c_bs};
+             reinterpret_cast<bf16*>(Kc), reinterpret_cast<bf16*>(Vc), c_bs, tok0, n_valid, Ncap};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (m <= 4) {
     constexpr int NB = 4;  // blocks per (half-)warp
@@ -413,6 +418,9 @@ lcc_status lcc_sync_status(void* stream) {
   if (code == DEV_ERR_RANGE)
     return fail(LCC_ERR_DEVICE, "decode append: the new token of sequence %u falls outside its raw buffer, or the "
                 "block it completes outside the raw buffer or the caches", detail);
+  if (code == DEV_ERR_POS)
+    return fail(LCC_ERR_DEVICE, "compress_at: the first token of sequence %u is negative or not a multiple of m "
+                "(the sequence was skipped)", detail);
   return fail(LCC_ERR_DEVICE, "index list entry out of range at list position %u", detail);
 }
 
@@ -438,6 +446,16 @@ lcc_status lcc_compress(int m, const lcc_bf16* K, const lcc_bf16* V, const float
                         int64_t kv_bstride, int64_t gate_bstride, lcc_bf16* Kc, lcc_bf16* Vc, int64_t c_bstride,
                         void* stream) {
   return compress_impl(m, K, V, gate, B, n_blocks, D, kv_bstride, gate_bstride, Kc, Vc, c_bstride, stream);
+}
+
+lcc_status lcc_compress_at(int m, const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int n_tokens,
+                           int D, int64_t kv_bstride, int64_t gate_bstride, const int64_t* tok0, lcc_bf16* Kc,
+                           lcc_bf16* Vc, int Ncap, int64_t c_bstride, int32_t* n_valid, void* stream) {
+  const char* name = "lcc_compress_at";
+  if (!tok0) return fail(LCC_ERR_ARG, "%s: null tok0", name);
+  if (m < 1 || n_tokens < 0) return fail(LCC_ERR_SHAPE, "%s: m=%d n_tokens=%d", name, m, n_tokens);
+  return compress_impl(m, K, V, gate, B, n_tokens / m, D, kv_bstride, gate_bstride, Kc, Vc, c_bstride, stream, tok0,
+                       n_valid, Ncap, name);
 }
 
 lcc_status lcc_hca_compress(const lcc_bf16* K, const lcc_bf16* V, const float* gate, int B, int n_blocks, int D,

@@ -20,7 +20,32 @@ struct PoolArgs {
   bf16* Kc;
   bf16* Vc;
   int64_t c_bs;
+  // device positions (optional): row 0 of sequence b is token tok0[b], a
+  // multiple of m; block j goes to entry tok0[b]/m + j if below Ncap, and
+  // n_valid[b] (optional) is raised to the entries present
+  const int64_t* tok0;
+  int32_t* n_valid;
+  int Ncap;
 };
+
+// Entry of block 0 of sequence b (-1: the sequence is skipped).  With device
+// positions, the first CTA of the sequence also raises n_valid and reports a
+// misaligned position.
+template <int M>
+__device__ __forceinline__ int64_t pool_entry0(const PoolArgs& a, int b, bool first_cta) {
+  if (!a.tok0) return 0;
+  const int64_t t0 = __ldg(a.tok0 + b);
+  if (t0 < 0 || t0 % M != 0) {
+    if (first_cta && threadIdx.x == 0) record_error(DEV_ERR_POS, static_cast<unsigned>(b));
+    return -1;
+  }
+  const int64_t e0 = t0 / M;
+  if (first_cta && threadIdx.x == 0 && a.n_valid) {
+    const int64_t top = e0 + a.nblk < a.Ncap ? e0 + a.nblk : a.Ncap;
+    if (top > 0) atomicMax(a.n_valid + b, static_cast<int>(top));
+  }
+  return e0;
+}
 
 __device__ __forceinline__ void fma8(float (&acc)[8], float a, uint4 v) {
   const __nv_bfloat162* p = reinterpret_cast<const __nv_bfloat162*>(&v);
@@ -93,6 +118,8 @@ __global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
   const int sub = lane / LPB, li = lane % LPB;
   const int isV = li / LPR, col = (li % LPR) * 8;
   const int b = blockIdx.y;
+  const int64_t e0 = pool_entry0<M>(a, b, blockIdx.x == 0);
+  if (e0 < 0) return;
   // the CTA's NB passes cover 8 * BPW * NB consecutive blocks
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * 8 * BPW * NB + warp * BPW + sub;
   uint4 v[NB][M];
@@ -124,7 +151,8 @@ __global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < M; ++i) fma8(acc, gv[n][i] * inv, v[n][i]);
-    *reinterpret_cast<uint4*>((isV ? a.Vc : a.Kc) + b * a.c_bs + blk * D + col) = pack8(acc);
+    if (!a.tok0 || e0 + blk < a.Ncap)
+      *reinterpret_cast<uint4*>((isV ? a.Vc : a.Kc) + b * a.c_bs + (e0 + blk) * D + col) = pack8(acc);
   }
 }
 
@@ -196,9 +224,11 @@ __global__ void __launch_bounds__(256) k_pool_large(PoolArgs a) {
   __shared__ PoolLargeSmem<M, D> sm;
   const int b = blockIdx.y;
   const int64_t blk = blockIdx.x;
+  const int64_t e0 = pool_entry0<M>(a, b, blk == 0);
+  if (e0 < 0 || (a.tok0 && e0 + blk >= a.Ncap)) return;  // uniform across the CTA
   pool_block_large<M, D, true>(a.gate + b * a.g_bs + blk * M, a.K + b * a.kv_bs + blk * M * D,
-                         a.V + b * a.kv_bs + blk * M * D, a.Kc + b * a.c_bs + blk * D, a.Vc + b * a.c_bs + blk * D,
-                         sm);
+                         a.V + b * a.kv_bs + blk * M * D, a.Kc + b * a.c_bs + (e0 + blk) * D,
+                         a.Vc + b * a.c_bs + (e0 + blk) * D, sm);
 }
 
 }  // namespace lcc

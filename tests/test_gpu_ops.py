@@ -52,6 +52,44 @@ def test_compress_parity(m, D, R):
         assert torch.isnan(Kc[b, n:].float()).all()
 
 
+@pytest.mark.parametrize("m,D,R", [(4, 128, 4 * 37 + 3), (128, 64, 128 * 3 + 50)])
+def test_compress_at_device_positions(m, D, R):
+    # positions and n_valid on the device: sequence 0 from token 0, sequence 1 from a later block,
+    # sequence 2 running past Ncap (blocks beyond it dropped), sequence 3 misaligned (skipped, reported)
+    B, n = 4, R // m
+    Ncap = n + 12
+    K = datagen.normal_bf16(15, 1, (B, R, D))
+    V = datagen.normal_bf16(15, 2, (B, R, D))
+    g = datagen.normal_f32(15, 3, (B, R))
+    e0 = [0, 9, Ncap - 5, 0]
+    tok0 = torch.tensor([e * m for e in e0[:3]] + [m + 1], dtype=torch.int64, device=DEV)
+    nv0 = [3, n + 20, 0, 2]
+    n_valid = torch.tensor(nv0, dtype=torch.int32, device=DEV)
+    Kc = torch.full((B, Ncap, D), float("nan"), dtype=torch.bfloat16, device=DEV)
+    Vc = torch.full_like(Kc, float("nan"))
+    lcc.compress_at(m, K.to(DEV), V.to(DEV), g.to(DEV), tok0, Kc, Vc, n_valid=n_valid)
+    torch.cuda.synchronize()
+    with pytest.raises(lcc.LccError, match="not a multiple of m"):
+        lcc.sync_status()
+    want_nv = [max(nv0[b], min(Ncap, e0[b] + n)) for b in range(3)] + [nv0[3]]
+    assert n_valid.cpu().tolist() == want_nv
+    for b in range(3):
+        ex_k, ex_v = oracle.pool_exact(f64(K[b]), f64(V[b]), f64(g[b]), m)
+        # fp32 arithmetic before the bf16 rounding: weights (exp, division) and the m products
+        # each within a few fp32 ulps of sum_i a_i |x_i|, which matters where the entry cancels
+        mag_k, mag_v = oracle.pool_exact(np.abs(f64(K[b])), np.abs(f64(V[b])), f64(g[b]), m)
+        lo, hi = e0[b], min(Ncap, e0[b] + n)
+        for what, gpu, ex, mag in (("K", Kc[b, lo:hi], ex_k[:hi - lo], mag_k[:hi - lo]),
+                                   ("V", Vc[b, lo:hi], ex_v[:hi - lo], mag_v[:hi - lo])):
+            gv = f64(gpu)
+            ulp = np.ldexp(1.0, np.frexp(np.abs(ex))[1] - 8) + np.ldexp(mag, -20)
+            r = np.abs(gv - ex) / ulp
+            assert np.isfinite(gv).all(), f"sequence {b} {what}: {np.sum(~np.isfinite(gv))} entries not written"
+            assert r.max() <= 1.0, f"sequence {b} {what}: {r.max():.3f} of the bound at {np.unravel_index(r.argmax(), r.shape)}"
+        assert torch.isnan(Kc[b, :lo].float()).all() and torch.isnan(Kc[b, hi:].float()).all()
+    assert torch.isnan(Kc[3].float()).all() and torch.isnan(Vc[3].float()).all()
+
+
 def test_compress_m1_is_a_copy():
     # m = 1 (the DSA comparator's cache): every token is its own entry
     B, R, D = 2, 77, 128
