@@ -364,7 +364,8 @@ lcc_status lcc_hca_layer_attn(const lcc_bf16* q, int B, int Tq, int H, int D, fl
  * (H/16) * 4096, k <= 128, a few query rows) go further: after the indexer,
  * one thread-block cluster per query (one CTA per 16 heads) selects the
  * top-k and attends, the index list passed between its CTAs on chip; the
- * index lists and outputs are identical to the two calls'.
+ * index lists are identical to the two calls', the outputs equal up to
+ * rounding (the attention walks the keys in 16-key tiles).
  * Arguments as the two calls; idx [B, Tq, k] int32 is written; workspace:
  * at least lcc_csa_layer_workspace(B, Tq, H, D, Ncap, k, W) bytes.
  * ---------------------------------------------------------------------- */

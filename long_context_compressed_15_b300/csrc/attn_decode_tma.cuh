@@ -20,17 +20,17 @@
 
 namespace lcc {
 
-template <int NW, int KT>
+template <int NW, int KT, int NB = 1>
 struct WsplitTmaSmem {
   static constexpr int D = 128;
   static constexpr size_t q_bytes = 16 * D * 2;                           // 4 KB, 1024-aligned region
   static constexpr size_t tile_bytes = size_t(2) * KT * D * 2;            // K and V of one warp tile
   static constexpr int CS = D + 8;
   static constexpr size_t comb_bytes = size_t(NW) * 16 * (CS + 2) * 4;
-  static constexpr size_t work = NW * tile_bytes > comb_bytes ? NW * tile_bytes : comb_bytes;
+  static constexpr size_t work = NW * NB * tile_bytes > comb_bytes ? NW * NB * tile_bytes : comb_bytes;
   static constexpr size_t off_work = (q_bytes + 1023) / 1024 * 1024;
   static constexpr size_t off_keys = off_work + (work + 1023) / 1024 * 1024;
-  static constexpr size_t off_bars = off_keys + NW * KT * 4;
+  static constexpr size_t off_bars = off_keys + NW * NB * KT * 4;
   static constexpr size_t total = off_bars + NW * 8 + 1024;               // + alignment slack
 };
 
@@ -40,20 +40,27 @@ struct WsplitTmaSmem {
 // (sidx[0..k)).  between() runs after the window rows and queries are
 // requested and before the index list is read: it waits for whatever
 // produces the list.
-template <int NW, int KT, bool SIDX, class Between>
+//
+// NB = 2 (every warp holds one selected-entry tile and one window tile, the
+// caller guarantees T1, T2 <= NW): a warp's window tile is requested before
+// between() and attended while its selected rows are still being gathered.
+template <int NW, int KT, bool SIDX, int NB = 1, class Between>
 __device__ __forceinline__ void attn_wsplit_tma_body(const CUtensorMap* tmK, const CUtensorMap* tmV,
                                                      const AttnArgs& a, uint8_t* smem, int qi, int h0, int b,
                                                      const int* sidx, Between& between) {
   constexpr int D = 128, CPR = D / 8, NKS = D / 16, NDT = D / 8;
   static_assert(KT % 4 == 0 && KT / 4 <= 32, "four rows per gather, one lane per gather");
-  using S = WsplitTmaSmem<NW, KT>;
+  static_assert(NB == 1 || NB == 2, "one or two tile buffers per warp");
+  using S = WsplitTmaSmem<NW, KT, NB>;
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   uint8_t* work = smem + S::off_work;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c4 = lane & 3;
-  bf16* sK = reinterpret_cast<bf16*>(work + warp * S::tile_bytes);
+  auto buf_k = [&](int bi) { return reinterpret_cast<bf16*>(work + (warp * NB + bi) * S::tile_bytes); };
+  auto buf_key = [&](int bi) { return reinterpret_cast<int*>(smem + S::off_keys) + (warp * NB + bi) * KT; };
+  bf16* sK = buf_k(0);
   bf16* sV = sK + KT * D;
-  int* sKey = reinterpret_cast<int*>(smem + S::off_keys) + warp * KT;
+  int* sKey = buf_key(0);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + S::off_bars) + warp;
 
   int lo2 = 0, hi2 = 0;
@@ -140,19 +147,50 @@ __device__ __forceinline__ void attn_wsplit_tma_body(const CUtensorMap* tmK, con
   uint32_t qf[NKS][4];
   int j0 = 0;
   pdl_trigger();
-  // window rows are inputs of the call; index lists come later
-  if (warp < T1 + T2 && warp >= T1) j0 = load_window(warp);
-  between();
-  if (warp < T1) j0 = load_gather(warp);
-  cp_async_wait<0>();
-  __syncthreads();  // queries visible to every warp
+  if constexpr (NB == 2) {
+    int jw = 0;
+    sK = buf_k(1);
+    sV = sK + KT * D;
+    sKey = buf_key(1);
+    if (warp < T2) jw = load_window(T1 + warp);  // an input of the call: requested before the wait
+    between();
+    sK = buf_k(0);
+    sV = sK + KT * D;
+    sKey = buf_key(0);
+    if (warp < T1) j0 = load_gather(warp);
+    cp_async_wait<0>();
+    __syncthreads();  // queries visible to every warp
 #pragma unroll
-  for (int ks = 0; ks < NKS; ++ks) {
-    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int cc = 2 * ks + (lane >> 4);
-    ldsm_x4(smem_u32(sQ + r * D + ((cc ^ (r & 7)) * 8)), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    for (int ks = 0; ks < NKS; ++ks) {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int cc = 2 * ks + (lane >> 4);
+      ldsm_x4(smem_u32(sQ + r * D + ((cc ^ (r & 7)) * 8)), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    }
+    if (warp < T2)  // the window tile first, while the gather is in flight
+      attn_tile_step<D, KT, false>(qf, buf_k(1), buf_k(1) + KT * D, buf_key(1), jw, lo2, hi2, lo2, hi2,
+                                   a.scale_log2, m0, m1, l0, l1, oacc);
+    if (warp < T1) {
+      tc::mbar_wait(bar, 0, 31);  // bounded; a timeout is recorded for lcc_sync_status
+      __syncwarp();
+      attn_tile_step<D, KT, true>(qf, buf_k(0), buf_k(0) + KT * D, buf_key(0), j0, 0, a.k, 0, a.k, a.scale_log2,
+                                  m0, m1, l0, l1, oacc);
+    }
   }
-  for (int tt = warp; tt < T1 + T2; tt += NW) {
+  // window rows are inputs of the call; index lists come later
+  if (NB == 1 && warp < T1 + T2 && warp >= T1) j0 = load_window(warp);
+  if constexpr (NB == 1) between();
+  if (NB == 1 && warp < T1) j0 = load_gather(warp);
+  if constexpr (NB == 1) {
+    cp_async_wait<0>();
+    __syncthreads();  // queries visible to every warp
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks) {
+      const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+      const int cc = 2 * ks + (lane >> 4);
+      ldsm_x4(smem_u32(sQ + r * D + ((cc ^ (r & 7)) * 8)), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+    }
+  }
+  for (int tt = warp; NB == 1 && tt < T1 + T2; tt += NW) {
     const bool gath = tt < T1;
     if (tt != warp) {
       __syncwarp();

@@ -16,7 +16,9 @@
 //     distributed shared memory, into the index list of every CTA of the
 //     cluster; one cluster barrier;
 //   * every CTA gathers the selected K/V rows by TMA and runs the attention
-//     of its 16 heads (attn_wsplit_tma_body) from its own copy of the list.
+//     of its 16 heads (attn_wsplit_tma_body, two 16-key tiles per warp: its
+//     window tile is attended while its selected rows are gathered) from its
+//     own copy of the list.
 #pragma once
 #include "attn_decode_tma.cuh"
 #include "topk_cluster.cuh"
@@ -40,7 +42,7 @@ struct TopkOutCluster {
 
 template <int NW, int KT, int PER, int CAP, int MAXG>
 struct CsaFusedSmem {
-  using A = WsplitTmaSmem<NW, KT>;
+  using A = WsplitTmaSmem<NW, KT, 2>;
   using T = TopkClSmem<NW * 32, PER, CAP, MAXG>;
   static constexpr size_t off_topk = (A::off_bars + NW * 8 + 127) / 128 * 128;
   static constexpr size_t off_idx = off_topk + T::total;
@@ -68,7 +70,7 @@ __global__ void __launch_bounds__(NW * 32) k_csa_decode_fused(const __grid_const
     topk_cluster_row<NW * 32, PER, CAP, MAXG>(t, smem + S::off_topk, row, out);
     clu::sync();  // CTA 0's list stores are visible in every CTA
   };
-  attn_wsplit_tma_body<NW, KT, true>(&tmK, &tmV, a, smem, qi, static_cast<int>(rk) * 16, b, sidx, select);
+  attn_wsplit_tma_body<NW, KT, true, 2>(&tmK, &tmV, a, smem, qi, static_cast<int>(rk) * 16, b, sidx, select);
 }
 
 }  // namespace lcc

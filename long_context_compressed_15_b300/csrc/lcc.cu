@@ -1208,7 +1208,8 @@ static_assert(kWsplitWarps * 32 == kClNT, "the fused kernel's top-k runs on the 
 // that an indexer CTA of the next call fits on the same SM (its launch then
 // overlaps this kernel)
 constexpr int kCfCap = 1024;
-using CfSmem = CsaFusedSmem<kWsplitWarps, kWsplitTile, kCfPer, kCfCap, kClMaxG>;
+constexpr int kCfTile = 16;  // keys per warp tile: one selected-entry and one window tile per warp
+using CfSmem = CsaFusedSmem<kWsplitWarps, kCfTile, kCfPer, kCfCap, kClMaxG>;
 unsigned long long g_csa_fused_done = 0;
 
 // Decode-shaped calls whose top-k fits the cluster selection (one CTA per 16
@@ -1220,7 +1221,8 @@ bool use_csa_fused(lcc_key_format fmt, int B, int Tq, int H, int D, int HI, floa
   const int cl = H / 16;
   const int64_t groups16 = static_cast<int64_t>(B) * Tq * cl;
   return !use_fused_topk(fmt, Tq, HI, k) && Ncap <= cl * kClNT * kCfPer && 2 * k <= kClMaxG &&
-         static_cast<int64_t>(k) * 8 <= kCfCap && !use_gather_tc(B, Tq, H, D, scale, Ncap, Rcap) &&
+         static_cast<int64_t>(k) * 8 <= kCfCap && k <= kWsplitWarps * kCfTile && W <= kWsplitWarps * kCfTile &&
+         !use_gather_tc(B, Tq, H, D, scale, Ncap, Rcap) &&
          use_wsplit<ATT_GATHER>(groups16, static_cast<int64_t>(k) + W) &&
          static_cast<int64_t>(B) * Ncap < (int64_t(1) << 31) && static_cast<int64_t>(Tq) * cl <= 0x7FFFFFFF &&
          B <= 65535 && index_chunk(B, Tq, Ncap) >= Tq;
@@ -1234,7 +1236,7 @@ lcc_status launch_csa_fused(const AttnArgs& a, const TopkThrArgs& t, int cl, cud
   if ((st = make_tmap_2d(&tv, a.V, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_csa_decode_fused V")) !=
       LCC_OK)
     return st;
-  auto kern = k_csa_decode_fused<kWsplitWarps, kWsplitTile, kCfPer, kCfCap, kClMaxG>;
+  auto kern = k_csa_decode_fused<kWsplitWarps, kCfTile, kCfPer, kCfCap, kClMaxG>;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
     if ((st = ensure_smem(kern, CfSmem::total, g_csa_fused_done)) != LCC_OK) return st;

@@ -110,7 +110,7 @@ __device__ __forceinline__ void pool_block_small(const float* g, const bf16* K, 
 // loads issued before any arithmetic, so that each lane keeps NB * M 16-byte
 // loads in flight; the arithmetic is pool_block_small's.
 template <int M, int D, int NB>
-__global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
+__global__ void __launch_bounds__(256, 2) k_pool_small(PoolArgs a) {
   constexpr int LPB = 2 * (D / 8);    // lanes per block (K and V)
   constexpr int BPW = 32 / LPB;       // blocks per warp and pass
   constexpr int LPR = D / 8;
@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
   const int b = blockIdx.y;
   const int64_t e0 = pool_entry0<M>(a, b, blockIdx.x == 0);
   if (e0 < 0) return;
+  // block j goes to entry e0 + j; blocks at or past `lim` fall beyond Ncap
+  bf16* const dst0 = (isV ? a.Vc : a.Kc) + b * a.c_bs + e0 * D + col;
+  const int64_t lim = a.tok0 ? a.Ncap - e0 : a.nblk;
   // the CTA's NB passes cover 8 * BPW * NB consecutive blocks
   const int64_t blk0 = static_cast<int64_t>(blockIdx.x) * 8 * BPW * NB + warp * BPW + sub;
   uint4 v[NB][M];
@@ -151,8 +154,7 @@ __global__ void __launch_bounds__(256) k_pool_small(PoolArgs a) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
     for (int i = 0; i < M; ++i) fma8(acc, gv[n][i] * inv, v[n][i]);
-    if (!a.tok0 || e0 + blk < a.Ncap)
-      *reinterpret_cast<uint4*>((isV ? a.Vc : a.Kc) + b * a.c_bs + (e0 + blk) * D + col) = pack8(acc);
+    if (blk < lim) *reinterpret_cast<uint4*>(dst0 + blk * D) = pack8(acc);
   }
 }
 

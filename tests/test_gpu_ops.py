@@ -797,8 +797,8 @@ def test_bounded_wait_runs_out_and_context_survives():
 ])
 def test_csa_layer_decode_one_cluster_per_query(H, B, Tq, Ncap, k, nval, nvfp4):
     # the whole layer call against the two-call composition (index + top-k, then the layer
-    # attention over that list): the same index lists and bit-identical outputs; and both
-    # against the oracle on every row
+    # attention over that list): the same index lists and outputs equal up to rounding; and
+    # the layer call against the oracle on every row
     D, W, HI, DI, m = 128, 128, 8, 64, 4
     seed = 40 + H
     q = datagen.normal_bf16(seed, 1, (B, Tq, H, D), 1.0 / np.sqrt(D))
@@ -831,7 +831,8 @@ def test_csa_layer_decode_one_cluster_per_query(H, B, Tq, Ncap, k, nval, nvfp4):
     torch.cuda.synchronize()
     lcc.sync_status()
     assert torch.equal(idx1, idx2)
-    assert torch.equal(out1, out2)
+    # the one-cluster path attends in 16-key tiles, the two-call path in 32-key ones: equal up to rounding
+    assert_close(out1.float().cpu().numpy(), out2.float().cpu().numpy(), "one cluster vs two calls")
     g, go = idx1.cpu().numpy(), out1.float().cpu().numpy()
     qh, Kch, Vch, Krh, Vrh = f64(q), f64(Kc), f64(Vc), f64(Kr), f64(Vr)
     near = 0
