@@ -264,7 +264,7 @@ __device__ __forceinline__ void attn_wsplit_tma_body(const CUtensorMap* tmK, con
   }
 }
 
-template <int NW, int KT>
+template <int NW, int KT, int NB = 1>
 __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_constant__ CUtensorMap tmK,
                                                              const __grid_constant__ CUtensorMap tmV, AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -272,8 +272,8 @@ __global__ void __launch_bounds__(NW * 32) k_attn_wsplit_tma(const __grid_consta
   const int hblocks = (a.H + 15) / 16;
   const int qi = blockIdx.x / hblocks, h0 = (blockIdx.x % hblocks) * 16;
   auto wait_lists = []() { pdl_wait(); };  // index lists may come from the previous kernel
-  attn_wsplit_tma_body<NW, KT, false>(&tmK, &tmV, a, smem, qi, h0, static_cast<int>(blockIdx.y), nullptr,
-                                      wait_lists);
+  attn_wsplit_tma_body<NW, KT, false, NB>(&tmK, &tmV, a, smem, qi, h0, static_cast<int>(blockIdx.y), nullptr,
+                                          wait_lists);
 }
 
 }  // namespace lcc

@@ -993,8 +993,12 @@ lcc_status launch_wsplit(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pd
 
 // CSA layer decode with the selected entries gathered by TMA (D = 128).
 unsigned long long g_wsplit_tma_done = 0;
-lcc_status launch_wsplit_tma(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pdl) {
-  using Sm = WsplitTmaSmem<kWsplitWarps, kWsplitTile>;
+// Lists of at most 8 x 16 selected entries and window rows: every warp takes
+// one 16-key tile of each (the window tile attended while the selected rows
+// are gathered); longer lists: 32-key tiles walked in turn.
+template <int KT, int NB>
+lcc_status launch_wsplit_tma_k(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pdl, unsigned long long& done) {
+  using Sm = WsplitTmaSmem<kWsplitWarps, KT, NB>;
   CUtensorMap tk, tv;
   const uint64_t rows = static_cast<uint64_t>(a.B) * a.Ncap;
   lcc_status st = make_tmap_2d(&tk, a.K, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_wsplit_tma K");
@@ -1002,13 +1006,20 @@ lcc_status launch_wsplit_tma(const AttnArgs& a, unsigned gx, cudaStream_t s, boo
   if ((st = make_tmap_2d(&tv, a.V, 128, rows, a.kv_rs, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B, "k_attn_wsplit_tma V")) !=
       LCC_OK)
     return st;
-  auto kern = k_attn_wsplit_tma<kWsplitWarps, kWsplitTile>;
+  auto kern = k_attn_wsplit_tma<kWsplitWarps, KT, NB>;
   {
     std::lock_guard<std::mutex> lk(g_attr_mu);
-    if ((st = ensure_smem(kern, Sm::total, g_wsplit_tma_done)) != LCC_OK) return st;
+    if ((st = ensure_smem(kern, Sm::total, done)) != LCC_OK) return st;
   }
   launch_k(kern, dim3(gx, a.B), dim3(kWsplitWarps * 32), Sm::total, s, pdl, tk, tv, a);
   return launch_check("k_attn_wsplit_tma");
+}
+unsigned long long g_wsplit_tma2_done = 0;
+lcc_status launch_wsplit_tma(const AttnArgs& a, unsigned gx, cudaStream_t s, bool pdl) {
+  constexpr int KT2 = 16;
+  if (a.k <= kWsplitWarps * KT2 && a.W <= kWsplitWarps * KT2)
+    return launch_wsplit_tma_k<KT2, 2>(a, gx, s, pdl, g_wsplit_tma2_done);
+  return launch_wsplit_tma_k<kWsplitTile, 1>(a, gx, s, pdl, g_wsplit_tma_done);
 }
 
 // One pass over (compressed source ++ window rows) -> bf16 layer output.
