@@ -90,18 +90,47 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
   const int lane = threadIdx.x & 31;
   pdl_wait();  // the partials come from the split attention kernel
   if (row >= rows) return;
-  // every split's lse at once (lane s holds splits s, s+32, ...), then weights
-  float L = -INFINITY;
-  for (int s = lane; s < nsplit; s += 32) L = fmaxf(L, __ldg(lp + s * rows + row));
+  // the first CH splits' partial rows are requested together with every
+  // split's lse (lane s holds splits s, s+32, ...): for up to CH splits the
+  // reduction waits on one round of loads
+  constexpr int CH = 24;
+  const float ls0 = lane < nsplit ? __ldg(lp + static_cast<int64_t>(lane) * rows + row) : -INFINITY;
+  const int n0 = min(CH, nsplit);
+  float x0[CH][PER];
+#pragma unroll
+  for (int u = 0; u < CH; ++u) {
+    const bool in = u < n0;  // an empty split's partial is written as zeros
+    const float* src = Op + (static_cast<int64_t>(u) * rows + row) * D + lane * PER;
+    if constexpr (PER == 4) {
+      const float4 v = in ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      x0[u][0] = v.x; x0[u][1] = v.y; x0[u][2] = v.z; x0[u][3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < PER; ++e) x0[u][e] = in ? __ldg(src + e) : 0.f;
+    }
+  }
+  float L = ls0;
+  for (int s = lane + 32; s < nsplit; s += 32) L = fmaxf(L, __ldg(lp + static_cast<int64_t>(s) * rows + row));
   L = warp_max(L);
   float acc[PER];
 #pragma unroll
   for (int e = 0; e < PER; ++e) acc[e] = 0.f;
   float tot = 0.f;
   if (L != -INFINITY) {
-    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+    const float wl0 = ls0 == -INFINITY ? 0.f : expf(ls0 - L);
+#pragma unroll
+    for (int u = 0; u < CH; ++u) {
+      const float w = __shfl_sync(0xffffffffu, wl0, u);
+      if (u < n0) {
+        tot += w;
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x0[u][e], acc[e]);
+      }
+    }
+    // further splits, 32 at a time (lane s holds split s0 + s)
+    for (int s0 = CH; s0 < nsplit; s0 += 32) {
       const int sl = s0 + lane;
-      const float ls = sl < nsplit ? __ldg(lp + sl * rows + row) : -INFINITY;
+      const float ls = sl < nsplit ? __ldg(lp + static_cast<int64_t>(sl) * rows + row) : -INFINITY;
       const float wl = ls == -INFINITY ? 0.f : expf(ls - L);
       const int n = min(32, nsplit - s0);
       // partial rows are independent loads: up to 16 vector loads in flight per lane
@@ -111,8 +140,8 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           wj[u] = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
-          const bool in = j + u < n;  // an empty split's partial is written as zeros
-          const float* src = Op + ((s0 + j + u) * rows + row) * D + lane * PER;
+          const bool in = j + u < n;
+          const float* src = Op + (static_cast<int64_t>(s0 + j + u) * rows + row) * D + lane * PER;
           if constexpr (PER == 4) {
             const float4 v = in ? __ldg(reinterpret_cast<const float4*>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
             x[u][0] = v.x; x[u][1] = v.y; x[u][2] = v.z; x[u][3] = v.w;
