@@ -58,7 +58,11 @@ Readings where the pages are silent:
      top-k; a re-index layer scores only the notes, with its own indexer
      query and weights against the same indexer keys, and attends to its
      top-k among them; a reuse layer attends to the entries the layer before
-     it selected; each layer attends to its own compressed cache.
+     it selected; each layer attends to its own compressed cache;
+  R16 the indexer "runs in FP4": its query is quantised to NVFP4 by R7's
+     rule (per group of 16: scale = e4m3 nearest to amax/6, elements = e2m1
+     nearest to x/scale, ties to even, saturating) and its keys are NVFP4;
+     the head weights stay fp32.
 
 Parity unpinned: the pages print no worked numeric example and no model
 dimensions, so the model-level figures (27% of V3.2's per-token FLOPs, ~10%
@@ -68,15 +72,15 @@ Every function below is pinned by closed forms, brute force or library
 special cases in tests/test_oracle_pins.py.
 """
 from .formats import (bf16_to_f64, f64_to_bf16_bits, round_bf16, e2m1_value,
-                      e4m3_value, nvfp4_decode)
+                      e4m3_value, nvfp4_decode, nvfp4_quantize, nearest_code)
 from .method import (pool_weights, pool_exact, pool, visible_count, index_scores,
-                     topk_select, attend, window_positions, merge, rms_norm, rope_partial,
+                     index_scores_fp4, topk_select, attend, window_positions, merge, rms_norm, rope_partial,
                      qkv_prologue)
 from . import runs
 
 __all__ = [
     "bf16_to_f64", "f64_to_bf16_bits", "round_bf16", "e2m1_value", "e4m3_value",
-    "nvfp4_decode", "pool_weights", "pool_exact", "pool", "visible_count",
+    "nvfp4_decode", "nvfp4_quantize", "nearest_code", "index_scores_fp4", "pool_weights", "pool_exact", "pool", "visible_count",
     "index_scores", "topk_select", "attend", "window_positions", "merge", "rms_norm",
     "rope_partial", "qkv_prologue", "runs",
 ]

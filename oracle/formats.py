@@ -71,3 +71,55 @@ def nvfp4_decode(packed, scale) -> np.ndarray:
     vals = np.stack([lo, hi], axis=-1).reshape(*p.shape[:-1], p.shape[-1] * 2)
     sc = np.repeat(e4m3_value(s), 16, axis=-1)
     return vals * sc
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 quantisation of the indexer query ([HYBRID]: the lightning indexer
+# runs in FP4; reading R16)
+# ---------------------------------------------------------------------------
+E2M1_MAGNITUDES = e2m1_value(np.arange(8))      # codes 0..7: 0, .5, 1, 1.5, 2, 3, 4, 6
+E4M3_NONNEGATIVE = e4m3_value(np.arange(127))   # codes 0..126: 0 .. 448 (127 is NaN)
+
+
+def nearest_code(y, table) -> np.ndarray:
+    """Code of the table value nearest to each y (table ascending).
+
+    Found by measuring the distance to every table value.  When two values
+    are equally near (they are neighbours, one with an even code and one with
+    an odd code) the even code wins: round to nearest, ties to even mantissa.
+    A y beyond the last value gets the last code (saturation).
+    """
+    table = np.asarray(table, np.float64)
+    # beyond the last value the last code is nearest; clamping first keeps a
+    # huge y from making every distance round to the same number
+    y = np.minimum(np.asarray(y, np.float64), table[-1])
+    d = np.abs(y[..., None] - table)
+    hit = d == d.min(axis=-1, keepdims=True)
+    even = hit & (np.arange(len(table)) % 2 == 0)
+    return np.where(even.any(axis=-1), even.argmax(axis=-1), hit.argmax(axis=-1))
+
+
+def nvfp4_quantize(x):
+    """fp64 [..., D] (D % 16 == 0) -> NVFP4 (packed uint8 [..., D/2], scale uint8 [..., D/16]).
+
+    Reading R16, the rule of R7's keys applied to the indexer query: the
+    scale of each group of 16 is the e4m3 value nearest to amax/6 (ties to
+    even, saturating at 448); every element becomes the e2m1 value nearest to
+    x/scale (ties to even, saturating at 6), sign kept, a zero magnitude
+    stored as +0; a zero scale stores all-zero codes.  These decisions are
+    exact in fp64 and in fp32 alike: for bf16 inputs, amax/6 and x/scale are
+    never within 2^-9 (relative) of a rounding boundary unless they lie on it.
+    """
+    x = np.asarray(x, np.float64)
+    D = x.shape[-1]
+    assert D % 16 == 0
+    g = x.reshape(*x.shape[:-1], D // 16, 16)
+    amax = np.abs(g).max(axis=-1)
+    sc = nearest_code(amax / 6.0, E4M3_NONNEGATIVE)
+    s = E4M3_NONNEGATIVE[sc]
+    y = np.abs(g) / np.where(s > 0, s, 1.0)[..., None]
+    mag = np.where(s[..., None] > 0, nearest_code(y, E2M1_MAGNITUDES), 0)
+    code = mag | np.where((g < 0) & (mag > 0), 8, 0)
+    code = code.reshape(*x.shape[:-1], D)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    return packed, sc.astype(np.uint8)

@@ -5,7 +5,7 @@ reordered.  Citation keys are defined in oracle/__init__.py.
 """
 import numpy as np
 
-from .formats import round_bf16
+from .formats import nvfp4_decode, nvfp4_quantize, round_bf16
 
 
 # ---------------------------------------------------------------------------
@@ -73,6 +73,19 @@ def index_scores(qI, w, kI) -> np.ndarray:
     """
     dots = np.asarray(kI, np.float64) @ np.asarray(qI, np.float64).T   # [n, HI]
     return np.maximum(dots, 0.0) @ np.asarray(w, np.float64)
+
+
+def index_scores_fp4(qI, w, kI_packed, kI_scale) -> np.ndarray:
+    """Indexer score with the indexer in FP4.
+
+    [HYBRID]: the lightning indexer runs in FP4; [V41]: the keys it reads are
+    kept in FP4.  Reading R16: the query is quantised to NVFP4 (per (head)
+    row, groups of 16, nvfp4_quantize) and the keys are NVFP4 (R7); the score
+    is R3's on the decoded values.
+    qI: [HI, DI] (bf16 values), w: [HI], kI_packed: [n, DI/2], kI_scale: [n, DI/16].
+    """
+    q = nvfp4_decode(*nvfp4_quantize(qI))
+    return index_scores(q, w, nvfp4_decode(kI_packed, kI_scale))
 
 
 def topk_select(s, k):

@@ -99,6 +99,100 @@ def test_nvfp4_values_fit_bf16_exactly():
     assert np.array_equal(oracle.round_bf16(prod.ravel()), prod.ravel())
 
 
+# NVFP4 quantisation of the indexer query (reading R16)
+def test_nvfp4_quantize_hand_case():
+    # amax 3 -> scale 3/6 = 0.5 = e4m3 0x30; x/0.5: 0.2 -> 0, -0.4 -> -0.5 (code 9),
+    # 6 -> 6 (code 7), 1.4 -> 1.5 (code 3); element 2i in the low nibble of byte i
+    x = np.array([[0.1, -0.2, 3.0, 0.7] * 4])
+    packed, scale = oracle.nvfp4_quantize(x)
+    assert scale.tolist() == [[0x30]]
+    assert packed.tolist() == [[0x90, 0x37] * 4]
+    assert oracle.nvfp4_decode(packed, scale).tolist() == [[0.0, -0.25, 3.0, 0.75] * 4]
+
+
+def test_nvfp4_quantize_ties_go_to_even_codes():
+    # x/scale exactly between two e2m1 values: the neighbour with the even code
+    # (even mantissa bit) is kept; hand table of the seven midpoints
+    want = {0.25: 0.0, 0.75: 1.0, 1.25: 1.0, 1.75: 2.0, 2.5: 2.0, 3.5: 4.0, 5.0: 4.0}
+    for s in (2.0 ** -9, 2.0 ** -6, 0.375, 1.0, 13.0, 448.0):
+        for mid, v in want.items():
+            row = np.zeros(16)
+            row[0] = 6.0 * s            # amax = 6 s -> scale exactly s
+            row[1], row[2] = mid * s, -mid * s
+            p, sc = oracle.nvfp4_quantize(row[None])
+            d = oracle.nvfp4_decode(p, sc)[0]
+            assert oracle.e4m3_value(sc[0, 0]) == s
+            assert d[1] == v * s and d[2] == -v * s, (s, mid)
+
+
+def test_nvfp4_quantize_grid_values_round_trip():
+    # values already on the grid of a group whose amax is 6*scale come back unchanged
+    r = np.random.default_rng(7)
+    codes = r.integers(0, 16, size=(300, 64))
+    codes[:, ::16] = 7                       # each group holds +6
+    codes = np.where(codes == 8, 0, codes)   # -0 is stored as +0
+    scales = r.integers(1, 127, size=(300, 4)).astype(np.uint8)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    x = oracle.nvfp4_decode(packed, scales)
+    p2, s2 = oracle.nvfp4_quantize(x)
+    assert np.array_equal(s2, scales) and np.array_equal(p2, packed)
+
+
+def test_nvfp4_quantize_is_nearest_by_brute_force():
+    # every element lands on a grid value of its group no farther than any other one
+    r = np.random.default_rng(8)
+    x = _bf16_grid((64, 64)) * np.exp(r.uniform(-6, 6, size=(64, 1)))
+    p, sc = oracle.nvfp4_quantize(x)
+    d = oracle.nvfp4_decode(p, sc)
+    s = np.repeat(oracle.e4m3_value(sc), 16, axis=-1)
+    grid = oracle.e2m1_value(np.arange(16))                 # all 16 codes
+    err = np.abs(x - d)
+    best = np.abs(x[..., None] - grid * s[..., None]).min(axis=-1)
+    assert np.all(err <= best)
+
+
+def test_nvfp4_scale_every_bf16_amax_vs_library_rounding():
+    # every positive finite bf16 value as a group maximum: the scale is the e4m3
+    # value nearest to amax/6 -- torch's float8_e4m3fn rounding below 448, and
+    # saturation at 448 above it
+    bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    amax = oracle.bf16_to_f64(bits)
+    g = np.zeros((amax.size, 16))
+    g[:, 5] = amax
+    _, sc = oracle.nvfp4_quantize(g)
+    got = oracle.e4m3_value(sc[:, 0])
+    small = amax / 6.0 < 448.0
+    lib = torch.from_numpy(amax[small] / 6.0).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(got[small], lib)
+    assert np.all(got[~small] == 448.0)
+
+
+def test_nvfp4_quantize_agrees_with_the_key_encoder():
+    # the input generator encodes NVFP4 keys by formulas (frexp/round), the
+    # oracle by distance to every table value: two independent codings of R7
+    import datagen
+    r = np.random.default_rng(9)
+    x = _bf16_grid((512, 64)) * np.exp(r.uniform(-12, 8, size=(512, 1)))
+    p1, s1 = oracle.nvfp4_quantize(x)
+    p2, s2 = datagen.nvfp4_encode(torch.from_numpy(x))
+    assert np.array_equal(s1, s2.numpy()) and np.array_equal(p1, p2.numpy())
+
+
+def test_index_scores_fp4_hand_case():
+    # query head 0: amax 6 -> scale 1: [6, 3, 0.7, -0.2] -> [6, 3, 0.5, 0];
+    # head 1 is its negative.  Key: codes 1, 2, 4 (0.5, 1, 2) at scale 2 -> [1, 2, 4].
+    # head 0: 6 + 6 + 2 = 14, weight 0.5 -> 7; head 1: ReLU(-14) = 0
+    qI = np.zeros((2, 16))
+    qI[0, :4] = [6.0, 3.0, 0.7, -0.2]
+    qI[1] = -qI[0]
+    w = np.array([0.5, 3.0])
+    kp = np.zeros((1, 8), np.uint8)
+    kp[0, 0] = 0x21
+    kp[0, 1] = 0x04
+    ks = np.array([[0x40]], np.uint8)
+    assert oracle.index_scores_fp4(qI, w, kp, ks).tolist() == [7.0]
+
+
 # ---------------------------------------------------------------------------
 # pooling
 # ---------------------------------------------------------------------------
