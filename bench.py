@@ -642,7 +642,49 @@ class CsaPrefillBench:
         d["pool"] = {"kernel": "k_pool_small<4,128,4>", "bound": "hbm", "bytes": nbytes, "launch_us": round(tp * 1e6, 3),
                      "achieved_gbs": round(nbytes / tp / 1e9, 1), "frac": round(nbytes / tp / 1e9 / hbm, 4),
                      "timing": "one launch after an L2 flush, median of 4"}
+        d["fp4_indexer"] = self.fp4_indexer(stream)
         return d
+
+    def fp4_indexer(self, stream):
+        """The indexer in FP4 over the same prefill: the query quantised to NVFP4 and
+        NVFP4 keys (quantiser + key expansion + the fused indexer/top-k), against the
+        bf16 indexer call, each timed alone with CUDA events (median of 4 after 2)."""
+        import datagen
+        import long_context_compressed_15_b300 as lcc
+        c, g = self.cfg, self.g
+        dev = g["qI"].device
+        kp, ks = datagen.nvfp4_normal(c.seed, 77, c.N, c.DI, device=dev)
+        kp, ks = kp.reshape(1, c.N, c.DI // 2), ks.reshape(1, c.N, c.DI // 16)
+        ws4 = torch.empty(lcc.fp4_index_topk_workspace(1, c.T, c.HI, c.DI, c.N, c.k), dtype=torch.uint8, device=dev)
+        idx4 = torch.empty_like(self.plan.idx)
+
+        def fp4():
+            lcc.fp4_index_topk(g["qI"], g["w"], 0, kp, ks, c.N, c.m, c.k, idx=idx4, workspace=ws4)
+
+        def bf16():
+            self.dominant_steps(0, 1)
+
+        def timed(fn):
+            times = []
+            for i in range(6):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                if i >= 2:
+                    times.append(e0.elapsed_time(e1) / 1e3)
+            return float(np.median(times))
+
+        t4, t16 = timed(fp4), timed(bf16)
+        lcc.sync_status()
+        del ws4
+        work = self.dominant_work()
+        return {"call": "lcc_fp4_index_topk (k_nvfp4_quant + k_nvfp4_expand + k_index_topk_pw)",
+                "ms": round(t4 * 1e3, 3), "tflops": round(work / t4 / 1e12, 1),
+                "bf16_indexer_ms": round(t16 * 1e3, 3), "fp4_over_bf16_time": round(t4 / t16, 4),
+                "keys": "NVFP4 N(0,1) keys, 32768 entries; query quantised to NVFP4 by the call"}
 
 
 class HcaPrefillBench:

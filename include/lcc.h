@@ -278,6 +278,57 @@ lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const float* w,
                                             int32_t* idx, float* score, void* stream);
 
 /* ---------------------------------------------------------------------- *
+ * NVFP4 quantisation ([HYBRID]: the lightning indexer runs in FP4; [V41]:
+ * the global KV cache is kept in FP4).  Row layout as the NVFP4 indexer keys:
+ * e2m1 codes, element 2c in the low nibble of byte c, one e4m3 scale per 16
+ * consecutive elements.  Each group of 16 is quantised as
+ *   scale  = the e4m3 value nearest to amax/6 (ties to even, saturating at 448);
+ *   code_i = the e2m1 value nearest to x_i/scale (ties to even, saturating
+ *            at 6) with x_i's sign; magnitude 0 is stored as +0 and a zero
+ *            scale stores all-zero codes.
+ * The decisions are exact (no rounding step can move a value across a
+ * boundary), so the codes are unique for every finite bf16 input; inputs must
+ * be finite.
+ *
+ * lcc_nvfp4_quantize: x [rows, D] bf16 with rows ld elements apart (ld >= D,
+ * ld*2 a multiple of 16 bytes, x 16-byte aligned); D a positive multiple of
+ * 16.  Outputs, each optional (NULL skips it): packed [rows, D/2] uint8
+ * (8-byte aligned), scale [rows, D/16] uint8, xq [rows, D] bf16 = the
+ * dequantised values (16-byte aligned; exact: every e2m1 x e4m3 product is a
+ * bf16 value).  The caller owns every buffer; nothing is allocated.
+ * lcc_nvfp4_dequantize: packed/scale as above, contiguous rows -> x [rows, D]
+ * bf16 (exact).
+ * ---------------------------------------------------------------------- */
+lcc_status lcc_nvfp4_quantize(const lcc_bf16* x, int64_t rows, int D, int64_t ld,
+                              uint8_t* packed, uint8_t* scale, lcc_bf16* xq, void* stream);
+lcc_status lcc_nvfp4_dequantize(const uint8_t* packed, const uint8_t* scale, int64_t rows, int D,
+                                lcc_bf16* x, void* stream);
+
+/* The lightning indexer in FP4 ([HYBRID], section "두 가지 압축 전략: CSA 및
+ * HCA": the indexer runs in FP4).  As lcc_lightning_index_topk with NVFP4
+ * keys, but the indexer query is first quantised to NVFP4 by
+ * lcc_nvfp4_quantize's rule (per (query, head) row, groups of 16): the score
+ * of entry j is
+ *   s = sum_h w[b,i,h] * max(0, Q(qI[b,i,h,:]) . kI[b,j,:])
+ * with Q the quantise-dequantise map and both vectors in their exact NVFP4
+ * values; the head weights stay fp32.  Products of two NVFP4 values are exact
+ * in fp32, so the result equals the block-scaled FP4 contraction up to the
+ * order of the fp32 sums.
+ * kI [B, Ncap, DI/2] uint8 (8-byte aligned), kI_scale [B, Ncap, DI/16];
+ * HI = 8, DI = 64; other arguments as lcc_lightning_index_topk.
+ * workspace: at least lcc_fp4_index_topk_workspace(B, Tq, HI, DI, Ncap, k)
+ * bytes, 16-byte aligned.  Prefill shapes (Tq*HI > 16, k <= 256) expand the
+ * keys to bf16 in the workspace once per call (36 bytes read and 128 written
+ * per entry) and run the tensor-core indexer with the top-k fused into its
+ * epilogue; other shapes run the NVFP4-key indexer on the quantised query. */
+size_t lcc_fp4_index_topk_workspace(int B, int Tq, int HI, int DI, int Ncap, int k);
+lcc_status lcc_fp4_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                              const int64_t* q_pos0, const uint8_t* kI, const uint8_t* kI_scale,
+                              const int32_t* n_valid, int Ncap, int m, int k,
+                              int32_t* idx, float* score,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------- *
  * CSA sparse attention: MQA (all H heads share one K/V row, [HYBRID]) over
  * the k entries idx[b,i,:] of the compressed cache; entries < 0 are skipped.
  *   z_h,j = scale * q[b,i,h,:] . Kc[b,idx_j,:];  lse = log sum_j e^z;

@@ -46,6 +46,10 @@ _SIGS = {
     "lcc_index_topk_workspace": [_I, _I, _I, _I],
     "lcc_lightning_index_topk": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
     "lcc_lightning_index_topk_noalloc": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _I, _P, _P, _P],
+    "lcc_nvfp4_quantize": [_P, _L, _I, _L, _P, _P, _P, _P],
+    "lcc_nvfp4_dequantize": [_P, _P, _L, _I, _P, _P],
+    "lcc_fp4_index_topk_workspace": [_I, _I, _I, _I, _I, _I],
+    "lcc_fp4_index_topk": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _Z, _P],
     "lcc_lightning_index_scores": [_P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _I, _I, _P, _P],
     "lcc_csa_sparse_attn": [_P, _I, _I, _I, _I, _F, _P, _P, _L, _I, _P, _I, _P, _P, _P],
     "lcc_dense_attn_workspace": [_I, _I, _I, _I, _I],
@@ -66,7 +70,7 @@ _SIGS = {
     "lcc_launch_count": [],
     "lcc_test_set_wait_fault": [ctypes.c_uint64, _I],
 }
-_RET = {"lcc_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z, "lcc_csa_layer_workspace": _Z,
+_RET = {"lcc_index_topk_workspace": _Z, "lcc_fp4_index_topk_workspace": _Z, "lcc_dense_attn_workspace": _Z, "lcc_layer_attn_workspace": _Z, "lcc_csa_layer_workspace": _Z,
         "lcc_last_error": ctypes.c_char_p, "lcc_version": ctypes.c_char_p, "lcc_launch_count": ctypes.c_uint64}
 
 
@@ -329,6 +333,81 @@ def lightning_index_topk(qI, w, q_pos0, kI, n_valid, m, k, kI_scale=None, idx=No
     _call("lcc_lightning_index_topk", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), fmt, _ptr(kI),
           _ptr(kI_scale), _ptr(n_valid), Ncap, int(m), int(k), _ptr(idx), _ptr(score),
           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return idx
+
+
+def nvfp4_quantize(x, packed=None, scale=None, xq=None, stream=None):
+    """NVFP4 quantisation of the rows of x [..., D] bf16 (D % 16 == 0, rows may
+    be strided): per group of 16, scale = e4m3 nearest to amax/6 and codes =
+    e2m1 nearest to x/scale (ties to even, saturating).  Returns (packed uint8
+    [..., D/2], scale uint8 [..., D/16], xq bf16 [..., D] dequantised)."""
+    _need(x, torch.bfloat16, "x")
+    D = x.shape[-1]
+    rows = x.numel() // D if D else 0
+    x2 = x.reshape(rows, D) if x.dim() != 2 else x
+    if x2.stride(1) != 1:
+        raise ValueError("x rows must be contiguous in their last dimension")
+    lead = tuple(x.shape[:-1])
+    dev = x.device
+    if packed is None:
+        packed = torch.empty(lead + (D // 2,), dtype=torch.uint8, device=dev)
+    if scale is None:
+        scale = torch.empty(lead + (D // 16,), dtype=torch.uint8, device=dev)
+    if xq is None:
+        xq = torch.empty(lead + (D,), dtype=torch.bfloat16, device=dev)
+    for t, n in ((packed, "packed"), (scale, "scale"), (xq, "xq")):
+        if not t.is_contiguous():
+            raise ValueError(f"{n} must be contiguous")
+    _call("lcc_nvfp4_quantize", _ptr(x2), rows, D, x2.stride(0) if rows else D, _ptr(packed), _ptr(scale),
+          _ptr(xq), _stream(stream))
+    return packed, scale, xq
+
+
+def nvfp4_dequantize(packed, scale, out=None, stream=None):
+    """NVFP4 rows (packed uint8 [..., D/2], scale uint8 [..., D/16]) -> bf16 [..., D] (exact)."""
+    _need(packed, torch.uint8, "packed")
+    _need(scale, torch.uint8, "scale")
+    if not (packed.is_contiguous() and scale.is_contiguous()):
+        raise ValueError("packed and scale must be contiguous")
+    D = packed.shape[-1] * 2
+    rows = packed.numel() // packed.shape[-1] if packed.shape[-1] else 0
+    if out is None:
+        out = torch.empty(tuple(packed.shape[:-1]) + (D,), dtype=torch.bfloat16, device=packed.device)
+    _call("lcc_nvfp4_dequantize", _ptr(packed), _ptr(scale), rows, D, _ptr(out), _stream(stream))
+    return out
+
+
+def fp4_index_topk_workspace(B, Tq, HI, DI, Ncap, k) -> int:
+    return int(load().lcc_fp4_index_topk_workspace(B, Tq, HI, DI, Ncap, k))
+
+
+def fp4_index_topk(qI, w, q_pos0, kI, kI_scale, n_valid, m, k, idx=None, score=None, workspace=None, stream=None):
+    """The lightning indexer in FP4: qI [B, Tq, 8, 64] bf16 is quantised to NVFP4
+    (nvfp4_quantize's rule) and scored against the NVFP4 keys kI [B, Ncap, 32]
+    uint8 / kI_scale [B, Ncap, 4]; otherwise as lightning_index_topk.  Returns
+    idx [B, Tq, k] int32 (and writes score [B, Tq, k] fp32 if given)."""
+    _need(qI, torch.bfloat16, "qI", 4)
+    _need(w, torch.float32, "w", 3)
+    _need(kI, torch.uint8, "kI", 3)
+    _need(kI_scale, torch.uint8, "kI_scale", 3)
+    if not (qI.is_contiguous() and w.is_contiguous() and kI.is_contiguous() and kI_scale.is_contiguous()):
+        raise ValueError("qI, w, kI and kI_scale must be contiguous")
+    B, Tq, HI, DI = qI.shape
+    Ncap = kI.shape[1]
+    dev = qI.device
+    q_pos0 = _positions(q_pos0, B, dev)
+    n_valid = _positions(n_valid, B, dev, torch.int32)
+    if idx is None:
+        idx = torch.empty((B, Tq, k), dtype=torch.int32, device=dev)
+    _need(idx, torch.int32, "idx", 3)
+    if score is not None:
+        _need(score, torch.float32, "score", 3)
+    need = fp4_index_topk_workspace(B, Tq, HI, DI, Ncap, k)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _call("lcc_fp4_index_topk", _ptr(qI), _ptr(w), B, Tq, HI, DI, _ptr(q_pos0), _ptr(kI), _ptr(kI_scale),
+          _ptr(n_valid), Ncap, int(m), int(k), _ptr(idx), _ptr(score), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream(stream))
     return idx
 
 

@@ -16,6 +16,7 @@
 #include "decode_step.cuh"
 #include "prologue.cuh"
 #include "reindex.cuh"
+#include "nvfp4.cuh"
 #include <cmath>
 #include <type_traits>
 #include "merge.cuh"
@@ -1544,3 +1545,118 @@ extern "C" lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const
   return run_index_topk(qI, w, B, Tq, HI, DI, q_pos0, fmt, kI, kI_scale, n_valid, Ncap, m, k, idx, score, scratch, qc,
                         static_cast<cudaStream_t>(stream));
 }
+
+// ------------------------------------------------------------------ NVFP4
+namespace {
+lcc_status launch_nvfp4_quant(const lcc_bf16* x, int64_t rows, int D, int64_t ld, uint8_t* packed, uint8_t* scale,
+                              lcc_bf16* xq, cudaStream_t s) {
+  const int64_t groups = rows * (D / 16);
+  if (groups == 0) return LCC_OK;
+  Nvfp4QuantArgs a{reinterpret_cast<const bf16*>(x), rows, D / 16, ld, packed, scale, reinterpret_cast<bf16*>(xq)};
+  launch_k(k_nvfp4_quant, dim3(static_cast<unsigned>((groups + 255) / 256)), dim3(256), 0, s, false, a);
+  return launch_check("k_nvfp4_quant");
+}
+
+lcc_status launch_nvfp4_expand(const uint8_t* packed, const uint8_t* scale, int64_t rows, int D, lcc_bf16* out,
+                               cudaStream_t s) {
+  const int64_t groups = rows * (D / 16);
+  if (groups == 0) return LCC_OK;
+  Nvfp4ExpandArgs a{packed, scale, rows, D / 16, reinterpret_cast<bf16*>(out)};
+  launch_k(k_nvfp4_expand, dim3(static_cast<unsigned>((groups + 255) / 256)), dim3(256), 0, s, true, a);
+  return launch_check("k_nvfp4_expand");
+}
+
+lcc_status check_nvfp4_shape(const char* name, int64_t rows, int D) {
+  if (rows < 0) return fail(LCC_ERR_SHAPE, "%s: rows=%lld must be >= 0", name, static_cast<long long>(rows));
+  if (D <= 0 || D % 16) return fail(LCC_ERR_SHAPE, "%s: D=%d must be a positive multiple of 16", name, D);
+  if (rows * (D / 16) > 0x7FFFFFFFLL * 256)
+    return fail(LCC_ERR_SHAPE, "%s: %lld groups of 16", name, static_cast<long long>(rows * (D / 16)));
+  return LCC_OK;
+}
+
+// Scratch of the FP4 indexer: the dequantised query, then either the keys
+// expanded to bf16 (prefill shapes, fused top-k) or the indexer's chunk scratch.
+struct Fp4Ws {
+  size_t q, keys, index, total;
+};
+Fp4Ws fp4_ws(int B, int Tq, int HI, int DI, int Ncap, int k) {
+  Fp4Ws w{};
+  if (B <= 0 || Tq <= 0 || Ncap <= 0 || k <= 0 || HI <= 0 || DI <= 0) return w;
+  w.q = round_up(static_cast<size_t>(B) * Tq * HI * DI * sizeof(bf16), 256);
+  if (use_fused_topk(LCC_KEY_BF16, Tq, HI, k))
+    w.keys = round_up(static_cast<size_t>(B) * Ncap * DI * sizeof(bf16), 256);
+  else
+    w.index = index_ws(B, Tq, Ncap, k).total;
+  w.total = w.q + w.keys + w.index;
+  return w;
+}
+}  // namespace
+
+extern "C" {
+
+lcc_status lcc_nvfp4_quantize(const lcc_bf16* x, int64_t rows, int D, int64_t ld, uint8_t* packed, uint8_t* scale,
+                              lcc_bf16* xq, void* stream) {
+  const char* name = "lcc_nvfp4_quantize";
+  lcc_status st = check_nvfp4_shape(name, rows, D);
+  if (st != LCC_OK) return st;
+  if (ld < D) return fail(LCC_ERR_SHAPE, "%s: ld=%lld < D=%d", name, static_cast<long long>(ld), D);
+  if (rows == 0) return LCC_OK;
+  if (!x) return fail(LCC_ERR_ARG, "%s: x is NULL", name);
+  if (!aligned16(x) || (ld * 2) % 16)
+    return fail(LCC_ERR_ALIGN, "%s: x and its row stride (ld*2 bytes) must be 16-byte aligned", name);
+  if (packed && (reinterpret_cast<uintptr_t>(packed) & 7))
+    return fail(LCC_ERR_ALIGN, "%s: packed must be 8-byte aligned", name);
+  if (xq && !aligned16(xq)) return fail(LCC_ERR_ALIGN, "%s: xq must be 16-byte aligned", name);
+  return launch_nvfp4_quant(x, rows, D, ld, packed, scale, xq, static_cast<cudaStream_t>(stream));
+}
+
+lcc_status lcc_nvfp4_dequantize(const uint8_t* packed, const uint8_t* scale, int64_t rows, int D, lcc_bf16* x,
+                                void* stream) {
+  const char* name = "lcc_nvfp4_dequantize";
+  lcc_status st = check_nvfp4_shape(name, rows, D);
+  if (st != LCC_OK) return st;
+  if (rows == 0) return LCC_OK;
+  if (!packed || !scale || !x) return fail(LCC_ERR_ARG, "%s: NULL pointer", name);
+  if (reinterpret_cast<uintptr_t>(packed) & 7) return fail(LCC_ERR_ALIGN, "%s: packed must be 8-byte aligned", name);
+  if (!aligned16(x)) return fail(LCC_ERR_ALIGN, "%s: x must be 16-byte aligned", name);
+  return launch_nvfp4_expand(packed, scale, rows, D, x, static_cast<cudaStream_t>(stream));
+}
+
+size_t lcc_fp4_index_topk_workspace(int B, int Tq, int HI, int DI, int Ncap, int k) {
+  return fp4_ws(B, Tq, HI, DI, Ncap, k).total;
+}
+
+lcc_status lcc_fp4_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int HI, int DI,
+                              const int64_t* q_pos0, const uint8_t* kI, const uint8_t* kI_scale,
+                              const int32_t* n_valid, int Ncap, int m, int k, int32_t* idx, float* score,
+                              void* workspace, size_t workspace_bytes, void* stream) {
+  const char* name = "lcc_fp4_index_topk";
+  if (B < 0 || Tq < 0) return fail(LCC_ERR_SHAPE, "%s: B=%d Tq=%d must be >= 0", name, B, Tq);
+  if (B == 0 || Tq == 0) return LCC_OK;
+  lcc_status st =
+      check_index_args(name, qI, w, B, Tq, HI, DI, q_pos0, LCC_KEY_NVFP4, kI, kI_scale, n_valid, Ncap, m, idx);
+  if (st != LCC_OK) return st;
+  if (k < 1 || k > 1024) return fail(LCC_ERR_SHAPE, "%s: k=%d (supported: 1..1024)", name, k);
+  if (reinterpret_cast<uintptr_t>(kI) & 7) return fail(LCC_ERR_ALIGN, "%s: kI must be 8-byte aligned", name);
+  const Fp4Ws ws = fp4_ws(B, Tq, HI, DI, Ncap, k);
+  if (!workspace || workspace_bytes < ws.total)
+    return fail(LCC_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", name, workspace_bytes, ws.total);
+  if (!aligned16(workspace)) return fail(LCC_ERR_ALIGN, "%s: workspace must be 16-byte aligned", name);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  lcc_bf16* qd = reinterpret_cast<lcc_bf16*>(base);
+  const int64_t qrows = static_cast<int64_t>(B) * Tq * HI;
+  if ((st = launch_nvfp4_quant(qI, qrows, DI, DI, nullptr, nullptr, qd, s)) != LCC_OK) return st;
+  if (ws.keys) {
+    // prefill shapes: keys expanded once per call, then the fused indexer + top-k
+    lcc_bf16* kd = reinterpret_cast<lcc_bf16*>(base + ws.q);
+    if ((st = launch_nvfp4_expand(kI, kI_scale, static_cast<int64_t>(B) * Ncap, DI, kd, s)) != LCC_OK) return st;
+    return run_index_topk(qd, w, B, Tq, HI, DI, q_pos0, LCC_KEY_BF16, kd, nullptr, n_valid, Ncap, m, k, idx, score,
+                          nullptr, Tq, s);
+  }
+  return run_index_topk(qd, w, B, Tq, HI, DI, q_pos0, LCC_KEY_NVFP4, kI, kI_scale, n_valid, Ncap, m, k, idx, score,
+                        base + ws.q, index_chunk(B, Tq, Ncap), s);
+}
+
+}  // extern "C"
+

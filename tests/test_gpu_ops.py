@@ -239,6 +239,100 @@ def test_index_topk_scores_output():
 
 
 # ---------------------------------------------------------------------------
+# NVFP4 quantiser and the FP4 indexer
+# ---------------------------------------------------------------------------
+def _nvfp4_quant_rows():
+    """Groups of 16 that cover every finite bf16 value, every e4m3 scale with
+    elements on and beside each e2m1 rounding midpoint, and random rows."""
+    every = np.arange(65536, dtype=np.uint16)
+    every = every[((every >> 7) & 0xFF) != 0xFF]                 # finite values only
+    v = oracle.bf16_to_f64(every)
+    groups = list(v[np.argsort(np.abs(v), kind="stable")].reshape(-1, 16))
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    for c in range(1, 127):
+        s = float(oracle.e4m3_value(c))
+        vals = []
+        for mu in mids:
+            b = int(oracle.f64_to_bf16_bits(np.array([mu * s]))[0])
+            vals += [mu * s, float(oracle.bf16_to_f64(np.array([b + 1]))[0]),
+                     float(oracle.bf16_to_f64(np.array([b - 1]))[0])]
+        vals += [-mu * s for mu in mids]
+        groups.append(np.array([6.0 * s] + vals[:15]))
+        groups.append(np.array([-6.0 * s] + vals[15:] + [0.0] * (30 - len(vals))))
+    x = np.stack(groups).reshape(-1, 64)
+    r = np.random.default_rng(31)
+    rnd = r.standard_normal((256, 64)) * np.exp(r.uniform(-8, 8, size=(256, 1)))
+    x = np.concatenate([x, oracle.round_bf16(rnd)])
+    assert np.array_equal(oracle.round_bf16(x), x)
+    return x
+
+
+def test_nvfp4_quantize_bit_exact():
+    x = _nvfp4_quant_rows()
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    packed, scale, xq = lcc.nvfp4_quantize(xt.to(DEV))
+    torch.cuda.synchronize()
+    want_p, want_s = oracle.nvfp4_quantize(x)
+    assert np.array_equal(scale.cpu().numpy(), want_s)
+    assert np.array_equal(packed.cpu().numpy(), want_p)
+    want_xq = torch.from_numpy(oracle.nvfp4_decode(want_p, want_s)).to(torch.bfloat16)
+    assert np.array_equal(bits(xq), bits(want_xq))
+    # strided rows (ld = 96 elements), and the dequantiser on the codes
+    big = torch.zeros((x.shape[0], 96), dtype=torch.bfloat16)
+    big[:, :64] = xt
+    p2, s2, _ = lcc.nvfp4_quantize(big.to(DEV)[:, :64])
+    back = lcc.nvfp4_dequantize(p2, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(p2.cpu(), packed.cpu()) and torch.equal(s2.cpu(), scale.cpu())
+    assert np.array_equal(bits(back), bits(want_xq))
+
+
+def test_nvfp4_dequantize_every_code_and_scale():
+    codes = np.arange(256, dtype=np.uint8)
+    scales = np.array([c for c in range(255) if c != 0x7F], dtype=np.uint8)    # not NaN
+    packed = np.tile(codes, (scales.size, 1)).reshape(-1, 8)                   # 32 groups per scale
+    sc = np.repeat(scales, 32)[:, None]
+    out = lcc.nvfp4_dequantize(torch.from_numpy(packed).to(DEV), torch.from_numpy(sc).to(DEV))
+    torch.cuda.synchronize()
+    want = torch.from_numpy(oracle.nvfp4_decode(packed, sc)).to(torch.bfloat16)
+    assert np.array_equal(bits(out), bits(want))
+
+
+@pytest.mark.parametrize("B,Tq,Ncap,k,nv", [(2, 150, 3000, 64, [3000, 1700]),     # prefill: fused top-k
+                                            (3, 1, 20000, 128, [20000, 9000, 77])])  # decode: NVFP4-key indexer
+def test_fp4_index_topk_parity(B, Tq, Ncap, k, nv):
+    seed, HI, DI, m = 41 + Tq, 8, 64, 4
+    qI = datagen.normal_bf16(seed, 5, (B, Tq, HI, DI))
+    w = datagen.uniform_f32(seed, 6, (B, Tq, HI))
+    kp, ks = datagen.nvfp4_normal(seed, 7, B * Ncap, DI)
+    kp, ks = kp.reshape(B, Ncap, DI // 2), ks.reshape(B, Ncap, DI // 16)
+    pos0 = [m * Ncap - Tq] * B
+    sc = torch.empty((B, Tq, k), dtype=torch.float32, device=DEV)
+    idx = lcc.fp4_index_topk(qI.to(DEV), w.to(DEV), torch.tensor(pos0, device=DEV), kp.to(DEV), ks.to(DEV),
+                             torch.tensor(nv, dtype=torch.int32, device=DEV), m, k, score=sc)
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    g, gs = idx.cpu().numpy(), sc.cpu().numpy()
+    near, moved = 0, 0
+    for b in range(B):
+        rows = []
+        for i in range(Tq):
+            n = oracle.visible_count(pos0[b] + i, m, nv[b])
+            s = oracle.index_scores_fp4(f64(qI[b, i]), f64(w[b, i]), kp[b, :n].numpy(), ks[b, :n].numpy())
+            oi, kth = oracle.topk_select(s, k)
+            rows.append(dict(idx=oi, scores=s, kth=kth))
+            sel = g[b, i][g[b, i] >= 0]
+            np.testing.assert_allclose(gs[b, i, :sel.size], s[sel], rtol=1e-5, atol=1e-5 * np.abs(s).max())
+            # the query really was quantised: bf16-query scores differ
+            plain = oracle.index_scores(f64(qI[b, i]), f64(w[b, i]), oracle.nvfp4_decode(kp[b, :n].numpy(),
+                                                                                           ks[b, :n].numpy()))
+            moved += int(np.abs(plain[sel] - s[sel]).max() > 1e-3 * np.abs(s).max())
+        near += check_topk_rows(g[b], rows, k, what=f"batch {b}")
+    assert near <= max(1, B * Tq // 100)
+    assert moved == B * Tq
+
+
+# ---------------------------------------------------------------------------
 # attention branches
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("H,D,k", [(64, 128, 128), (8, 64, 16), (16, 128, 40), (128, 64, 70)])
