@@ -278,7 +278,7 @@ lcc_status lcc_lightning_index_topk_noalloc(const lcc_bf16* qI, const float* w,
                                             int32_t* idx, float* score, void* stream);
 
 /* ---------------------------------------------------------------------- *
- * NVFP4 quantisation ([HYBRID]: the lightning indexer runs in FP4; [V41]:
+ * NVFP4 quantisation ([HYBRID]: the lightning indexer computes in FP4; [V41]:
  * the global KV cache is kept in FP4).  Row layout as the NVFP4 indexer keys:
  * e2m1 codes, element 2c in the low nibble of byte c, one e4m3 scale per 16
  * consecutive elements.  Each group of 16 is quantised as
@@ -305,7 +305,7 @@ lcc_status lcc_nvfp4_dequantize(const uint8_t* packed, const uint8_t* scale, int
                                 lcc_bf16* x, void* stream);
 
 /* The lightning indexer in FP4 ([HYBRID], section "두 가지 압축 전략: CSA 및
- * HCA": the indexer runs in FP4).  As lcc_lightning_index_topk with NVFP4
+ * HCA": the indexer computes in FP4).  As lcc_lightning_index_topk with NVFP4
  * keys, but the indexer query is first quantised to NVFP4 by
  * lcc_nvfp4_quantize's rule (per (query, head) row, groups of 16): the score
  * of entry j is

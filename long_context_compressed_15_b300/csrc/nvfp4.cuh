@@ -1,6 +1,6 @@
 // NVFP4 for the indexer: quantisation of the indexer query and expansion of
 // NVFP4 rows to bf16.  Source: "DeepSeek-V4가 이차적 어텐션 비용 없이 ...",
-// section "두 가지 압축 전략: CSA 및 HCA" (the lightning indexer runs in FP4),
+// section "두 가지 압축 전략: CSA 및 HCA" (the lightning indexer computes in FP4),
 // and the DeepSeek V4.1 Flash post (the global KV cache kept in FP4).
 //
 // NVFP4 row layout: e2m1 codes, element 2i in the low nibble of byte i, and

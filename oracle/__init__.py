@@ -59,7 +59,7 @@ Readings where the pages are silent:
      query and weights against the same indexer keys, and attends to its
      top-k among them; a reuse layer attends to the entries the layer before
      it selected; each layer attends to its own compressed cache;
-  R16 the indexer "runs in FP4": its query is quantised to NVFP4 by R7's
+  R16 the indexer computes in FP4: its query is quantised to NVFP4 by R7's
      rule (per group of 16: scale = e4m3 nearest to amax/6, elements = e2m1
      nearest to x/scale, ties to even, saturating) and its keys are NVFP4;
      the head weights stay fp32.

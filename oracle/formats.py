@@ -4,7 +4,7 @@ bf16: 1 sign, 8 exponent (bias 127), 7 mantissa bits -- the top half of an
 IEEE binary32.  e4m3 (OCP FP8 "E4M3FN"): bias 7, subnormals, no infinities,
 S.1111.111 is NaN.  e2m1 (OCP FP4): bias 1, one mantissa bit, no NaN/inf.
 NVFP4 stores e2m1 values with one e4m3 scale per 16 consecutive elements; the
-pages say the indexer "runs in FP4" ([HYBRID]) and that the global KV cache is
+pages put the indexer's arithmetic in FP4 ([HYBRID]) and that the global KV cache is
 kept in FP4 ([V41]).
 """
 import numpy as np
@@ -75,7 +75,7 @@ def nvfp4_decode(packed, scale) -> np.ndarray:
 
 # ---------------------------------------------------------------------------
 # NVFP4 quantisation of the indexer query ([HYBRID]: the lightning indexer
-# runs in FP4; reading R16)
+# computes in FP4; reading R16)
 # ---------------------------------------------------------------------------
 E2M1_MAGNITUDES = e2m1_value(np.arange(8))      # codes 0..7: 0, .5, 1, 1.5, 2, 3, 4, 6
 E4M3_NONNEGATIVE = e4m3_value(np.arange(127))   # codes 0..126: 0 .. 448 (127 is NaN)

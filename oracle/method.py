@@ -78,7 +78,7 @@ def index_scores(qI, w, kI) -> np.ndarray:
 def index_scores_fp4(qI, w, kI_packed, kI_scale) -> np.ndarray:
     """Indexer score with the indexer in FP4.
 
-    [HYBRID]: the lightning indexer runs in FP4; [V41]: the keys it reads are
+    [HYBRID]: the lightning indexer computes in FP4; [V41]: the keys it reads are
     kept in FP4.  Reading R16: the query is quantised to NVFP4 (per (head)
     row, groups of 16, nvfp4_quantize) and the keys are NVFP4 (R7); the score
     is R3's on the decoded values.
