@@ -119,9 +119,12 @@ __device__ __forceinline__ int warp_compact_t(uint32_t* keys, int32_t* ids, int 
 // and sets m_out; falls back to the exact cut when the bins do not separate
 // (many equal keys) and the buffer would stay fuller than `room_left`.
 // hist: 256 words of shared memory private to the warp.
+// With kp > 0 it also sets *p_out to a key that at least kp kept keys reach
+// (the smallest kept key of the highest bins holding kp keys; the k-th key
+// after an exact cut).
 template <int CAPQ>
 __device__ __forceinline__ int warp_cut(uint32_t* keys, int32_t* ids, int n, int k, int max_keep, uint32_t* hist,
-                                        uint32_t& m_out) {
+                                        uint32_t& m_out, int kp = 0, uint32_t* p_out = nullptr) {
   constexpr int V = CAPQ / 32;
   const int lane = threadIdx.x & 31;
   uint32_t v[V];
@@ -162,39 +165,45 @@ __device__ __forceinline__ int warp_cut(uint32_t* keys, int32_t* ids, int n, int
     if (lane + o < 32) above += y;
   }
   uint32_t run = above - t;
-  int bstar = -1;
+  int bstar = -1, bp = -1;
   uint32_t keep_n = 0;
 #pragma unroll
   for (int j = 7; j >= 0; --j) {
     if (bstar < 0 && run + h[j] >= static_cast<uint32_t>(k)) { bstar = lane * 8 + j; keep_n = run + h[j]; }
+    if (bp < 0 && run + h[j] >= static_cast<uint32_t>(kp)) bp = lane * 8 + j;
     run += h[j];
   }
   int best = __reduce_max_sync(0xffffffffu, bstar);
+  const int bestp = kp > 0 ? __reduce_max_sync(0xffffffffu, bp) : 256;
   const uint32_t kept = __shfl_sync(0xffffffffu, keep_n, __ffs(__ballot_sync(0xffffffffu, bstar == best)) - 1);
   __syncwarp();  // everyone has read the histogram before the next use
   if (best < 0 || static_cast<int>(kept) > max_keep) {
     uint32_t T = 0u;
     const int r = warp_compact_t<CAPQ>(keys, ids, n, k, T);
     m_out = T;
+    if (kp > 0) *p_out = T;
     return r;
   }
   int out = 0;
-  uint32_t mk = 0xFFFFFFFFu;
+  uint32_t mk = 0xFFFFFFFFu, mp = 0xFFFFFFFFu;
 #pragma unroll
   for (int i = 0; i < V; ++i) {
     const int e = lane + 32 * i;
-    const bool keep = e < n && static_cast<int>((bins[i / 4] >> (8 * (i % 4))) & 255u) >= best;
+    const int bn = static_cast<int>((bins[i / 4] >> (8 * (i % 4))) & 255u);
+    const bool keep = e < n && bn >= best;
     const unsigned m = __ballot_sync(0xffffffffu, keep);
     if (keep) {
       const int p = out + __popc(m & ((1u << lane) - 1u));
       keys[p] = v[i];
       ids[p] = id[i];
       mk = min(mk, v[i]);
+      if (bn >= bestp) mp = min(mp, v[i]);
     }
     out += __popc(m);
   }
   __syncwarp();
   m_out = __reduce_min_sync(0xffffffffu, mk);
+  if (kp > 0) *p_out = __reduce_min_sync(0xffffffffu, mp);
   return out;
 }
 
@@ -510,7 +519,8 @@ struct IndexTopkPwCfg {
   static constexpr int OFF_IDS = OFF_KEYS + NB * CAPB * 4;
   static constexpr int OFF_CNT = OFF_IDS + NB * CAPB * 4;   // final count of every buffer
   static constexpr int OFF_HIST = OFF_CNT + NB * 4;         // 256 words per epilogue warp
-  static constexpr int SMEM = OFF_HIST + EW * 256 * 4 + 1024;
+  static constexpr int OFF_PUB = OFF_HIST + EW * 256 * 4;   // published bound of every buffer
+  static constexpr int SMEM = OFF_PUB + NB * 4 + 1024;
 };
 
 template <int HI, int DI, int NQ, int STAGES>
@@ -547,6 +557,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
   int32_t* sIds = reinterpret_cast<int32_t*>(smem + X::OFF_IDS);      // [NQ][4][CAPB]
   int* sCnt = reinterpret_cast<int*>(smem + X::OFF_CNT);              // [NQ][4]
   uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + X::OFF_HIST);  // [EW][256]
+  uint32_t* sPub = reinterpret_cast<uint32_t*>(smem + X::OFF_PUB);    // [NQ][4], 0 = none yet
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.z;
@@ -597,6 +608,7 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       const int qq = qg0 + u;
       sVis[u] = qq < qend ? visible_entries(pos0 + qq, a.m, nval, a.Ncap) : 0;
     }
+    for (int u = t; u < X::NB; u += NEPI) sPub[u] = 0u;
     tc::fence_proxy_async_smem();
   }
   tc::tc_fence_before();
@@ -658,8 +670,27 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       cnt[j] = 0;
     }
     auto buf = [&](int j) { return ((grpq * QG + j) * 4 + quarter) * CAPB; };
+    // A second filter shared by the four quadrant warps of a query: at every
+    // cut a warp publishes a key that at least ceil(k/4) entries of its
+    // buffer reach; the four quadrants together then hold at least k entries
+    // at or above the smallest published key, so no entry below it can enter
+    // the query's top-k (entries equal to it may, by the index rule, and
+    // pass).  It is read at cuts and every 8 tiles; a stale read only gives
+    // an older, smaller bound.
+    const int kp = (k + 3) / 4;
+    auto shared_bound = [&](int j) -> float {
+      const volatile uint32_t* P = sPub + (grpq * QG + j) * 4;
+      const uint32_t m4 = min(min(P[0], P[1]), min(P[2], P[3]));
+      if (m4 <= 1u) return -INFINITY;
+      const uint32_t below = m4 - 1u == 0x7FFFFFFFu ? 0x7FFFFFFEu : m4 - 1u;  // skip -0 below +0
+      return key_to_f32(below);  // the largest float below the bound: s > it <=> s >= bound
+    };
     for (int t = 0; t < ntiles; ++t) {
       const int acc = t % NACC;
+      if ((t & 7) == 7) {
+#pragma unroll
+        for (int j = 0; j < QG; ++j) thf[j] = fmaxf(thf[j], shared_bound(j));
+      }
       const bool wok = __all_sync(0xffffffffu, !*s_abort && tc::mbar_wait(tfull + acc, (t / NACC) & 1, 26));
       if (!wok) {
         *s_abort = 1;
@@ -713,9 +744,11 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
             cnt[j] += __popc(msk);
             if (cnt[j] > CAPB - 32) {  // the next tile could overflow: cut to a superset of the top-k
               __syncwarp();
-              uint32_t th;
-              cnt[j] = ftk::warp_cut<CAPB>(sKeys + bo, sIds + bo, cnt[j], k, CAPB - 32, sHist + ew * 256, th);
-              thf[j] = key_to_f32(th);
+              uint32_t th, pb;
+              cnt[j] = ftk::warp_cut<CAPB>(sKeys + bo, sIds + bo, cnt[j], k, CAPB - 32, sHist + ew * 256, th, kp,
+                                           &pb);
+              if (lane == 0) reinterpret_cast<volatile uint32_t*>(sPub)[bo / CAPB] = pb;
+              thf[j] = fmaxf(key_to_f32(th), shared_bound(j));
             }
           }
         }
