@@ -207,6 +207,273 @@ __device__ __forceinline__ int warp_cut(uint32_t* keys, int32_t* ids, int n, int
   return out;
 }
 
+
+// Highest bin b of a 256-bin histogram (hist, shared memory, 8 bins per
+// lane) such that the bins >= b hold at least `need` keys; -1 if none.
+__device__ __forceinline__ int hist_top_bin(const uint32_t* hist, int need) {
+  const int lane = threadIdx.x & 31;
+  uint32_t h[8], t = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) { h[j] = hist[lane * 8 + j]; t += h[j]; }
+  uint32_t above = t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, above, o);
+    if (lane + o < 32) above += y;
+  }
+  uint32_t run = above - t;
+  int bstar = -1;
+#pragma unroll
+  for (int j = 7; j >= 0; --j) {
+    if (bstar < 0 && run + h[j] >= static_cast<uint32_t>(need)) bstar = lane * 8 + j;
+    run += h[j];
+  }
+  return __reduce_max_sync(0xffffffffu, bstar);
+}
+
+// Exact top-k (key desc, index asc) of the union of four candidate lists
+// that are each in ascending index order (lists r at keys + r*CAPB, counts
+// cnt4[r]), written to oi / os in ascending index order and padded with -1
+// / -inf up to k.  One warp.  P is a key that the union's k-th largest key
+// reaches (0 = none): entries below it are dropped first.  When at most CAPB
+// entries remain, they are gathered into one list and selected once (the
+// bitwise select starts at the highest bit in which the remaining keys
+// differ), and each kept entry finds its output slot by binary searches in
+// the other lists.  More than CAPB are first cut to the keys of the highest
+// bins of a 256-bin histogram spread linearly over their key range that hold
+// at least k of them (a superset of the top-k, in list order); if that still
+// leaves more than CAPB (many equal keys), every list is cut to its own top-k
+// and the lists are merged one after the other.  The lists' storage is
+// overwritten; hist: 256 words of shared memory private to the warp.
+template <int CAPB>
+__device__ __forceinline__ void union_topk_out(uint32_t* keys, int32_t* ids, const int* cnt4, uint32_t P, int k,
+                                               uint32_t* hist, int32_t* oi, float* os) {
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+  int c[4];
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {  // drop the entries below P (stable, in place)
+    uint32_t* kr = keys + r * CAPB;
+    int32_t* ir = ids + r * CAPB;
+    const int n = cnt4[r];
+    int out = 0;
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int e = e0 + lane;
+      uint32_t kv = 0u;
+      int32_t iv = 0;
+      if (e < n) { kv = kr[e]; iv = ir[e]; }
+      const bool keep = e < n && kv >= P;
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      __syncwarp();
+      if (keep) { kr[out + __popc(m & below)] = kv; ir[out + __popc(m & below)] = iv; }
+      out += __popc(m);
+    }
+    c[r] = out;
+  }
+  __syncwarp();
+  int ntot = c[0] + c[1] + c[2] + c[3];
+  if (ntot > CAPB) {
+    uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      for (int e = lane; e < c[r]; e += 32) {
+        const uint32_t kv = keys[r * CAPB + e];
+        lo = min(lo, kv);
+        hi = max(hi, kv);
+      }
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+    __syncwarp();
+    const float inv = 256.f / (static_cast<float>(hi - lo) + 1.f);
+    auto bin = [&](uint32_t kv) { return min(255u, static_cast<uint32_t>(static_cast<float>(kv - lo) * inv)); };
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      for (int e = lane; e < c[r]; e += 32) atomicAdd(hist + bin(keys[r * CAPB + e]), 1u);
+    __syncwarp();
+    const int best = hist_top_bin(hist, k);
+    __syncwarp();
+    if (best >= 0) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {  // keep the bins >= best (stable, in place)
+        uint32_t* kr = keys + r * CAPB;
+        int32_t* ir = ids + r * CAPB;
+        const int n = c[r];
+        int out = 0;
+        for (int e0 = 0; e0 < n; e0 += 32) {
+          const int e = e0 + lane;
+          uint32_t kv = 0u;
+          int32_t iv = 0;
+          if (e < n) { kv = kr[e]; iv = ir[e]; }
+          const bool keep = e < n && static_cast<int>(bin(kv)) >= best;
+          const unsigned m = __ballot_sync(0xffffffffu, keep);
+          __syncwarp();
+          if (keep) { kr[out + __popc(m & below)] = kv; ir[out + __popc(m & below)] = iv; }
+          out += __popc(m);
+        }
+        c[r] = out;
+      }
+      __syncwarp();
+      ntot = c[0] + c[1] + c[2] + c[3];
+    }
+  }
+  if (ntot > CAPB) {
+    // many equal keys: each list down to its own top-k, then merged in turn
+    int n = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t T;
+      const int cr = warp_compact_t<CAPB>(keys + r * CAPB, ids + r * CAPB, c[r], k, T);
+      if (r == 0) { n = cr; continue; }
+      for (int e0 = 0; e0 < cr; e0 += 32) {  // behind the running top-k (forward copy)
+        const int e = e0 + lane;
+        uint32_t kv = 0u;
+        int32_t iv = 0;
+        if (e < cr) { kv = keys[r * CAPB + e]; iv = ids[r * CAPB + e]; }
+        __syncwarp();
+        if (e < cr) { keys[n + e] = kv; ids[n + e] = iv; }
+        __syncwarp();
+      }
+      n = warp_compact_t<2 * CAPB>(keys, ids, n + cr, k, T);
+      __syncwarp();
+    }
+    for (int o = lane; o < k; o += 32) {
+      if (o < n) {
+        const int32_t me = ids[o];
+        int p = 0;
+        for (int d = 0; d < n; ++d) p += ids[d] < me;
+        oi[p] = me;
+        if (os) os[p] = key_to_f32(keys[o]);
+      } else {
+        oi[o] = -1;
+        if (os) os[o] = -INFINITY;
+      }
+    }
+    return;
+  }
+  // gather the lists behind list 0 (the destination stays below CAPB, under
+  // every later list's storage)
+  int b[5];
+  b[0] = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) b[r + 1] = b[r] + c[r];
+#pragma unroll
+  for (int r = 1; r < 4; ++r)
+    for (int e = lane; e < c[r]; e += 32) { keys[b[r] + e] = keys[r * CAPB + e]; ids[b[r] + e] = ids[r * CAPB + e]; }
+  __syncwarp();
+  constexpr int V = CAPB / 32;
+  uint32_t v[V];
+  int32_t id[V];
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < ntot ? keys[e] : 0u;
+    id[i] = e < ntot ? ids[e] : 0x7FFFFFFF;
+    if (e < ntot) { lo = min(lo, v[i]); hi = max(hi, v[i]); }
+  }
+  unsigned km[V];  // ballot of the kept entries of each register slot
+  if (ntot > k) {
+    lo = __reduce_min_sync(0xffffffffu, lo);
+    hi = __reduce_max_sync(0xffffffffu, hi);
+    // k-th largest key: bits above the highest one in which lo and hi differ
+    // are common to every candidate
+    uint32_t T = hi;
+    if (lo != hi) {
+      const int top = 31 - __clz(lo ^ hi);
+      uint32_t prefix = top == 31 ? 0u : hi & ~((2u << top) - 1u);
+      int need = k;
+      for (int bit = top; bit >= 0; --bit) {
+        const uint32_t hm = ~((2u << bit) - 1u);  // bits above `bit` (bit 31: none)
+        const uint32_t hmask = bit == 31 ? 0u : hm;
+        int cc = 0;
+#pragma unroll
+        for (int i = 0; i < V; ++i) cc += ((v[i] & hmask) == prefix) && ((v[i] >> bit) & 1u);
+        cc = __reduce_add_sync(0xffffffffu, cc);
+        if (cc >= need) prefix |= 1u << bit;
+        else need -= cc;
+      }
+      T = prefix;
+    }
+    int gt = 0, eq = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) { gt += v[i] > T; eq += v[i] == T; }
+    gt = __reduce_add_sync(0xffffffffu, gt);
+    eq = __reduce_add_sync(0xffffffffu, eq);
+    const int need_eq = k - gt;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      bool keep = v[i] > T;
+      if (v[i] == T) {
+        if (eq == need_eq) {
+          keep = true;
+        } else {  // only with exactly equal scores: the lowest indices among them
+          int before = 0;
+          for (int e2 = 0; e2 < ntot; ++e2) before += (keys[e2] == T) && (ids[e2] < id[i]);
+          keep = before < need_eq;
+        }
+      }
+      km[i] = __ballot_sync(0xffffffffu, keep);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) km[i] = __ballot_sync(0xffffffffu, lane + 32 * i < ntot);
+  }
+  // kept entries, in list order, to the front; kb[r] = first kept of list r
+  int kb[5];
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int lim = min(max(b[r] - 32 * i, 0), 32);
+      cnt += __popc(km[i] & (lim == 32 ? 0xffffffffu : (1u << lim) - 1u));
+    }
+    kb[r] = cnt;
+  }
+  __syncwarp();  // every lane holds its entries before they are overwritten
+  {
+    int out = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      if ((km[i] >> lane) & 1u) {
+        const int p = out + __popc(km[i] & below);
+        keys[p] = v[i];
+        ids[p] = id[i];
+      }
+      out += __popc(km[i]);
+    }
+  }
+  __syncwarp();
+  const int nk = kb[4];
+  for (int p = lane; p < nk; p += 32) {
+    const int32_t me = ids[p];
+    int rank = 0;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int s0 = kb[r], s1 = kb[r + 1];
+      if (p >= s0 && p < s1) {
+        rank += p - s0;  // its own list is in index order
+      } else {           // entries of list r with a lower index: binary search
+        int lo2 = s0, hi2 = s1;
+        while (lo2 < hi2) {
+          const int mid = (lo2 + hi2) >> 1;
+          if (ids[mid] < me) lo2 = mid + 1;
+          else hi2 = mid;
+        }
+        rank += lo2 - s0;
+      }
+    }
+    oi[rank] = me;
+    if (os) os[rank] = key_to_f32(keys[p]);
+  }
+  for (int o = nk + lane; o < k; o += 32) {
+    oi[o] = -1;
+    if (os) os[o] = -INFINITY;
+  }
+}
+
 }  // namespace ftk
 
 struct IndexTopkTcArgs {
@@ -755,54 +1022,21 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       }
     }
 #pragma unroll
-    for (int j = 0; j < QG; ++j) {  // every buffer down to at most k before the merge
-      const int bo = buf(j);
-      __syncwarp();
-      uint32_t T;
-      const int n = *s_abort ? 0 : ftk::warp_compact_t<CAPB>(sKeys + bo, sIds + bo, cnt[j], k, T);
-      if (lane == 0) sCnt[bo / CAPB] = n;
-    }
+    for (int j = 0; j < QG; ++j)
+      if (lane == 0) sCnt[buf(j) / CAPB] = cnt[j];
     tc::named_sync(1, NEPI);
     // ---- final: exact top-k of every query over its four buffers, ascending index order ----
     for (int qi = ew; qi < NQ; qi += EW) {
       const int q = qg0 + qi;
       if (q >= qend) continue;
-      uint32_t* kq = sKeys + qi * 4 * CAPB;
-      int32_t* iq = sIds + qi * 4 * CAPB;
-      int n = sCnt[qi * 4];
-      for (int qd = 1; qd < 4; ++qd) {
-        // append list qd behind the running top-k (forward copy: the destination
-        // starts at most k <= CAPB - 32 slots in, below the source), then keep
-        // the top-k of the union
-        const int c = sCnt[qi * 4 + qd];
-        for (int e0 = 0; e0 < c; e0 += 32) {
-          const int e = e0 + lane;
-          uint32_t kv = 0u;
-          int32_t iv = 0;
-          if (e < c) { kv = kq[qd * CAPB + e]; iv = iq[qd * CAPB + e]; }
-          __syncwarp();
-          if (e < c) { kq[n + e] = kv; iq[n + e] = iv; }
-          __syncwarp();
-        }
-        uint32_t T;
-        n = ftk::warp_compact_t<2 * CAPB>(kq, iq, n + c, k, T);
-        __syncwarp();
-      }
-      if (*s_abort) n = 0;
-      int32_t* oi = a.idx + (static_cast<int64_t>(b) * a.Tq + q) * k;
-      float* os = a.score ? a.score + (static_cast<int64_t>(b) * a.Tq + q) * k : nullptr;
-      for (int c = lane; c < k; c += 32) {
-        if (c < n) {
-          const int32_t me = iq[c];
-          int p = 0;
-          for (int d = 0; d < n; ++d) p += iq[d] < me;
-          oi[p] = me;
-          if (os) os[p] = key_to_f32(kq[c]);
-        } else {
-          oi[c] = -1;
-          if (os) os[c] = -INFINITY;
-        }
-      }
+      const volatile uint32_t* Pq = sPub + qi * 4;
+      const uint32_t P = min(min(Pq[0], Pq[1]), min(Pq[2], Pq[3]));
+      int c4[4];  // an abandoned run (a wait that gave up) writes padding only
+#pragma unroll
+      for (int r = 0; r < 4; ++r) c4[r] = *s_abort ? 0 : sCnt[qi * 4 + r];
+      ftk::union_topk_out<CAPB>(sKeys + qi * 4 * CAPB, sIds + qi * 4 * CAPB, c4, P, k, sHist + ew * 256,
+                                a.idx + (static_cast<int64_t>(b) * a.Tq + q) * k,
+                                a.score ? a.score + (static_cast<int64_t>(b) * a.Tq + q) * k : nullptr);
     }
   }
   tc::tc_fence_before();
