@@ -981,15 +981,19 @@ __global__ void __launch_bounds__(IndexTopkPwCfg<HI, DI, NQ, STAGES>::NT, 1)
       unsigned anyq = 0u;  // bit j: this lane's entry passes query j's threshold
 #pragma unroll
       for (int j = 0; j < QG; ++j) {
-        float s0 = 0.f, s1 = 0.f;
+        // two fp32 chains (even and odd heads) in one packed register pair:
+        // each half is an IEEE fma, in the order of the scalar code
+        uint64_t s01 = 0ull;
 #pragma unroll
         for (int h4 = 0; h4 < HI / 4; ++h4) {
           const float4 wv = sW4[j * HI / 4 + h4];
-          s0 = fmaf(wv.x, fmaxf(v[j * HI + 4 * h4 + 0], 0.f), s0);
-          s1 = fmaf(wv.y, fmaxf(v[j * HI + 4 * h4 + 1], 0.f), s1);
-          s0 = fmaf(wv.z, fmaxf(v[j * HI + 4 * h4 + 2], 0.f), s0);
-          s1 = fmaf(wv.w, fmaxf(v[j * HI + 4 * h4 + 3], 0.f), s1);
+          s01 = fma_f32x2(pack_f32x2(wv.x, wv.y),
+                          pack_f32x2(fmaxf(v[j * HI + 4 * h4 + 0], 0.f), fmaxf(v[j * HI + 4 * h4 + 1], 0.f)), s01);
+          s01 = fma_f32x2(pack_f32x2(wv.z, wv.w),
+                          pack_f32x2(fmaxf(v[j * HI + 4 * h4 + 2], 0.f), fmaxf(v[j * HI + 4 * h4 + 3], 0.f)), s01);
         }
+        float s0, s1;
+        unpack_f32x2(s01, s0, s1);
         const float s = s0 + s1;
         sc[j] = (all_vis || entry < visr[j]) ? s : -INFINITY;
         anyq |= (sc[j] > thf[j] ? 1u : 0u) << j;
