@@ -231,6 +231,44 @@ __device__ __forceinline__ int hist_top_bin(const uint32_t* hist, int need) {
   return __reduce_max_sync(0xffffffffu, bstar);
 }
 
+// Output of a kept set stored as four runs [kb[r], kb[r+1]) that are each in
+// ascending index order: the entry at p goes to slot sum_r #{entries of run r
+// with a lower index} (its own run contributes p - kb[r]), found by
+// fixed-step binary searches (runs shorter than 256), two entries per lane in
+// flight; slots kb[4] .. k-1 get -1 / -inf.
+template <int CAPB>
+__device__ __forceinline__ void runs_out(const uint32_t* keys, const int32_t* ids, const int (&kb)[5], int k,
+                                         int32_t* oi, float* os) {
+  static_assert(CAPB <= 256, "runs shorter than 256");
+  const int lane = threadIdx.x & 31;
+  const int nk = kb[4];
+  for (int p0 = 0; p0 < nk; p0 += 64) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int p = p0 + 32 * h + lane;
+      if (p < nk) {
+        const int32_t me = ids[p];
+        int rank = 0;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int s0 = kb[r], s1 = kb[r + 1];
+          int pos = s0;
+#pragma unroll
+          for (int step = 128; step >= 1; step >>= 1)
+            if (pos + step <= s1 && ids[pos + step - 1] < me) pos += step;
+          rank += pos - s0;
+        }
+        oi[rank] = me;
+        if (os) os[rank] = key_to_f32(keys[p]);
+      }
+    }
+  }
+  for (int o = nk + lane; o < k; o += 32) {
+    oi[o] = -1;
+    if (os) os[o] = -INFINITY;
+  }
+}
+
 // Exact top-k (key desc, index asc) of the union of four candidate lists
 // that are each in ascending index order (lists r at keys + r*CAPB, counts
 // cnt4[r]), written to oi / os in ascending index order and padded with -1
@@ -246,8 +284,8 @@ __device__ __forceinline__ int hist_top_bin(const uint32_t* hist, int need) {
 // and the lists are merged one after the other.  The lists' storage is
 // overwritten; hist: 256 words of shared memory private to the warp.
 template <int CAPB>
-__device__ __forceinline__ void union_topk_out(uint32_t* keys, int32_t* ids, const int* cnt4, uint32_t P, int k,
-                                               uint32_t* hist, int32_t* oi, float* os) {
+__device__ __forceinline__ void union_topk_general(uint32_t* keys, int32_t* ids, const int* cnt4, uint32_t P, int k,
+                                                   uint32_t* hist, int32_t* oi, float* os) {
   const int lane = threadIdx.x & 31;
   const unsigned below = (1u << lane) - 1u;
   int c[4];
@@ -446,32 +484,169 @@ __device__ __forceinline__ void union_topk_out(uint32_t* keys, int32_t* ids, con
     }
   }
   __syncwarp();
-  const int nk = kb[4];
-  for (int p = lane; p < nk; p += 32) {
-    const int32_t me = ids[p];
-    int rank = 0;
+  runs_out<CAPB>(keys, ids, kb, k, oi, os);
+}
+
+
+// Exact top-k (key desc, index asc) of the union of four candidate lists
+// that are each in ascending index order (list r at keys + r*CAPB, count
+// cnt4[r]), written to oi / os in ascending index order and padded with -1
+// / -inf up to k.  One warp; hist: 256 words of shared memory private to the
+// warp; the lists' storage is overwritten.  P is a key that the union's k-th
+// largest key reaches (0 = none).  One read-only pass counts the entries at
+// or above P and their key range; a 256-bin histogram spread linearly over
+// that range gives the bin that holds the k-th largest key: the entries of
+// higher bins are kept, and those of that bin (at most 32 of them) are
+// ranked against each other.  The kept entries are gathered list by list,
+// so each list stays a run in index order, and every entry finds its output
+// slot by binary searches in the other runs.  A bin of more than 32 entries
+// (many nearly equal keys) takes the general path.
+template <int CAPB>
+__device__ __forceinline__ void union_topk_out(uint32_t* keys, int32_t* ids, const int* cnt4, uint32_t P, int k,
+                                               uint32_t* hist, int32_t* oi, float* os) {
+  constexpr int V = CAPB / 32;
+  const int lane = threadIdx.x & 31;
+  const unsigned below = (1u << lane) - 1u;
+  int ntot = 0;
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int s0 = kb[r], s1 = kb[r + 1];
-      if (p >= s0 && p < s1) {
-        rank += p - s0;  // its own list is in index order
-      } else {           // entries of list r with a lower index: binary search
-        int lo2 = s0, hi2 = s1;
-        while (lo2 < hi2) {
-          const int mid = (lo2 + hi2) >> 1;
-          if (ids[mid] < me) lo2 = mid + 1;
-          else hi2 = mid;
-        }
-        rank += lo2 - s0;
-      }
+  for (int r = 0; r < 4; ++r) {
+    int cnt = 0;
+    for (int e = lane; e < cnt4[r]; e += 32) {
+      const uint32_t kv = keys[r * CAPB + e];
+      if (kv >= P) { ++cnt; lo = min(lo, kv); hi = max(hi, kv); }
     }
-    oi[rank] = me;
-    if (os) os[rank] = key_to_f32(keys[p]);
+    ntot += __reduce_add_sync(0xffffffffu, cnt);
   }
-  for (int o = nk + lane; o < k; o += 32) {
-    oi[o] = -1;
-    if (os) os[o] = -INFINITY;
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  const bool all = ntot <= k;
+  const float inv = 256.f / (static_cast<float>(hi - lo) + 1.f);
+  auto bin = [&](uint32_t kv) {
+    return static_cast<int>(min(255u, static_cast<uint32_t>(static_cast<float>(kv - lo) * inv)));
+  };
+  int best = 0, A = 0, Bc = 0;
+  if (!all) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) hist[lane * 8 + j] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+      for (int e = lane; e < cnt4[r]; e += 32) {
+        const uint32_t kv = keys[r * CAPB + e];
+        if (kv >= P) atomicAdd(hist + bin(kv), 1u);
+      }
+    __syncwarp();
+    best = hist_top_bin(hist, k);
+    int a = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a += (lane * 8 + j > best) ? static_cast<int>(hist[lane * 8 + j]) : 0;
+    A = __reduce_add_sync(0xffffffffu, a);
+    Bc = best >= 0 ? static_cast<int>(hist[best]) : 0;
+    __syncwarp();
+    if (best < 0 || Bc > 32 || A + Bc > CAPB) {
+      union_topk_general<CAPB>(keys, ids, cnt4, P, k, hist, oi, os);
+      return;
+    }
   }
+  // gather the candidates (at or above P and, unless all are kept, in bins
+  // >= best), list by list; b[r] = first of list r
+  int b[5];
+  int out = 0;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const uint32_t* kr = keys + r * CAPB;
+    const int32_t* ir = ids + r * CAPB;
+    const int n = cnt4[r];
+    b[r] = out;
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int e = e0 + lane;
+      uint32_t kv = 0u;
+      int32_t iv = 0;
+      if (e < n) { kv = kr[e]; iv = ir[e]; }
+      const bool keep = e < n && kv >= P && (all || bin(kv) >= best);
+      const unsigned m = __ballot_sync(0xffffffffu, keep);
+      __syncwarp();  // list 0 is compacted in place: the chunk is read before it is overwritten
+      if (keep) { keys[out + __popc(m & below)] = kv; ids[out + __popc(m & below)] = iv; }
+      out += __popc(m);
+    }
+  }
+  b[4] = out;
+  __syncwarp();
+  uint32_t v[V];
+  int32_t id[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < out ? keys[e] : 0u;
+    id[i] = e < out ? ids[e] : 0x7FFFFFFF;
+  }
+  unsigned km[V];  // ballot of the kept entries of each register slot
+  if (!all) {
+    // the entries of bin `best` to hist[0 .. Bc) (keys) and hist[32 ..] (indices)
+    unsigned bm[V];
+    int q = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const bool isb = lane + 32 * i < out && bin(v[i]) == best;
+      bm[i] = __ballot_sync(0xffffffffu, isb);
+      if (isb) {
+        const int slot = q + __popc(bm[i] & below);
+        hist[slot] = v[i];
+        hist[32 + slot] = static_cast<uint32_t>(id[i]);
+      }
+      q += __popc(bm[i]);
+    }
+    __syncwarp();
+    const uint32_t mk = lane < Bc ? hist[lane] : 0u;
+    const int32_t mi = lane < Bc ? static_cast<int32_t>(hist[32 + lane]) : 0x7FFFFFFF;
+    int rank = 0;  // bin entries before this one (key desc, index asc)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t ok = __shfl_sync(0xffffffffu, mk, j);
+      const int32_t oj = __shfl_sync(0xffffffffu, mi, j);
+      rank += (j < Bc) && (ok > mk || (ok == mk && oj < mi));
+    }
+    const unsigned win = __ballot_sync(0xffffffffu, lane < Bc && rank < k - A);
+    q = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const bool isb = (bm[i] >> lane) & 1u;
+      const int slot = q + __popc(bm[i] & below);
+      const bool keep = lane + 32 * i < out && (!isb || ((win >> slot) & 1u));
+      km[i] = __ballot_sync(0xffffffffu, keep);
+      q += __popc(bm[i]);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < V; ++i) km[i] = __ballot_sync(0xffffffffu, lane + 32 * i < out);
+  }
+  int kb[5];
+#pragma unroll
+  for (int r = 0; r < 5; ++r) {
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      const int lim = min(max(b[r] - 32 * i, 0), 32);
+      cnt += __popc(km[i] & (lim == 32 ? 0xffffffffu : (1u << lim) - 1u));
+    }
+    kb[r] = cnt;
+  }
+  __syncwarp();  // every lane holds its entries before they are overwritten
+  {
+    int o2 = 0;
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      if ((km[i] >> lane) & 1u) {
+        const int p = o2 + __popc(km[i] & below);
+        keys[p] = v[i];
+        ids[p] = id[i];
+      }
+      o2 += __popc(km[i]);
+    }
+  }
+  __syncwarp();
+  runs_out<CAPB>(keys, ids, kb, k, oi, os);
 }
 
 }  // namespace ftk
