@@ -52,7 +52,7 @@ typedef enum {
   LCC_ERR_ARG = 1,          /* null pointer or invalid value */
   LCC_ERR_SHAPE = 2,        /* unsupported or inconsistent size */
   LCC_ERR_ALIGN = 3,        /* pointer or stride not 16-byte aligned */
-  LCC_ERR_UNSUPPORTED = 4,  /* valid request this build does not implement */
+  LCC_ERR_UNSUPPORTED = 4,  /* valid request the library does not implement */
   LCC_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
   LCC_ERR_TIMEOUT = 6,      /* a bounded device-side wait gave up */
   LCC_ERR_DEVICE = 7,       /* a kernel found invalid data (see lcc_last_error) */
