@@ -642,7 +642,7 @@ class CsaPrefillBench:
         tp = float(np.median(times))
         nbytes = c.B * (c.T * c.D * 2 * 2 + c.T * 4 + c.N * c.D * 2 * 2)  # K, V, gates in; pooled K, V out
         hbm = peaks()["hbm_gbs"]
-        d["pool"] = {"kernel": "k_pool_small<4,128,4>", "bound": "hbm", "bytes": nbytes, "launch_us": round(tp * 1e6, 3),
+        d["pool"] = {"kernel": "k_pool_small<4,128,2>", "bound": "hbm", "bytes": nbytes, "launch_us": round(tp * 1e6, 3),
                      "achieved_gbs": round(nbytes / tp / 1e9, 1), "frac": round(nbytes / tp / 1e9 / hbm, 4),
                      "timing": "one launch after an L2 flush, median of 4"}
         d["fp4_indexer"] = self.fp4_indexer(stream)

@@ -142,7 +142,7 @@ lcc_status compress_impl(int m, const lcc_bf16* K, const lcc_bf16* V, const floa
              reinterpret_cast<bf16*>(Kc), reinterpret_cast<bf16*>(Vc), c_bs, tok0, n_valid, Ncap};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (m <= 4) {
-    constexpr int NB = 4;  // blocks per (half-)warp
+    constexpr int NB = 2;  // blocks per (half-)warp
     const int bpw = 32 / (2 * (D / 8));
     const int64_t per_cta = 8LL * bpw * NB;
     const int64_t gx = (nblk + per_cta - 1) / per_cta;
