@@ -99,3 +99,24 @@ def test_workspace_sizes(lib):
     assert lcc.layer_attn_workspace(1, 4096, 64, 128, 256) == 0   # prefill layers write bf16 directly
     assert lcc.dense_attn_workspace(8, 1, 64, 128, 8192) > 0      # decode splits the key range
     assert lcc.dense_attn_workspace(1, 32768, 64, 128, 8448) == 0  # prefill needs none
+
+
+def test_nvfp4_and_fp4_indexer_host_checks(lib):
+    P = ctypes.c_void_p
+    # quantiser: D not a multiple of 16, row stride below D, misaligned input; empty work is a no-op
+    assert lib.lcc_nvfp4_quantize(P(16), 4, 24, 24, P(16), P(16), P(16), None) == 2 and "D=24" in lcc.last_error()
+    assert lib.lcc_nvfp4_quantize(P(16), 4, 64, 32, P(16), P(16), P(16), None) == 2
+    assert lib.lcc_nvfp4_quantize(P(18), 4, 64, 64, P(16), P(16), P(16), None) == 3
+    assert lib.lcc_nvfp4_quantize(None, 0, 64, 64, None, None, None, None) == 0
+    assert lib.lcc_nvfp4_dequantize(None, P(16), 4, 64, P(16), None) == 1
+    assert lib.lcc_nvfp4_dequantize(P(12), P(16), 4, 64, P(16), None) == 3
+    # the FP4 indexer takes the NVFP4 shapes (8 heads of 64) and needs its workspace
+    args = [P(16), P(16), 1, 300, 8, 64, P(16), P(16), P(16), P(16), 32768, 4, 128, P(16), None, None, 0, None]
+    assert lib.lcc_fp4_index_topk(*args) == 8 and "workspace" in lcc.last_error()
+    args[4] = 4
+    assert lib.lcc_fp4_index_topk(*args) == 2
+    # workspace: the dequantised query, plus the keys expanded to bf16 (prefill shapes) or the
+    # indexer's scratch (decode shapes)
+    assert lcc.fp4_index_topk_workspace(1, 300, 8, 64, 32768, 128) >= 300 * 8 * 64 * 2 + 32768 * 64 * 2
+    assert (lcc.fp4_index_topk_workspace(4, 1, 8, 64, 262160, 128)
+            >= 4 * 8 * 64 * 2 + lcc.index_topk_workspace(4, 1, 262160, 128))
