@@ -594,6 +594,33 @@ def test_index_topk_prefill_passes_parity(Ncap, Tq, q0, k):
     assert near <= 2
 
 
+@pytest.mark.parametrize("k", [128, 224])
+def test_index_topk_prefill_fused_signed_weights(k):
+    # head weights of both signs (scores below zero, keys on both sides of +0) and the largest k the
+    # fused kernel's warp-private buffers take; rows long enough for every buffer cut and the
+    # shared bound of the quadrant warps
+    B, Tq, HI, DI, Ncap, m = 1, 200, 8, 64, 6000, 4
+    qI = datagen.normal_bf16(33, 5, (B, Tq, HI, DI))
+    w = datagen.uniform_f32(33, 6, (B, Tq, HI)) * 2.0 - 1.0
+    kI = datagen.normal_bf16(33, 7, (B, Ncap, DI))
+    q0 = m * Ncap - Tq
+    sc = torch.empty((B, Tq, k), dtype=torch.float32, device=DEV)
+    idx = lcc.lightning_index_topk(qI.to(DEV), w.to(DEV), q0, kI.to(DEV), Ncap, m, k, score=sc)
+    torch.cuda.synchronize()
+    lcc.sync_status()
+    g, gs = idx.cpu().numpy()[0], sc.cpu().numpy()[0]
+    rows = []
+    for i in range(Tq):
+        vis = min(Ncap, (q0 + i + 1) // m)
+        s = oracle.index_scores(f64(qI[0, i]), f64(w[0, i]), f64(kI[0, :vis]))
+        oi, kth = oracle.topk_select(s, k)
+        rows.append(dict(idx=oi, scores=s, kth=kth))
+        sel = g[i][g[i] >= 0]
+        np.testing.assert_allclose(gs[i, :sel.size], s[sel], rtol=1e-5, atol=1e-5 * np.abs(s).max())
+    assert min(float(r["scores"].min()) for r in rows) < 0, "the case must hold negative scores"
+    assert check_topk_rows(g, rows, k) <= 2
+
+
 def test_index_topk_prefill_passes_integer_score_ties():
     # scores that are small integers (binary keys, one head): thousands of exact ties around the
     # k-th score (candidate buffers fill with equal keys); the result must be bit-exact
