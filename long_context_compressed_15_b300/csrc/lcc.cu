@@ -931,6 +931,7 @@ size_t tc_decode_ws(int B, int Tq, int H, int D, int64_t keys, int* nsplit_out, 
   const int64_t tiles = (keys + 127) / 128;
   const int64_t ctas = static_cast<int64_t>(B) * Tq;
   int64_t ns = (num_sms() + ctas - 1) / ctas;
+  if (ns > kCombineFirstSplits) ns = kCombineFirstSplits;  // the combine then needs one round of loads
   if (ns > tiles) ns = tiles;
   if (ns < 1) ns = 1;
   const int64_t tps = (tiles + ns - 1) / ns;

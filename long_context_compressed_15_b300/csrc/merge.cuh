@@ -78,6 +78,10 @@ __global__ void __launch_bounds__(256) k_merge(MergeArgs a) {
   if (a.lse_out && lane == 0) a.lse_out[row] = (L == -INFINITY) ? -INFINITY : L + logf(tot);
 }
 
+// Splits whose partial rows the combine requests together with the lse values
+// (one round of loads); decode calls split their keys at most this many ways.
+constexpr int kCombineFirstSplits = 24;
+
 // Reduction of `nsplit` key-range partials stored [nsplit][rows][D] and
 // [nsplit][rows] into O [rows][D] fp32 and/or out [rows][D] bf16, and lse
 // [rows] (each output optional).
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(256) k_split_combine(const float* __restrict__
   // the first CH splits' partial rows are requested together with every
   // split's lse (lane s holds splits s, s+32, ...): for up to CH splits the
   // reduction waits on one round of loads
-  constexpr int CH = 24;
+  constexpr int CH = kCombineFirstSplits;
   const float ls0 = lane < nsplit ? __ldg(lp + static_cast<int64_t>(lane) * rows + row) : -INFINITY;
   const int n0 = min(CH, nsplit);
   float x0[CH][PER];
