@@ -198,9 +198,16 @@ unsigned long long g_topk_cl_done = 0;
 // (measured on the 32 x 16384 decode batch: 31.7 us against 35.3 us per
 // step); longer rows come here, where reading ~k groups instead of the whole
 // row wins (262144-entry rows: the layer-pair step 86 us -> 68 us).
+// A call with few rows leaves most SMs idle: its rows take 1024-thread CTAs
+// (finer partitions for the threshold, twice the loads in flight), which
+// finish sooner (4 rows of 262160 entries: 56.2 -> 54.4 us per layer-pair
+// step); with many rows the 512-thread CTA is faster (32 rows of 65536: 70.0
+// against 72.1 us per step).
 constexpr int kGselNT = 512;
+constexpr int kGselNTFew = 1024;
+constexpr int kGselFewRows = 16;
 constexpr int kGselCap = 4096;
-unsigned long long g_topk_gsel_done = 0;
+unsigned long long g_topk_gsel_done[2] = {};
 size_t gsel_smem(int Ncap) { return static_cast<size_t>(((Ncap + 31) / 32 + 3) & ~3) * 8 + kGselCap * 8; }
 bool use_gsel(int Ncap, int k) { return k <= 256 && gsel_smem(Ncap) <= 200 * 1024; }
 
@@ -643,13 +650,14 @@ lcc_status run_index_topk(const lcc_bf16* qI, const float* w, int B, int Tq, int
     if (rows > 0x7FFFFFFF / 8) return fail(LCC_ERR_SHAPE, "top-k: %lld rows", static_cast<long long>(rows));
     const int cl = topk_cluster_ctas(Ncap, k, ta.gs);
     if (cl == 0 && use_gsel(Ncap, k)) {
-      auto kern = k_topk_gsel<kGselNT, kGselCap>;
+      const bool few = rows <= kGselFewRows;
+      auto kern = few ? k_topk_gsel<kGselNTFew, kGselCap> : k_topk_gsel<kGselNT, kGselCap>;
       const size_t smem = gsel_smem(Ncap);
       {
         std::lock_guard<std::mutex> lk(g_attr_mu);
-        if ((st = ensure_smem(kern, 200 * 1024, g_topk_gsel_done)) != LCC_OK) return st;
+        if ((st = ensure_smem(kern, 200 * 1024, g_topk_gsel_done[few])) != LCC_OK) return st;
       }
-      launch_k(kern, dim3(static_cast<unsigned>(rows)), dim3(kGselNT), smem, s, true, ta);
+      launch_k(kern, dim3(static_cast<unsigned>(rows)), dim3(few ? kGselNTFew : kGselNT), smem, s, true, ta);
       if ((st = launch_check("k_topk_gsel")) != LCC_OK) return st;
       continue;
     }
